@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark: constrained decode steps/s of the trie-constrained greedy decoder.
+
+Default workload: the large single-sequence head (vocab 151,936, hidden 2,048
+Gaussian bf16 tied embedding of 622 MB, the 42-tool catalog in constant
+memory, k = 5, batch 1), queries cycled from the 1,000-query set.
+
+One timed bench step = one tc_decode call: a captured CUDA graph that resets
+the batch and runs the constrained decode step (mask, sparse head, argmax,
+advance) until every sequence has stopped.  The reported value is decode
+steps per second: loop iterations, each one step of the whole batch.
+
+Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a
+barrier and torch.cuda.synchronize(); each step's device time is taken with
+CUDA events on the launching stream around the graph launch only; between
+steps (outside the events) the query's hidden states are copied into the
+graph's input buffer (device to device) and L2 is flushed by writing a 512 MiB
+buffer.  Max over ranks; ranks decode disjoint queries (weak scaling, no
+collective on the data path).
+
+Also printed: end-to-end rate through the same call with the inputs copied
+from pinned host memory and the results read back inside the timed region;
+the roofline of the step kernel (algorithmic bytes per launch over its
+per-launch CUDA-event time); the dense-head comparison; the oracle timed on
+the host cores; GPU clocks sampled during the timed region.
+
+`--impl reference` times the CPU oracle on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from trie_constrained_decoding_gb300 import inputs as I  # noqa: E402
+
+METRIC = "constrained decode steps/s"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="large_head", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--head", choices=["sparse", "dense"], default="sparse")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-extras", action="store_true", help="skip the dense/host-loop/e2e/roofline passes")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def read_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- helpers
+
+def query_ids(n_queries: int, rank: int, world: int, count: int):
+    return [(rank + world * i) % n_queries for i in range(count)]
+
+
+def host_hidden(w, qids):
+    """bf16 bits [len(qids), steps, batch, hidden] of the queries' hidden states."""
+    B = w.batch
+    uniq = sorted(set(qids))
+    start, stop = uniq[0], uniq[-1] + 1
+    all_h = w.hidden_states(start * B, (stop - start) * B)       # [S, (stop-start)*B, H]
+    S, _, H = all_h.shape
+    all_h = all_h.reshape(S, stop - start, B, H).transpose(1, 0, 2, 3)
+    return {q: np.ascontiguousarray(all_h[q - start]) for q in uniq}
+
+
+def oracle_baseline(w, seconds: float, head: str = "sparse"):
+    """Greedy decode with the oracle on the host, query by query, for about `seconds`."""
+    from oracle import decode as D
+    from oracle import grammar as G
+    trie = G.compile_catalog(w.catalog, w.sep_id, w.stop_id, w.vocab, max_fanout=w.max_fanout)
+    emb = w.embedding()
+    t0 = time.perf_counter()
+    steps = tokens = queries = 0
+    q = 0
+    hid_cache = None
+    while True:
+        if hid_cache is None or q % 64 == 0:
+            hid_cache = w.hidden_states(q * w.batch, 64 * w.batch)
+        base = (q % 64) * w.batch
+        t_start = time.perf_counter()
+        lens = []
+        for b in range(w.batch):
+            toks, _, _ = D.greedy_decode(trie, w.k, emb, hid_cache[:, base + b], w.max_steps, head=head)
+            lens.append(len(toks))
+        tokens += sum(lens)
+        steps += max(lens)
+        queries += 1
+        q = (q + 1) % max(1, w.n_queries // w.batch)
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": steps / dt, "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "tokens_per_s": tokens / dt, "seconds": round(dt, 3),
+            "sample": f"{queries} query batches of '{w.name}' (batch {w.batch}), decoded in order by the "
+                      f"fp64 oracle ({head} head), single process"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = I.WORKLOADS[args.workload]()
+    # Each bench step decodes one query batch with the oracle; bounded so that
+    # warm-up + steps finish within a few minutes.
+    budget = min(120.0, max(5.0, 0.05 * (args.steps + args.warmup)))
+    base = oracle_baseline(w, budget, head="sparse")
+    line = {"metric": METRIC, "value": base["value"], "unit": "steps/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / base["value"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "batch": w.batch, "k": w.k, "vocab": w.vocab, "hidden": w.hidden,
+                       "catalog": len(w.catalog), "note": "CPU oracle (plain Python + numpy fp64)"},
+            "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": base["value"], "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    from trie_constrained_decoding_gb300 import binding as tcd
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    stream = torch.cuda.current_stream()
+    w = I.WORKLOADS[args.workload]()
+    head = tcd.HEAD_SPARSE if args.head == "sparse" else tcd.HEAD_DENSE
+    B, S, H = w.batch, w.max_steps, w.hidden
+
+    emb_bits = w.embedding()
+    emb = torch.from_numpy(emb_bits.view(np.int16)).to(f"cuda:{dev}").view(torch.bfloat16)
+    del emb_bits
+    trie = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
+    tinfo = trie.info()
+    ctx = tcd.Context(emb, max_batch=B, cand_cap=w.cand_cap)
+    res = {"const": tcd.RES_CONST, "global": tcd.RES_GLOBAL, "auto": tcd.RES_AUTO}[w.residency]
+    ctx.bind(trie, res)
+
+    n_batches = max(1, w.n_queries // B)
+    K, W = args.steps, args.warmup
+    qids = query_ids(n_batches, rank, world, K + W)
+    hh = host_hidden(w, qids)
+    dev_hidden = {q: torch.from_numpy(h.view(np.int16)).to(f"cuda:{dev}").view(torch.bfloat16)
+                  for q, h in hh.items()}
+    hid_buf = torch.empty((S, B, H), dtype=torch.bfloat16, device=f"cuda:{dev}")
+    toks = torch.empty((B, S), dtype=torch.int32, device=f"cuda:{dev}")
+    logits = torch.empty((B, S), dtype=torch.float32, device=f"cuda:{dev}")
+    lens = torch.empty(B, dtype=torch.int32, device=f"cuda:{dev}")
+    status = torch.empty(B, dtype=torch.int32, device=f"cuda:{dev}")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{dev}")
+
+    def decode_one(q, ev=None):
+        hid_buf.copy_(dev_hidden[q])
+        flush.zero_()
+        if ev is not None:
+            ev[0].record(stream)
+        ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(W):
+        decode_one(qids[i])
+    torch.cuda.synchronize()
+    ctx.raise_on_error()
+    ctx.stats(reset=True)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        decode_one(qids[W + i], evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    dev_ms = sum(a.elapsed_time(b) for a, b in evs)
+    st = ctx.stats(reset=True)
+    ctx.raise_on_error()
+    decode_steps = st["step_launches"]
+    tokens = st["seq_steps"]
+    gpu_launches = st["step_launches"] + st["reset_launches"]
+
+    tot = torch.tensor([dev_ms, float(decode_steps), float(tokens)], dtype=torch.float64, device=f"cuda:{dev}")
+    if dist:
+        t_max = tot[0:1].clone()
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+        sums = tot[1:3].clone()
+        dist.all_reduce(sums, op=dist.ReduceOp.SUM)
+        dev_ms_max, all_steps, all_tokens = float(t_max[0]), float(sums[0]), float(sums[1])
+    else:
+        dev_ms_max, all_steps, all_tokens = dev_ms, float(decode_steps), float(tokens)
+    value = all_steps / (dev_ms_max / 1000.0)
+
+    extras = {}
+    e2e = None
+    roof = None
+    if not args.no_extras:
+        roof, extras = extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids[W:], head, flush,
+                                    hid_buf, toks, logits, lens, status)
+        e2e = extras.pop("e2e")
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = read_peaks()
+    if roof is not None:
+        roof["peak"] = peak
+        roof["frac"] = roof["achieved"] / peak
+        roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if peak_kind == "measured" \
+            else "fallback 6.8 TB/s"
+    cpu = None
+    if world == 1 and not args.no_extras:
+        cpu = oracle_baseline(w, args.cpu_seconds)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": dev_ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 x bf16 -> fp32 accumulate", "data": "synthetic (seeded; no dataset or weights)",
+        "config": {"workload": w.name, "batch": B, "k": w.k, "vocab": w.vocab, "hidden": H,
+                   "catalog_strings": len(w.catalog), "trie_nodes": tinfo["n_nodes"], "trie_edges": tinfo["n_edges"],
+                   "max_fanout": tinfo["max_fanout"], "residency": ["auto", "const", "global"][ctx.residency()],
+                   "head": args.head, "bench_step": "one tc_decode graph launch decoding one query batch to the end",
+                   "decode_steps_per_bench_step": all_steps / (K * world),
+                   "tokens_per_s": all_tokens / (dev_ms_max / 1000.0),
+                   "l2": "flushed between timed steps (512 MiB write outside the CUDA events)",
+                   "wall_s_timed_region": round(t_wall, 3)},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if roof is not None:
+        line["roofline"] = roof
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    line["variants"] = extras
+    print(json.dumps(line))
+    ctx.close()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, head, flush, hid_buf, toks, logits,
+                 lens, status):
+    """Roofline of the step kernel, dense-head comparison, host loop and end-to-end rate."""
+    B, S, H = w.batch, w.max_steps, w.hidden
+    out = {}
+    n_roof = min(len(qids), 200 if B == 1 else 8)
+
+    # --- step kernel alone: tc_step (same kernel body, host-argument form), one
+    # event pair per launch; L2 flushed before every launch (cold) or not (warm).
+    tok = torch.empty(B, dtype=torch.int32, device=f"cuda:{dev}")
+    lg = torch.empty(B, dtype=torch.float32, device=f"cuda:{dev}")
+    stt = torch.empty(B, dtype=torch.int32, device=f"cuda:{dev}")
+
+    # steps each query needs (the graph loop's own count), so the step loop runs exactly those
+    n_steps = {}
+    for q in qids[:n_roof]:
+        hid_buf.copy_(dev_hidden[q])
+        ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head)
+        n_steps[q] = int(lens.max().item())
+
+    def kernel_pass(cold: bool):
+        pairs = []
+        for q in qids[:n_roof]:
+            hid_buf.copy_(dev_hidden[q])
+            ctx.reset(B, w.k)
+            for t in range(n_steps[q]):
+                if cold:
+                    flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                ctx.step(hid_buf[t], tok, lg, stt, head=head)
+                b.record(stream)
+                pairs.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in pairs]
+
+    ctx.stats(reset=True)
+    cold_ms = kernel_pass(True)
+    st = ctx.stats(reset=True)
+    launches = len(cold_ms)
+    seq_steps = float(st["seq_steps"])
+    cand_rows = float(st["cand_rows"])
+    algo_bytes = cand_rows * 2 * H + seq_steps * 2 * H    # embedding rows gathered + hidden states read
+    mean_ms = sum(cold_ms) / launches
+    achieved = algo_bytes / launches / (mean_ms / 1000.0) / 1e9
+    warm_ms = kernel_pass(False)
+    warm_mean = sum(warm_ms) / len(warm_ms)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": None, "unit": "GB/s", "frac": None, "traffic": None,
+            "kernel": "sparse_step_kernel" if head == tcd.HEAD_SPARSE else "dense_step_kernel",
+            "algorithmic_bytes_per_launch": algo_bytes / launches,
+            "mean_launch_us_cold_l2": mean_ms * 1000.0, "mean_launch_us_warm_l2": warm_mean * 1000.0,
+            "achieved_warm_gbs": algo_bytes / launches / (warm_mean / 1000.0) / 1e9,
+            "candidates_per_sequence_step": cand_rows / max(1.0, seq_steps),
+            "launches_timed": launches,
+            "note": "per-launch CUDA events around tc_step (same kernel body as the graph loop); "
+                    "bytes = candidate rows x 2H + hidden state 2H per sequence step"}
+
+    # --- dense head + mask over the same queries (subset)
+    if head == tcd.HEAD_SPARSE:
+        n_dense = min(len(qids), 20 if B == 1 else 2)
+        ctx.stats(reset=True)
+        evs = []
+        for q in qids[:n_dense]:
+            hid_buf.copy_(dev_hidden[q])
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=tcd.HEAD_DENSE)
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        st = ctx.stats(reset=True)
+        ms = sum(a.elapsed_time(b) for a, b in evs)
+        out["dense_head_steps_per_s"] = st["step_launches"] / (ms / 1000.0)
+        out["dense_head_gbs"] = st["seq_steps"] * (w.vocab * 2.0 * H) / (ms / 1000.0) / 1e9
+
+    # --- host-driven loop (one synchronising read per step) over a subset
+    n_host = min(len(qids), 100 if B == 1 else 4)
+    ctx.stats(reset=True)
+    t0 = time.perf_counter()
+    for q in qids[:n_host]:
+        hid_buf.copy_(dev_hidden[q])
+        ctx.decode_host(hid_buf, w.k, S, toks, logits, lens, status, head=head)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    st = ctx.stats(reset=True)
+    out["host_loop_steps_per_s_wall"] = st["step_launches"] / dt
+
+    # --- end to end through the C ABI with host buffers
+    n_e2e = min(len(qids), 500 if B == 1 else 8)
+    pin_h = {q: torch.from_numpy(hh[q].view(np.int16)).view(torch.bfloat16).pin_memory() for q in qids[:n_e2e]}
+    pt = torch.empty((B, S), dtype=torch.int32).pin_memory()
+    pl = torch.empty((B, S), dtype=torch.float32).pin_memory()
+    pn = torch.empty(B, dtype=torch.int32).pin_memory()
+    ps = torch.empty(B, dtype=torch.int32).pin_memory()
+    ctx.stats(reset=True)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for q in qids[:n_e2e]:
+        hid_buf.copy_(pin_h[q], non_blocking=True)
+        ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head)
+        pt.copy_(toks, non_blocking=True)
+        pl.copy_(logits, non_blocking=True)
+        pn.copy_(lens, non_blocking=True)
+        ps.copy_(status, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    st = ctx.stats(reset=True)
+    h2d = S * B * H * 2
+    d2h = B * S * 8 + B * 8
+    out["e2e"] = {"value": st["step_launches"] / (ms / 1000.0), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h,
+                  "note": "per bench step: pinned H2D of the query's hidden states, tc_decode, D2H of "
+                          "tokens/logits/lengths/status; CUDA events around the whole sequence, L2 not flushed"}
+    return roof, out
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,293 @@
+/*
+ * tcd.h - C ABI of the trie-constrained greedy decoder for GB300 (sm_103a).
+ *
+ * The decoder emits exactly k distinct pointers from a finite catalog of
+ * token-id strings, separated by a separator token and ended by a stop
+ * token, choosing each token greedily by a tied-embedding logit over the
+ * legal set only.  It follows "Constraint made cheaper than no constraint"
+ * (coreyjames.ai), sections "The grammar as a trie over tokens", "Masked
+ * sampling inside the sampler", "The sparse output layer" and "The whole loop
+ * on the device"; the legal set is the next-token mask of "GLRMask"
+ * (introduction) for that finite language.
+ *
+ * Conventions for every call:
+ *  - Pointers marked (host) are CPU memory, (device) are CUDA device memory of
+ *    the context's device.  bf16 values are 16-bit IEEE bfloat16 bit patterns.
+ *  - The caller owns every buffer it passes; the library never frees them and
+ *    never keeps a host pointer past the call.  Device buffers passed to
+ *    tc_decode / tc_decode_graph_create are remembered by the captured graph
+ *    and must stay valid while that graph may be launched.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    that take a stream are asynchronous with respect to the host unless
+ *    stated otherwise.
+ *  - Argument and compile errors are returned synchronously and leave the
+ *    objects unchanged.  Errors found on the device (an empty legal set, a
+ *    winner on a dead edge, an index out of range, running out of steps) are
+ *    recorded per sequence, stop that sequence only, and are read with
+ *    tc_first_error / tc_read_seq_state or the status outputs.
+ *  - The library is not thread-safe per object: one host thread at a time
+ *    per tc_ctx.  Constant-memory residency is one image per device (see
+ *    tc_bind_grammar).
+ */
+#ifndef TCD_H
+#define TCD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tc_status {
+  TC_OK = 0,
+  TC_ERR_INVALID_ARG = 1,        /* bad pointer, size or enum value */
+  TC_ERR_FANOUT = 2,             /* a node has more edges than max_fanout (control edges count) */
+  TC_ERR_DUPLICATE = 3,          /* two catalog strings are equal */
+  TC_ERR_CONTROL_COLLISION = 4,  /* a catalog string contains the separator or stop id */
+  TC_ERR_TOKEN_RANGE = 5,        /* a token id outside [0, vocab) */
+  TC_ERR_EMPTY_STRING = 6,       /* a catalog string has no tokens */
+  TC_ERR_K_RANGE = 7,            /* k < 1 or k > number of catalog strings */
+  TC_ERR_CONST_CAPACITY = 8,     /* constant residency requested but the walk image does not fit */
+  TC_ERR_NOT_BOUND = 9,          /* no grammar bound, or no tc_reset since binding */
+  TC_ERR_CAPACITY = 10,          /* batch > max_batch or max fan-out > the candidate buffer */
+  TC_ERR_UNSUPPORTED = 11,       /* shape the kernels do not handle (e.g. hidden % 8 != 0) */
+  TC_ERR_EMPTY_MASK = 16,        /* device: no legal token at a step */
+  TC_ERR_NO_LIVE_EDGE = 17,      /* device: the chosen token sits on no live edge (defensive) */
+  TC_ERR_MAX_STEPS = 18,         /* device: the step budget ran out before the stop token */
+  TC_ERR_BOUNDS = 19,            /* device: an index of the grammar image or a logit is invalid */
+  TC_ERR_CUDA = 32,              /* a CUDA runtime call failed (see tc_last_error_message) */
+  TC_ERR_OOM = 33                /* device allocation failed */
+} tc_status;
+
+/* Grammar residency (tc_bind_grammar). */
+enum {
+  TC_RES_AUTO = 0,    /* constant memory when the walk image fits, else global memory */
+  TC_RES_CONST = 1,   /* walk image in __constant__ memory (at most TC_CONST_CAPACITY_BYTES) */
+  TC_RES_GLOBAL = 2   /* walk image in global memory, read through the read-only cache */
+};
+
+/* Output head (tc_step / tc_decode). */
+enum {
+  TC_HEAD_SPARSE = 0,     /* one embedding-row dot product per legal candidate */
+  TC_HEAD_DENSE = 1       /* every vocabulary row, then the legal mask, then the argmax (cross-check) */
+};
+
+/* Bytes of __constant__ memory reserved for one walk image. */
+#define TC_CONST_CAPACITY_BYTES (63 * 1024)
+
+typedef struct tc_trie tc_trie;   /* compiled catalog, host object */
+typedef struct tc_ctx tc_ctx;     /* device context: model, bound grammar, per-sequence state */
+typedef struct tc_graph tc_graph; /* a captured device-resident decode loop */
+
+typedef struct tc_trie_info_t {
+  int32_t n_nodes;          /* N, root is node 0, nodes numbered in breadth-first order */
+  int32_t n_edges;          /* E, token edges plus two control edges per terminal node */
+  int32_t n_strings;        /* K, catalog size (pointer ids 0..K-1 in input order) */
+  int32_t max_fanout;       /* largest edge count of any node (control edges included) */
+  int32_t root_fanout;      /* edge count of the root */
+  int32_t max_depth;        /* longest catalog string, in tokens */
+  int32_t vocab, sep_id, stop_id;
+  int32_t reserved;
+  int64_t total_tokens;     /* sum of the string lengths */
+  int64_t walk_image_bytes; /* bytes of the device walk image (node ranges, edges, node pointer ids) */
+} tc_trie_info_t;
+
+/* ---------------------------------------------------------------- compiler */
+
+/*
+ * tc_compile_trie - compile a catalog of token-id strings into a CSR trie
+ * ("The grammar as a trie over tokens": an edge range per node, a token and a
+ * child per edge, and two sentinel children for the control edges).
+ *
+ *  ids        (host) int32[offsets[n_strings]]: the strings, concatenated.
+ *  offsets    (host) int64[n_strings + 1]: string i is ids[offsets[i] .. offsets[i+1]).
+ *  n_strings  K >= 1.  String i becomes pointer id i.
+ *  sep_id, stop_id  distinct ids in [0, vocab) used for the two control edges.
+ *  vocab      token ids must lie in [0, vocab).
+ *  max_fanout refuse any node with more edges than this (the page's cap is
+ *             256; control edges count).  Must be >= 2.
+ *  out        receives a new tc_trie the caller frees with tc_trie_free.
+ *
+ * Refusals (nothing is allocated): TC_ERR_EMPTY_STRING, TC_ERR_DUPLICATE,
+ * TC_ERR_CONTROL_COLLISION, TC_ERR_TOKEN_RANGE, TC_ERR_FANOUT,
+ * TC_ERR_INVALID_ARG.  Host only; needs no GPU.
+ */
+tc_status tc_compile_trie(const int32_t* ids, const int64_t* offsets, int32_t n_strings,
+                          int32_t sep_id, int32_t stop_id, int32_t vocab, int32_t max_fanout,
+                          tc_trie** out);
+
+/* tc_trie_info - sizes of a compiled trie into *out (host). */
+tc_status tc_trie_info(const tc_trie* trie, tc_trie_info_t* out);
+
+/*
+ * tc_trie_export - copy the CSR arrays into caller buffers (host), any of
+ * which may be NULL.  Sizes from tc_trie_info:
+ *  node_begin  int32[N+1]  edges of node n are [node_begin[n], node_begin[n+1])
+ *  edge_tok    int32[E]    token of each edge; a node's edges ascend by token
+ *  edge_child  int32[E]    child node, or -1 for the separator edge (back to
+ *                          the root), -2 for the stop edge
+ *  node_ptr    int32[N]    pointer id ending at the node, or -1
+ *  static_cnt  int32[E]    pointers ending at or below a token edge's child;
+ *                          0 on control edges
+ *  path_off    int32[K+1]  pointer p's root-to-terminal token edges are
+ *  path        int32[total_tokens]   path[path_off[p] .. path_off[p+1])
+ */
+tc_status tc_trie_export(const tc_trie* trie, int32_t* node_begin, int32_t* edge_tok,
+                         int32_t* edge_child, int32_t* node_ptr, int32_t* static_cnt,
+                         int32_t* path_off, int32_t* path);
+
+void tc_trie_free(tc_trie* trie);
+
+/* --------------------------------------------------------------- context */
+
+/*
+ * tc_ctx_create - a decoding context on `device` over a tied embedding.
+ *
+ *  emb_bf16   (device) bf16[vocab, hidden], row-major, 16-byte aligned; the
+ *             caller keeps it alive and unchanged while the context is used.
+ *  vocab      V >= 2.   hidden  H >= 8 and a multiple of 8.
+ *  max_batch  largest batch passed to tc_reset / tc_decode (>= 1).
+ *  cand_cap   candidate-buffer capacity C: grammars whose max fan-out exceeds
+ *             it are refused at bind (256 for the page's cap; up to 4096).
+ *
+ * Allocates the context's device scratch (O(max_batch * cand_cap) bytes).
+ */
+tc_status tc_ctx_create(int32_t device, const void* emb_bf16, int32_t vocab, int32_t hidden,
+                        int32_t max_batch, int32_t cand_cap, tc_ctx** out);
+
+/* tc_ctx_destroy - synchronise the device, free every graph, grammar image and buffer. */
+void tc_ctx_destroy(tc_ctx* ctx);
+
+/*
+ * tc_bind_grammar - make `trie` the context's grammar ("The grammar as a trie
+ * over tokens": constant residency is owned by one grammar and re-bound on
+ * every switch; a captured graph re-binds at launch).
+ *
+ * Uploads the trie's image to device memory owned by the context (once per
+ * distinct trie content; the trie may be freed afterwards) and allocates its
+ * per-sequence state for max_batch sequences.  residency is TC_RES_AUTO,
+ * TC_RES_CONST or TC_RES_GLOBAL; AUTO picks CONST when the walk image is at
+ * most TC_CONST_CAPACITY_BYTES.  With CONST the image is copied into the
+ * device's __constant__ bank on `stream` now, before any later tc_step, and
+ * as the first node of any graph captured for it.  There is one constant
+ * image per device: contexts that use different CONST grammars on
+ * concurrently running streams race; use GLOBAL for that.
+ *
+ * Errors: TC_ERR_TOKEN_RANGE (trie vocab > context vocab), TC_ERR_CAPACITY
+ * (max fan-out > cand_cap), TC_ERR_CONST_CAPACITY, TC_ERR_OOM, TC_ERR_CUDA.
+ * Binding invalidates the per-sequence state: call tc_reset before tc_step.
+ */
+tc_status tc_bind_grammar(tc_ctx* ctx, const tc_trie* trie, int32_t residency, void* stream);
+
+/* tc_bound_residency - the residency the bound grammar resolved to (TC_RES_CONST / TC_RES_GLOBAL). */
+tc_status tc_bound_residency(const tc_ctx* ctx, int32_t* residency);
+
+/*
+ * tc_reset - start `batch` sequences, each owing exactly k pointers, at the
+ * root of the bound grammar (live counts copied from the static counts,
+ * spent flags cleared).  1 <= batch <= max_batch; 1 <= k <= K (a larger k
+ * would make the language empty; TC_ERR_K_RANGE).  Asynchronous on `stream`.
+ */
+tc_status tc_reset(tc_ctx* ctx, int32_t batch, int32_t k, void* stream);
+
+/*
+ * tc_step - one decode step of every sequence of the last tc_reset, driven
+ * from the host ("Masked sampling inside the sampler"): mask the current
+ * node's edges, one logit per legal token (head = TC_HEAD_SPARSE) or every
+ * vocabulary logit then the mask (TC_HEAD_DENSE), argmax with ties to the
+ * lower token id, advance the trie, and on a completed pointer decrement the
+ * live counts along its path.
+ *
+ *  hidden_bf16 (device) bf16[batch, hidden]: this step's hidden state per sequence.
+ *  tok_out     (device) int32[batch]: the emitted token, or -1 for a sequence
+ *              that had already stopped or failed.
+ *  logit_out   (device) float[batch]: its fp32 logit (0 for -1 tokens); may be NULL.
+ *  status_out  (device) int32[batch]: TC_OK or the sequence's error; may be NULL.
+ *
+ * Asynchronous on `stream`; a sequence that meets an error stops there.
+ */
+tc_status tc_step(tc_ctx* ctx, const void* hidden_bf16, int32_t head, int32_t* tok_out,
+                  float* logit_out, int32_t* status_out, void* stream);
+
+/*
+ * tc_decode - decode `batch` sequences to completion in one device-resident
+ * graph ("The whole loop on the device": [re-bind] -> reset -> while (a
+ * sequence is live and step < max_steps) { step }, the step counter kept in
+ * device memory).  The graph is captured on first use for each distinct
+ * argument set and replayed afterwards.
+ *
+ *  hidden_steps_bf16 (device) bf16[n_steps, batch, hidden]: step t of sequence
+ *              b reads hidden_steps[t, b, :].
+ *  n_steps     rows available in hidden_steps; 1 <= max_steps <= n_steps.
+ *  toks        (device) int32[batch, max_steps]: emitted tokens, -1 after the end.
+ *  logits      (device) float[batch, max_steps]: their logits, 0 after the end.
+ *  lens        (device) int32[batch]: tokens emitted per sequence.
+ *  status      (device) int32[batch]: TC_OK (stopped normally) or the error
+ *              (TC_ERR_MAX_STEPS when the budget ran out).
+ *
+ * Asynchronous on `stream`; the host need not synchronise until it reads the
+ * outputs.  Leaves the context's sequences in their final state.
+ */
+tc_status tc_decode(tc_ctx* ctx, const void* hidden_steps_bf16, int32_t n_steps, int32_t batch,
+                    int32_t k, int32_t max_steps, int32_t head, int32_t* toks, float* logits,
+                    int32_t* lens, int32_t* status, void* stream);
+
+/*
+ * tc_decode_host - the same decode driven from the host: tc_reset, then one
+ * tc_step per step with a synchronising read of the live count after each,
+ * the comparison loop of "The whole loop on the device".  Same arguments and
+ * outputs as tc_decode.  Synchronous.
+ */
+tc_status tc_decode_host(tc_ctx* ctx, const void* hidden_steps_bf16, int32_t n_steps, int32_t batch,
+                         int32_t k, int32_t max_steps, int32_t head, int32_t* toks, float* logits,
+                         int32_t* lens, int32_t* status, void* stream);
+
+/*
+ * tc_decode_graph_create - capture the tc_decode graph for these arguments
+ * without launching it; the caller launches it with tc_graph_launch and frees
+ * it with tc_graph_destroy (before tc_ctx_destroy).  The graph keeps using the
+ * grammar bound now, even after another grammar is bound: its first node
+ * re-binds that grammar's constant image.
+ */
+tc_status tc_decode_graph_create(tc_ctx* ctx, const void* hidden_steps_bf16, int32_t n_steps,
+                                 int32_t batch, int32_t k, int32_t max_steps, int32_t head,
+                                 int32_t* toks, float* logits, int32_t* lens, int32_t* status,
+                                 tc_graph** out);
+tc_status tc_graph_launch(tc_graph* graph, void* stream);
+void tc_graph_destroy(tc_graph* graph);
+
+/*
+ * tc_first_error - synchronise `stream`, then report the lowest sequence
+ * index whose status is not TC_OK (*seq = -1, *code = TC_OK if none).
+ */
+tc_status tc_first_error(tc_ctx* ctx, void* stream, int32_t* seq, int32_t* code);
+
+/*
+ * tc_read_seq_state - synchronise `stream` and copy per-sequence state of the
+ * last reset's batch into host arrays int32[batch] (any may be NULL): current
+ * node, pointers completed, tokens emitted, status, done flag.
+ */
+tc_status tc_read_seq_state(tc_ctx* ctx, void* stream, int32_t* node, int32_t* emitted,
+                            int32_t* len, int32_t* status, int32_t* done);
+
+/*
+ * tc_read_stats - synchronise `stream` and copy the context's cumulative
+ * kernel counters into out (host) int64[4]: step-kernel launches, sequence
+ * steps (one per live sequence per step), legal candidates evaluated (rows
+ * gathered by the sparse head), reset-kernel launches.  reset != 0 zeroes
+ * them afterwards.  Used to count launches and algorithmic bytes.
+ */
+tc_status tc_read_stats(tc_ctx* ctx, void* stream, int64_t* out, int32_t reset);
+
+/* tc_status_str - a static name for a status code. */
+const char* tc_status_str(tc_status status);
+
+/* tc_last_error_message - detail of the last error on this host thread (static storage). */
+const char* tc_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCD_H */

@@ -13,3 +13,12 @@ def pytest_configure(config):
 
 
 GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def tcd():
+    """The C-ABI binding over a freshly built libtcd.so (builds if stale)."""
+    from trie_constrained_decoding_gb300 import build
+    build.build()
+    from trie_constrained_decoding_gb300 import binding
+    return binding

@@ -1,0 +1,116 @@
+// Host-visible parameter blocks and launchers of the decode-step kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tcd {
+
+constexpr int kThreads = 256;          // threads per CTA of every step kernel (8 warps)
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxTiles = 1024;        // upper bound of CTAs per sequence (partials per sequence)
+constexpr int kMaxHidden = 16384;
+constexpr int kMaxCandCap = 4096;
+// Dynamic shared memory a step kernel may request: x staged for the generic
+// hidden size plus two int32 candidate lists of up to kMaxCandCap entries.
+constexpr int kMaxDynamicSmem = kMaxHidden * 2 + 2 * kMaxCandCap * 4;
+
+// Per-sequence decode state (device memory, one record per sequence).
+struct SeqState {
+  int32_t node;     // current trie node
+  int32_t emitted;  // pointers completed so far (j)
+  int32_t len;      // tokens emitted so far
+  int32_t status;   // TC_OK or the error that stopped the sequence
+  int32_t done;     // 1 once the stop token was emitted or an error occurred
+  int32_t k;        // pointers owed in total
+  int32_t pad0, pad1;
+};
+
+// One CTA's best candidate, handed to the sequence's last CTA.
+struct Partial {
+  float logit;
+  int32_t tok;
+  int32_t edge;
+  int32_t pad;
+};
+
+// Device control block of the device-resident loop.
+struct Ctrl {
+  int32_t step;       // loop iteration being run
+  int32_t live;       // sequences neither stopped nor failed
+  int32_t max_steps;  // step budget
+  uint32_t ticket;    // CTAs of the current launch that have finished
+  int32_t pad[4];
+};
+
+// The bound grammar as the kernels see it.
+struct GrammarView {
+  const int32_t* img;        // walk image in global memory (also the source of the constant copy)
+  int32_t off_edges, off_ptr;
+  int32_t n_nodes, n_edges, n_strings;
+  const int32_t* static_cnt; // [E]
+  const int32_t* path_off;   // [K+1]
+  const int32_t* path;       // [total tokens]
+};
+
+struct StepParams {
+  GrammarView g;
+  const uint16_t* emb;      // bf16 [V, H]
+  int32_t V, H;
+  const uint16_t* hidden;   // bf16 [B, H] (host form) or [S, B, H] (device form)
+  SeqState* st;             // [B]
+  int32_t* cnt;             // [B, E] live-pointer counts
+  uint32_t* spent;          // [B, kw] spent flags
+  int32_t kw;               // words of spent flags per sequence
+  int32_t B;
+  int32_t cand_cap;         // C
+  Partial* part;            // [B, tiles]
+  uint32_t* seq_ticket;     // [B]
+  Ctrl* ctrl;               // control block (host form: only `live` is maintained)
+  int32_t* tok_out;         // host form: [b * out_stride]; device form: toks[b * out_stride + len]
+  float* logit_out;         // same indexing as tok_out (may be null in host form)
+  int32_t* status_out;      // [B] or null
+  int32_t* lens_out;        // [B] or null
+  int32_t out_stride;
+  unsigned long long cond;  // cudaGraphConditionalHandle of the loop (device form)
+  int32_t device_form;      // 1: hidden and output position come from the control block
+  unsigned long long* stats;  // optional counters, see StatSlot
+};
+
+// Cumulative counters kept by the kernels (one atomic per launch / per sequence step).
+enum StatSlot { kStatStepLaunches = 0, kStatSeqSteps = 1, kStatCandRows = 2, kStatResetLaunches = 3, kStatSlots = 4 };
+
+struct ResetParams {
+  GrammarView g;
+  SeqState* st;
+  int32_t* cnt;
+  uint32_t* spent;
+  int32_t kw;
+  int32_t B, k, max_steps;
+  uint32_t* seq_ticket;
+  Ctrl* ctrl;
+  int32_t* toks;            // optional [B, max_steps] prefill with -1
+  float* logits;            // optional [B, max_steps] prefill with 0
+  int32_t* lens_out;        // optional
+  int32_t* status_out;      // optional
+  unsigned long long cond;  // 0: none
+  unsigned long long* stats;
+};
+
+enum Head { kHeadSparse = 0, kHeadDense = 1 };
+
+// Number of CTAs per sequence the sparse step uses for a grammar of the given
+// largest fan-out at batch B, and the dense step's CTAs per sequence.
+int sparse_tiles(int max_fanout, int B, int num_sms);
+int dense_tiles(int B, int num_sms);
+
+// Opt the step kernels in to kMaxDynamicSmem bytes of dynamic shared memory
+// (current device; call once per device before the first launch or capture).
+cudaError_t prepare_kernels();
+cudaError_t launch_reset(const ResetParams& r, cudaStream_t s);
+cudaError_t launch_step(const StepParams& p, bool const_resident, int head, int tiles, cudaStream_t s);
+cudaError_t launch_finalize(const StepParams& p, cudaStream_t s);
+// Copy a walk image (device memory) into the constant bank, stream-ordered.
+cudaError_t const_upload(const void* d_src, size_t bytes, cudaStream_t s);
+
+}  // namespace tcd

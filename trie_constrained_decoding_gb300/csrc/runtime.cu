@@ -1,0 +1,660 @@
+// Runtime behind the C ABI: contexts, grammar residency, per-sequence state,
+// host-driven steps and the device-resident decode loop (CUDA graph with a
+// conditional WHILE node).
+//
+// "Constraint made cheaper than no constraint", section "The grammar as a
+// trie over tokens": constant residency is owned by one grammar and re-bound
+// on every switch, and a captured graph re-binds at launch because replay
+// does not repeat the host upload.  Here the owner of the device's constant
+// bank is tracked per device; a host-driven step re-copies the bound image
+// when another grammar owns the bank, and every captured graph starts with a
+// device-to-device copy node of its own grammar's image.
+//
+// Section "The whole loop on the device": the loop is one captured graph - a
+// reset, then a conditional body that runs the step while the predicate
+// holds - with every loop-varying value (step, live count) in device memory;
+// the kernels have a host-argument form (tc_step) and a device-pointer form
+// (the graph body) sharing one body.  "Understanding Inference for Systems
+// Engineers", section 6.2, makes the same choice: a small control block in
+// device memory so that the graph is captured once and replayed unchanged.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "tcd.h"
+#include "tcd_internal.h"
+
+using namespace tcd;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kGraphCacheSize = 16;
+
+std::mutex g_const_mu;
+const void* g_const_owner[kMaxDevices];  // grammar whose image the constant bank holds
+
+tc_status cuda_fail(cudaError_t e, const char* what) {
+  set_error_message(std::string(what) + ": " + cudaGetErrorString(e));
+  cudaGetLastError();  // clear a sticky-free error so later calls start clean
+  return e == cudaErrorMemoryAllocation ? TC_ERR_OOM : TC_ERR_CUDA;
+}
+
+#define TC_CUDA(call)                                      \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);    \
+  } while (0)
+
+bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+// A grammar resident on the device, with the per-sequence state of its batch.
+struct DevGrammar {
+  uint64_t hash = 0;
+  int32_t residency = TC_RES_GLOBAL;  // resolved: CONST or GLOBAL
+  int32_t n_nodes = 0, n_edges = 0, n_strings = 0, max_fanout = 0, max_depth = 0;
+  WalkLayout layout{};
+  int32_t* d_img = nullptr;
+  int32_t* d_static_cnt = nullptr;
+  int32_t* d_path_off = nullptr;
+  int32_t* d_path = nullptr;
+  SeqState* d_st = nullptr;
+  int32_t* d_cnt = nullptr;
+  uint32_t* d_spent = nullptr;
+  int32_t kw = 1;
+  int32_t batch = 0, k = 0;  // of the last reset (0: none)
+
+  GrammarView view() const {
+    GrammarView v;
+    v.img = d_img;
+    v.off_edges = layout.off_edges;
+    v.off_ptr = layout.off_ptr;
+    v.n_nodes = n_nodes;
+    v.n_edges = n_edges;
+    v.n_strings = n_strings;
+    v.static_cnt = d_static_cnt;
+    v.path_off = d_path_off;
+    v.path = d_path;
+    return v;
+  }
+  void release() {
+    cudaFree(d_img);
+    cudaFree(d_static_cnt);
+    cudaFree(d_path_off);
+    cudaFree(d_path);
+    cudaFree(d_st);
+    cudaFree(d_cnt);
+    cudaFree(d_spent);
+  }
+};
+
+struct GraphKey {
+  const DevGrammar* g;
+  const void* hidden;
+  int32_t n_steps, batch, k, max_steps, head;
+  void *toks, *logits, *lens, *status;
+  bool operator==(const GraphKey& o) const {
+    return g == o.g && hidden == o.hidden && n_steps == o.n_steps && batch == o.batch && k == o.k &&
+           max_steps == o.max_steps && head == o.head && toks == o.toks && logits == o.logits &&
+           lens == o.lens && status == o.status;
+  }
+};
+
+struct tc_graph {
+  tc_ctx* ctx = nullptr;
+  DevGrammar* g = nullptr;
+  GraphKey key{};
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  bool cached = false;  // owned by the context's cache
+};
+
+struct tc_ctx {
+  int device = 0;
+  int num_sms = 148;
+  const uint16_t* emb = nullptr;
+  int32_t V = 0, H = 0, max_batch = 0, cand_cap = 0;
+  std::vector<DevGrammar*> grammars;
+  DevGrammar* bound = nullptr;
+  Partial* d_part = nullptr;
+  uint32_t* d_seq_ticket = nullptr;
+  Ctrl* d_ctrl = nullptr;
+  unsigned long long* d_stats = nullptr;
+  int32_t* h_live = nullptr;  // pinned
+  cudaStream_t capture_stream = nullptr;
+  std::vector<tc_graph*> cache;  // most recently used last
+  std::vector<tc_graph*> owned;  // created by tc_decode_graph_create
+};
+
+namespace {
+
+int tiles_for(const tc_ctx* c, const DevGrammar* g, int head, int B) {
+  return head == TC_HEAD_SPARSE ? sparse_tiles(g->max_fanout, B, c->num_sms) : dense_tiles(B, c->num_sms);
+}
+
+StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
+  StepParams p{};
+  p.g = g->view();
+  p.emb = c->emb;
+  p.V = c->V;
+  p.H = c->H;
+  p.st = g->d_st;
+  p.cnt = g->d_cnt;
+  p.spent = g->d_spent;
+  p.kw = g->kw;
+  p.B = B;
+  p.cand_cap = c->cand_cap;
+  p.part = c->d_part;
+  p.seq_ticket = c->d_seq_ticket;
+  p.ctrl = c->d_ctrl;
+  p.stats = c->d_stats;
+  return p;
+}
+
+ResetParams reset_params(const tc_ctx* c, const DevGrammar* g, int B, int k, int max_steps) {
+  ResetParams r{};
+  r.g = g->view();
+  r.st = g->d_st;
+  r.cnt = g->d_cnt;
+  r.spent = g->d_spent;
+  r.kw = g->kw;
+  r.B = B;
+  r.k = k;
+  r.max_steps = max_steps;
+  r.seq_ticket = c->d_seq_ticket;
+  r.ctrl = c->d_ctrl;
+  r.stats = c->d_stats;
+  return r;
+}
+
+// Re-copy g's walk image into the constant bank unless g already owns it.
+tc_status ensure_const(tc_ctx* c, DevGrammar* g, cudaStream_t s) {
+  if (g->residency != TC_RES_CONST) return TC_OK;
+  std::lock_guard<std::mutex> lk(g_const_mu);
+  if (g_const_owner[c->device] == g) return TC_OK;
+  TC_CUDA(const_upload(g->d_img, (size_t)g->layout.words * 4, s));
+  g_const_owner[c->device] = g;
+  return TC_OK;
+}
+
+tc_status check_decode_args(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch, int32_t k,
+                            int32_t max_steps, int32_t head, int32_t* toks, float* logits, int32_t* lens,
+                            int32_t* status) {
+  if (!c || !hidden || !toks || !logits || !lens || !status) return TC_ERR_INVALID_ARG;
+  if (misaligned(hidden, 16) || misaligned(toks, 4) || misaligned(logits, 4) || misaligned(lens, 4) ||
+      misaligned(status, 4)) {
+    set_error_message("hidden states must be 16-byte aligned and outputs 4-byte aligned");
+    return TC_ERR_INVALID_ARG;
+  }
+  if (!c->bound) return TC_ERR_NOT_BOUND;
+  if (batch < 1 || batch > c->max_batch) return TC_ERR_CAPACITY;
+  if (k < 1 || k > c->bound->n_strings) return TC_ERR_K_RANGE;
+  if (max_steps < 1 || max_steps > n_steps) return TC_ERR_INVALID_ARG;
+  if (head != TC_HEAD_SPARSE && head != TC_HEAD_DENSE) return TC_ERR_INVALID_ARG;
+  return TC_OK;
+}
+
+void destroy_graph(tc_graph* gr) {
+  if (!gr) return;
+  if (gr->exec) cudaGraphExecDestroy(gr->exec);
+  if (gr->graph) cudaGraphDestroy(gr->graph);
+  delete gr;
+}
+
+// Capture: [constant re-bind] -> reset -> WHILE(cond) { step }.
+tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** out) {
+  auto* gr = new tc_graph();
+  gr->ctx = c;
+  gr->g = g;
+  gr->key = key;
+  cudaStream_t cs = c->capture_stream;
+  cudaGraphConditionalHandle cond = 0;
+  tc_status rc = TC_OK;
+  auto fail = [&](cudaError_t e, const char* what) {
+    cudaStreamCaptureStatus st;
+    if (cudaStreamIsCapturing(cs, &st) == cudaSuccess && st != cudaStreamCaptureStatusNone) {
+      cudaGraph_t junk = nullptr;
+      cudaStreamEndCapture(cs, &junk);
+      if (junk && junk != gr->graph) cudaGraphDestroy(junk);
+    }
+    rc = cuda_fail(e, what);
+    destroy_graph(gr);
+    return rc;
+  };
+  cudaError_t e;
+  if ((e = cudaGraphCreate(&gr->graph, 0)) != cudaSuccess) return fail(e, "cudaGraphCreate");
+  if ((e = cudaGraphConditionalHandleCreate(&cond, gr->graph, 0, 0)) != cudaSuccess)
+    return fail(e, "cudaGraphConditionalHandleCreate");
+  if ((e = cudaStreamBeginCaptureToGraph(cs, gr->graph, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal)) !=
+      cudaSuccess)
+    return fail(e, "cudaStreamBeginCaptureToGraph");
+  if (g->residency == TC_RES_CONST) {
+    if ((e = const_upload(g->d_img, (size_t)g->layout.words * 4, cs)) != cudaSuccess)
+      return fail(e, "constant re-bind node");
+  }
+  ResetParams r = reset_params(c, g, key.batch, key.k, key.max_steps);
+  r.toks = static_cast<int32_t*>(key.toks);
+  r.logits = static_cast<float*>(key.logits);
+  r.lens_out = static_cast<int32_t*>(key.lens);
+  r.status_out = static_cast<int32_t*>(key.status);
+  r.cond = (unsigned long long)cond;
+  if ((e = launch_reset(r, cs)) != cudaSuccess) return fail(e, "reset kernel capture");
+  cudaStreamCaptureStatus cst;
+  cudaGraph_t cap_graph = nullptr;
+  const cudaGraphNode_t* deps = nullptr;
+  const cudaGraphEdgeData* edata = nullptr;
+  size_t ndeps = 0;
+  if ((e = cudaStreamGetCaptureInfo(cs, &cst, nullptr, &cap_graph, &deps, &edata, &ndeps)) != cudaSuccess)
+    return fail(e, "cudaStreamGetCaptureInfo");
+  cudaGraphNodeParams np{};
+  np.type = cudaGraphNodeTypeConditional;
+  np.conditional.handle = cond;
+  np.conditional.type = cudaGraphCondTypeWhile;
+  np.conditional.size = 1;
+  cudaGraphNode_t cnode = nullptr;
+  if ((e = cudaGraphAddNode(&cnode, cap_graph, deps, edata, ndeps, &np)) != cudaSuccess)
+    return fail(e, "cudaGraphAddNode(conditional)");
+  cudaGraph_t body = np.conditional.phGraph_out[0];
+  if ((e = cudaStreamUpdateCaptureDependencies(cs, &cnode, nullptr, 1, cudaStreamSetCaptureDependencies)) !=
+      cudaSuccess)
+    return fail(e, "cudaStreamUpdateCaptureDependencies");
+  cudaGraph_t ended = nullptr;
+  if ((e = cudaStreamEndCapture(cs, &ended)) != cudaSuccess) return fail(e, "cudaStreamEndCapture");
+
+  if ((e = cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal)) !=
+      cudaSuccess)
+    return fail(e, "cudaStreamBeginCaptureToGraph(body)");
+  StepParams p = step_params(c, g, key.batch);
+  p.hidden = static_cast<const uint16_t*>(key.hidden);
+  p.tok_out = static_cast<int32_t*>(key.toks);
+  p.logit_out = static_cast<float*>(key.logits);
+  p.status_out = static_cast<int32_t*>(key.status);
+  p.lens_out = static_cast<int32_t*>(key.lens);
+  p.out_stride = key.max_steps;
+  p.cond = (unsigned long long)cond;
+  p.device_form = 1;
+  if ((e = launch_step(p, g->residency == TC_RES_CONST, key.head, tiles_for(c, g, key.head, key.batch), cs)) !=
+      cudaSuccess)
+    return fail(e, "step kernel capture");
+  cudaGraph_t body_ended = nullptr;
+  if ((e = cudaStreamEndCapture(cs, &body_ended)) != cudaSuccess) return fail(e, "cudaStreamEndCapture(body)");
+  if ((e = cudaGraphInstantiate(&gr->exec, gr->graph, 0)) != cudaSuccess) return fail(e, "cudaGraphInstantiate");
+  *out = gr;
+  return TC_OK;
+}
+
+tc_status launch_graph(tc_graph* gr, cudaStream_t s) {
+  tc_ctx* c = gr->ctx;
+  TC_CUDA(cudaGraphLaunch(gr->exec, s));
+  if (gr->g->residency == TC_RES_CONST) {
+    std::lock_guard<std::mutex> lk(g_const_mu);
+    g_const_owner[c->device] = gr->g;
+  }
+  gr->g->batch = gr->key.batch;
+  gr->g->k = gr->key.k;
+  return TC_OK;
+}
+
+}  // namespace
+
+extern "C" tc_status tc_ctx_create(int32_t device, const void* emb_bf16, int32_t vocab, int32_t hidden,
+                                   int32_t max_batch, int32_t cand_cap, tc_ctx** out) {
+  if (!out) return TC_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (device < 0 || device >= kMaxDevices || !emb_bf16 || vocab < 2 || hidden < 8 || max_batch < 1 ||
+      cand_cap < 2 || cand_cap > kMaxCandCap) {
+    set_error_message("tc_ctx_create: invalid arguments");
+    return TC_ERR_INVALID_ARG;
+  }
+  if (hidden % 8 != 0 || hidden > kMaxHidden || (reinterpret_cast<uintptr_t>(emb_bf16) & 15) != 0) {
+    set_error_message("tc_ctx_create: hidden must be a multiple of 8 (<= 16384) and the embedding 16-byte aligned");
+    return TC_ERR_UNSUPPORTED;
+  }
+  DeviceGuard dg(device);
+  int cur = -1;
+  TC_CUDA(cudaGetDevice(&cur));
+  if (cur != device) return TC_ERR_CUDA;
+  auto* c = new tc_ctx();
+  c->device = device;
+  c->emb = static_cast<const uint16_t*>(emb_bf16);
+  c->V = vocab;
+  c->H = hidden;
+  c->max_batch = max_batch;
+  c->cand_cap = cand_cap;
+  cudaError_t e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
+  if (e == cudaSuccess) e = prepare_kernels();
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_part, sizeof(Partial) * (size_t)max_batch * kMaxTiles);
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_seq_ticket, sizeof(uint32_t) * (size_t)max_batch);
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_ctrl, sizeof(Ctrl));
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_stats, sizeof(unsigned long long) * kStatSlots);
+  if (e == cudaSuccess) e = cudaMemset(c->d_stats, 0, sizeof(unsigned long long) * kStatSlots);
+  if (e == cudaSuccess) e = cudaMemset(c->d_seq_ticket, 0, sizeof(uint32_t) * (size_t)max_batch);
+  if (e == cudaSuccess) e = cudaMemset(c->d_ctrl, 0, sizeof(Ctrl));
+  if (e == cudaSuccess) e = cudaMallocHost(&c->h_live, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    tc_status rc = cuda_fail(e, "tc_ctx_create");
+    tc_ctx_destroy(c);
+    return rc;
+  }
+  *out = c;
+  return TC_OK;
+}
+
+extern "C" void tc_ctx_destroy(tc_ctx* c) {
+  if (!c) return;
+  DeviceGuard dg(c->device);
+  cudaDeviceSynchronize();
+  for (tc_graph* g : c->cache) destroy_graph(g);
+  for (tc_graph* g : c->owned) destroy_graph(g);
+  {
+    std::lock_guard<std::mutex> lk(g_const_mu);
+    for (DevGrammar* g : c->grammars)
+      if (g_const_owner[c->device] == g) g_const_owner[c->device] = nullptr;
+  }
+  for (DevGrammar* g : c->grammars) {
+    g->release();
+    delete g;
+  }
+  cudaFree(c->d_part);
+  cudaFree(c->d_seq_ticket);
+  cudaFree(c->d_ctrl);
+  cudaFree(c->d_stats);
+  if (c->h_live) cudaFreeHost(c->h_live);
+  if (c->capture_stream) cudaStreamDestroy(c->capture_stream);
+  delete c;
+}
+
+extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t residency, void* stream) {
+  if (!c || !t) return TC_ERR_INVALID_ARG;
+  if (residency != TC_RES_AUTO && residency != TC_RES_CONST && residency != TC_RES_GLOBAL) return TC_ERR_INVALID_ARG;
+  if (t->vocab > c->V) {
+    set_error_message("tc_bind_grammar: the trie's vocabulary is larger than the context's");
+    return TC_ERR_TOKEN_RANGE;
+  }
+  if (t->max_fanout > c->cand_cap) {
+    set_error_message("tc_bind_grammar: max fan-out " + std::to_string(t->max_fanout) +
+                      " exceeds the candidate buffer " + std::to_string(c->cand_cap));
+    return TC_ERR_CAPACITY;
+  }
+  const WalkLayout L = walk_layout(t->n_nodes(), t->n_edges());
+  const size_t img_bytes = (size_t)L.words * 4;
+  int32_t res = residency;
+  if (res == TC_RES_AUTO) res = img_bytes <= TC_CONST_CAPACITY_BYTES ? TC_RES_CONST : TC_RES_GLOBAL;
+  if (res == TC_RES_CONST && img_bytes > TC_CONST_CAPACITY_BYTES) {
+    set_error_message("tc_bind_grammar: walk image of " + std::to_string(img_bytes) + " bytes exceeds constant capacity");
+    return TC_ERR_CONST_CAPACITY;
+  }
+  DeviceGuard dg(c->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevGrammar* g = nullptr;
+  for (DevGrammar* x : c->grammars)
+    if (x->hash == t->content_hash && x->residency == res && x->n_nodes == t->n_nodes() &&
+        x->n_edges == t->n_edges())
+      g = x;
+  if (!g) {
+    g = new DevGrammar();
+    g->hash = t->content_hash;
+    g->residency = res;
+    g->n_nodes = t->n_nodes();
+    g->n_edges = t->n_edges();
+    g->n_strings = t->n_strings;
+    g->max_fanout = t->max_fanout;
+    g->max_depth = t->max_depth;
+    g->layout = L;
+    g->kw = (t->n_strings + 31) / 32;
+    const std::vector<int32_t> img = build_walk_image(*t, L);
+    const size_t B = (size_t)c->max_batch;
+    cudaError_t e = cudaMalloc(&g->d_img, img_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_static_cnt, sizeof(int32_t) * std::max<size_t>(1, t->static_cnt.size()));
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_path_off, sizeof(int32_t) * t->path_off.size());
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_path, sizeof(int32_t) * std::max<size_t>(1, t->path.size()));
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_st, sizeof(SeqState) * B);
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_cnt, sizeof(int32_t) * B * std::max<int32_t>(1, g->n_edges));
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_spent, sizeof(uint32_t) * B * g->kw);
+    if (e == cudaSuccess) e = cudaMemcpy(g->d_img, img.data(), img_bytes, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(g->d_static_cnt, t->static_cnt.data(), sizeof(int32_t) * t->static_cnt.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(g->d_path_off, t->path_off.data(), sizeof(int32_t) * t->path_off.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(g->d_path, t->path.data(), sizeof(int32_t) * t->path.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(g->d_st, 0, sizeof(SeqState) * B);
+    if (e != cudaSuccess) {
+      g->release();
+      delete g;
+      return cuda_fail(e, "tc_bind_grammar upload");
+    }
+    c->grammars.push_back(g);
+  }
+  if (res == TC_RES_CONST) {
+    std::lock_guard<std::mutex> lk(g_const_mu);
+    TC_CUDA(const_upload(g->d_img, img_bytes, s));
+    g_const_owner[c->device] = g;
+  }
+  g->batch = 0;
+  g->k = 0;
+  c->bound = g;
+  return TC_OK;
+}
+
+extern "C" tc_status tc_bound_residency(const tc_ctx* c, int32_t* residency) {
+  if (!c || !residency) return TC_ERR_INVALID_ARG;
+  if (!c->bound) return TC_ERR_NOT_BOUND;
+  *residency = c->bound->residency;
+  return TC_OK;
+}
+
+extern "C" tc_status tc_reset(tc_ctx* c, int32_t batch, int32_t k, void* stream) {
+  if (!c) return TC_ERR_INVALID_ARG;
+  if (!c->bound) return TC_ERR_NOT_BOUND;
+  if (batch < 1 || batch > c->max_batch) return TC_ERR_CAPACITY;
+  if (k < 1 || k > c->bound->n_strings) return TC_ERR_K_RANGE;
+  DeviceGuard dg(c->device);
+  ResetParams r = reset_params(c, c->bound, batch, k, 0);
+  TC_CUDA(launch_reset(r, static_cast<cudaStream_t>(stream)));
+  c->bound->batch = batch;
+  c->bound->k = k;
+  return TC_OK;
+}
+
+extern "C" tc_status tc_step(tc_ctx* c, const void* hidden, int32_t head, int32_t* tok_out, float* logit_out,
+                             int32_t* status_out, void* stream) {
+  if (!c || !hidden || !tok_out) return TC_ERR_INVALID_ARG;
+  if (head != TC_HEAD_SPARSE && head != TC_HEAD_DENSE) return TC_ERR_INVALID_ARG;
+  if (misaligned(hidden, 16) || misaligned(tok_out, 4) || misaligned(logit_out, 4) || misaligned(status_out, 4)) {
+    set_error_message("tc_step: hidden states must be 16-byte aligned and outputs 4-byte aligned");
+    return TC_ERR_INVALID_ARG;
+  }
+  DevGrammar* g = c->bound;
+  if (!g || g->batch < 1) return TC_ERR_NOT_BOUND;
+  DeviceGuard dg(c->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  tc_status rc = ensure_const(c, g, s);
+  if (rc != TC_OK) return rc;
+  StepParams p = step_params(c, g, g->batch);
+  p.hidden = static_cast<const uint16_t*>(hidden);
+  p.tok_out = tok_out;
+  p.logit_out = logit_out;
+  p.status_out = status_out;
+  p.out_stride = 1;
+  TC_CUDA(launch_step(p, g->residency == TC_RES_CONST, head, tiles_for(c, g, head, g->batch), s));
+  return TC_OK;
+}
+
+extern "C" tc_status tc_decode_graph_create(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch,
+                                            int32_t k, int32_t max_steps, int32_t head, int32_t* toks,
+                                            float* logits, int32_t* lens, int32_t* status, tc_graph** out) {
+  if (!out) return TC_ERR_INVALID_ARG;
+  *out = nullptr;
+  tc_status rc = check_decode_args(c, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status);
+  if (rc != TC_OK) return rc;
+  DeviceGuard dg(c->device);
+  GraphKey key{c->bound, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status};
+  tc_graph* gr = nullptr;
+  rc = build_graph(c, c->bound, key, &gr);
+  if (rc != TC_OK) return rc;
+  c->owned.push_back(gr);
+  *out = gr;
+  return TC_OK;
+}
+
+extern "C" tc_status tc_graph_launch(tc_graph* gr, void* stream) {
+  if (!gr) return TC_ERR_INVALID_ARG;
+  DeviceGuard dg(gr->ctx->device);
+  return launch_graph(gr, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" void tc_graph_destroy(tc_graph* gr) {
+  if (!gr) return;
+  tc_ctx* c = gr->ctx;
+  DeviceGuard dg(c->device);
+  auto it = std::find(c->owned.begin(), c->owned.end(), gr);
+  if (it != c->owned.end()) c->owned.erase(it);
+  destroy_graph(gr);
+}
+
+extern "C" tc_status tc_decode(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch, int32_t k,
+                               int32_t max_steps, int32_t head, int32_t* toks, float* logits, int32_t* lens,
+                               int32_t* status, void* stream) {
+  tc_status rc = check_decode_args(c, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status);
+  if (rc != TC_OK) return rc;
+  DeviceGuard dg(c->device);
+  GraphKey key{c->bound, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status};
+  tc_graph* gr = nullptr;
+  for (size_t i = 0; i < c->cache.size(); ++i) {
+    if (c->cache[i]->key == key) {
+      gr = c->cache[i];
+      c->cache.erase(c->cache.begin() + i);
+      c->cache.push_back(gr);
+      break;
+    }
+  }
+  if (!gr) {
+    rc = build_graph(c, c->bound, key, &gr);
+    if (rc != TC_OK) return rc;
+    gr->cached = true;
+    if (c->cache.size() >= kGraphCacheSize) {
+      // The evicted graph may still be running on some stream: finish first.
+      cudaDeviceSynchronize();
+      destroy_graph(c->cache.front());
+      c->cache.erase(c->cache.begin());
+    }
+    c->cache.push_back(gr);
+  }
+  return launch_graph(gr, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch, int32_t k,
+                                    int32_t max_steps, int32_t head, int32_t* toks, float* logits, int32_t* lens,
+                                    int32_t* status, void* stream) {
+  tc_status rc = check_decode_args(c, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status);
+  if (rc != TC_OK) return rc;
+  DeviceGuard dg(c->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevGrammar* g = c->bound;
+  rc = ensure_const(c, g, s);
+  if (rc != TC_OK) return rc;
+  ResetParams r = reset_params(c, g, batch, k, max_steps);
+  r.toks = toks;
+  r.logits = logits;
+  r.lens_out = lens;
+  r.status_out = status;
+  TC_CUDA(launch_reset(r, s));
+  g->batch = batch;
+  g->k = k;
+  const int tiles = tiles_for(c, g, head, batch);
+  const size_t row = (size_t)batch * (size_t)c->H;
+  for (int32_t t = 0; t < max_steps; ++t) {
+    StepParams p = step_params(c, g, batch);
+    p.hidden = static_cast<const uint16_t*>(hidden) + (size_t)t * row;
+    p.tok_out = toks + t;
+    p.logit_out = logits + t;
+    p.status_out = status;
+    p.lens_out = lens;
+    p.out_stride = max_steps;
+    TC_CUDA(launch_step(p, g->residency == TC_RES_CONST, head, tiles, s));
+    TC_CUDA(cudaMemcpyAsync(c->h_live, &c->d_ctrl->live, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    TC_CUDA(cudaStreamSynchronize(s));
+    if (*c->h_live <= 0) break;
+  }
+  StepParams p = step_params(c, g, batch);
+  p.status_out = status;
+  p.lens_out = lens;
+  TC_CUDA(launch_finalize(p, s));
+  TC_CUDA(cudaStreamSynchronize(s));
+  return TC_OK;
+}
+
+extern "C" tc_status tc_read_seq_state(tc_ctx* c, void* stream, int32_t* node, int32_t* emitted, int32_t* len,
+                                       int32_t* status, int32_t* done) {
+  if (!c) return TC_ERR_INVALID_ARG;
+  DevGrammar* g = c->bound;
+  if (!g || g->batch < 1) return TC_ERR_NOT_BOUND;
+  DeviceGuard dg(c->device);
+  TC_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  std::vector<SeqState> h((size_t)g->batch);
+  TC_CUDA(cudaMemcpy(h.data(), g->d_st, sizeof(SeqState) * h.size(), cudaMemcpyDeviceToHost));
+  for (int32_t b = 0; b < g->batch; ++b) {
+    if (node) node[b] = h[b].node;
+    if (emitted) emitted[b] = h[b].emitted;
+    if (len) len[b] = h[b].len;
+    if (status) status[b] = h[b].status;
+    if (done) done[b] = h[b].done;
+  }
+  return TC_OK;
+}
+
+extern "C" tc_status tc_first_error(tc_ctx* c, void* stream, int32_t* seq, int32_t* code) {
+  if (!c || !seq || !code) return TC_ERR_INVALID_ARG;
+  DevGrammar* g = c->bound;
+  if (!g || g->batch < 1) return TC_ERR_NOT_BOUND;
+  std::vector<int32_t> st((size_t)g->batch);
+  tc_status rc = tc_read_seq_state(c, stream, nullptr, nullptr, nullptr, st.data(), nullptr);
+  if (rc != TC_OK) return rc;
+  *seq = -1;
+  *code = TC_OK;
+  for (int32_t b = 0; b < g->batch; ++b) {
+    if (st[b] != TC_OK) {
+      *seq = b;
+      *code = st[b];
+      break;
+    }
+  }
+  return TC_OK;
+}
+
+extern "C" tc_status tc_read_stats(tc_ctx* c, void* stream, int64_t* out, int32_t reset) {
+  if (!c || !out) return TC_ERR_INVALID_ARG;
+  DeviceGuard dg(c->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long h[kStatSlots];
+  TC_CUDA(cudaMemcpyAsync(h, c->d_stats, sizeof(h), cudaMemcpyDeviceToHost, s));
+  TC_CUDA(cudaStreamSynchronize(s));
+  for (int i = 0; i < kStatSlots; ++i) out[i] = (int64_t)h[i];
+  if (reset) {
+    TC_CUDA(cudaMemsetAsync(c->d_stats, 0, sizeof(h), s));
+    TC_CUDA(cudaStreamSynchronize(s));
+  }
+  return TC_OK;
+}

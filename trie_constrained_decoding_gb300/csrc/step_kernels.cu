@@ -1,0 +1,638 @@
+// Decode-step kernels for sm_103a: reset, sparse step, dense step, finalize.
+//
+// One launch performs one whole step for every sequence of the batch
+// ("Constraint made cheaper than no constraint", section "Masked sampling
+// inside the sampler": read the current node's edge range, filter the edges,
+// take the argmax over the survivors with a fixed tree and the lower-id
+// tie-break, advance; section "The sparse output layer": one tied-embedding
+// dot product per legal candidate over a fixed grid).
+//
+// Grid: (tiles, B) CTAs of 256 threads.  Every CTA of sequence b filters the
+// node's edges itself (the filter is a few hundred bytes of cached reads), so
+// no second launch is needed to publish the candidate list.  Candidate rank r
+// belongs to CTA r % tiles; its warps gather embedding rows with 16-byte
+// loads and reduce each dot product with a fixed shuffle tree.  Each CTA
+// leaves its best (logit, token) in a fixed slot; the last CTA of the
+// sequence to arrive (atomic ticket after a fence, no waiting) folds the
+// slots in slot order and applies the transition.  In the device form the
+// last CTA of the whole grid also advances the step counter and sets the
+// loop's conditional-node value, so a loop iteration is a single launch.
+//
+// Determinism: a logit is a function of (row, x) only - lane l accumulates
+// elements 8*(32*i + l) .. +7 for i = 0, 1, ... in order with fp32 FMAs, then
+// a butterfly xor tree over the 32 lanes - so the sparse and the dense head
+// produce bit-identical logits, and the winner under (logit desc, token asc),
+// a strict total order on distinct tokens, does not depend on fold order.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <climits>
+
+#include "kernels.h"
+#include "tcd.h"
+
+namespace tcd {
+
+__constant__ int32_t c_walk[TC_CONST_CAPACITY_BYTES / 4];
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <bool kConst>
+struct WalkRd {
+  const int32_t* img;
+  int32_t off_edges, off_ptr;
+  __device__ __forceinline__ int32_t begin(int32_t n) const {
+    if constexpr (kConst) return c_walk[n];
+    else return __ldg(img + n);
+  }
+  __device__ __forceinline__ int2 edge(int32_t e) const {
+    if constexpr (kConst) return make_int2(c_walk[off_edges + 2 * e], c_walk[off_edges + 2 * e + 1]);
+    else return __ldg(reinterpret_cast<const int2*>(img + off_edges) + e);
+  }
+  __device__ __forceinline__ int32_t ptr(int32_t n) const {
+    if constexpr (kConst) return c_walk[off_ptr + n];
+    else return __ldg(img + off_ptr + n);
+  }
+};
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// acc += e[0]*x[0] + ... + e[7]*x[7], one FMA at a time in element order.
+__device__ __forceinline__ float dot8(const uint4 e, const uint4 x, float acc) {
+  acc = fmaf(bf_lo(e.x), bf_lo(x.x), acc);
+  acc = fmaf(bf_hi(e.x), bf_hi(x.x), acc);
+  acc = fmaf(bf_lo(e.y), bf_lo(x.y), acc);
+  acc = fmaf(bf_hi(e.y), bf_hi(x.y), acc);
+  acc = fmaf(bf_lo(e.z), bf_lo(x.z), acc);
+  acc = fmaf(bf_hi(e.z), bf_hi(x.z), acc);
+  acc = fmaf(bf_lo(e.w), bf_lo(x.w), acc);
+  acc = fmaf(bf_hi(e.w), bf_hi(x.w), acc);
+  return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+  v += __shfl_xor_sync(kFull, v, 16);
+  v += __shfl_xor_sync(kFull, v, 8);
+  v += __shfl_xor_sync(kFull, v, 4);
+  v += __shfl_xor_sync(kFull, v, 2);
+  v += __shfl_xor_sync(kFull, v, 1);
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_row(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// x fragment of one lane: chunks 32*i + lane (8 bf16 each).
+template <int NCH>
+struct XFrag {
+  uint4 v[NCH > 0 ? NCH : 1];
+  __device__ __forceinline__ void load(const uint16_t* x, int lane) {
+    const uint4* x4 = reinterpret_cast<const uint4*>(x);
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) v[i] = __ldg(x4 + i * 32 + lane);
+  }
+};
+
+// Row dot products with the fixed lane map.  NCH > 0: H == 256 * NCH and x in
+// registers.  NCH == 0: any H % 8 == 0, x staged in shared memory.
+template <int NCH>
+__device__ __forceinline__ float row_dot(const uint16_t* row, const XFrag<NCH>& xf,
+                                         const uint4* xs, int nch, int lane) {
+  const uint4* r4 = reinterpret_cast<const uint4*>(row);
+  float acc = 0.f;
+  if constexpr (NCH > 0) {
+    uint4 e[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) e[i] = ld_row(r4 + i * 32 + lane);
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xf.v[i], acc);
+  } else {
+    for (int c = lane; c < nch; c += 32) acc = dot8(ld_row(r4 + c), xs[c], acc);
+  }
+  return warp_sum(acc);
+}
+
+// Two rows at once (more loads in flight); each result is bit-identical to row_dot.
+template <int NCH>
+__device__ __forceinline__ void row_dot2(const uint16_t* ra, const uint16_t* rb, const XFrag<NCH>& xf,
+                                         const uint4* xs, int nch, int lane, float& oa, float& ob) {
+  const uint4* a4 = reinterpret_cast<const uint4*>(ra);
+  const uint4* b4 = reinterpret_cast<const uint4*>(rb);
+  float aa = 0.f, ab = 0.f;
+  if constexpr (NCH > 0) {
+    uint4 ea[NCH], eb[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      ea[i] = ld_row(a4 + i * 32 + lane);
+      eb[i] = ld_row(b4 + i * 32 + lane);
+    }
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      aa = dot8(ea[i], xf.v[i], aa);
+      ab = dot8(eb[i], xf.v[i], ab);
+    }
+  } else {
+    for (int c = lane; c < nch; c += 32) {
+      const uint4 ea = ld_row(a4 + c), eb = ld_row(b4 + c);
+      aa = dot8(ea, xs[c], aa);
+      ab = dot8(eb, xs[c], ab);
+    }
+  }
+  oa = warp_sum(aa);
+  ob = warp_sum(ab);
+}
+
+// (l, t) beats (bl, bt): larger logit, or equal logit and lower token id.
+// A NaN logit never beats anything.
+__device__ __forceinline__ bool better(float l, int32_t t, float bl, int32_t bt) {
+  return l > bl || (l == bl && t < bt);
+}
+
+struct FilterResult {
+  int32_t ncand;  // legal candidates at the node
+  int32_t err;    // an index of the grammar image was out of range
+};
+
+// Block-wide edge filter.  Legal candidate of rank r (edge order, which is
+// ascending token order) is stored at s_tok/s_edge[r / T] when r % T == t.
+template <bool kConst>
+__device__ FilterResult filter_node(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
+                                    int b, int T, int t, int32_t* s_tok, int32_t* s_edge,
+                                    int32_t* s_scan) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = s.node;
+  if (n < 0 || n >= p.g.n_nodes) return {0, 1};
+  const int beg = w.begin(n), end = w.begin(n + 1);
+  if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > p.cand_cap) return {0, 1};
+  const int pid = w.ptr(n);
+  bool ctl_ok = false;
+  int bad = 0;
+  if (pid >= 0) {
+    if (pid >= p.g.n_strings) {
+      bad = 1;
+    } else {
+      const uint32_t word = p.spent[(size_t)b * p.kw + (pid >> 5)];
+      ctl_ok = ((word >> (pid & 31)) & 1u) == 0;
+    }
+  }
+  const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
+  const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
+  const int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
+  int running = 0;
+  for (int base = beg; base < end; base += kThreads) {
+    const int e = base + tid;
+    bool legal = false;
+    int2 ed = make_int2(0, 0);
+    if (e < end) {
+      ed = w.edge(e);
+      if (ed.x < 0 || ed.x >= p.V) {
+        bad = 1;
+      } else if (ed.y >= 0) {
+        if (ed.y >= p.g.n_nodes) bad = 1;
+        else legal = cnt[e] > 0;
+      } else if (ed.y == -1) {
+        legal = sep_ok;
+      } else if (ed.y == -2) {
+        legal = stop_ok;
+      } else {
+        bad = 1;
+      }
+    }
+    const unsigned bal = __ballot_sync(kFull, legal);
+    if (lane == 0) s_scan[warp] = __popc(bal);
+    __syncthreads();
+    int woff = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+      const int c = s_scan[i];
+      woff += (i < warp) ? c : 0;
+      tot += c;
+    }
+    if (legal) {
+      const int rank = running + woff + __popc(bal & ((1u << lane) - 1u));
+      if (rank % T == t) {
+        s_tok[rank / T] = ed.x;
+        s_edge[rank / T] = e;
+      }
+    }
+    running += tot;
+    __syncthreads();
+  }
+  const int any_bad = __syncthreads_or(bad);
+  return {running, any_bad};
+}
+
+// Apply the transition of sequence b with winner (best_l, best_t, best_e).
+// Called by every thread of the sequence's last CTA.
+template <bool kConst>
+__device__ void finish_sequence(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b,
+                                float best_l, int32_t best_t, int32_t best_e, int32_t ncand, int32_t err) {
+  const int tid = threadIdx.x;
+  int status = TC_OK;
+  int32_t new_node = s.node, ptr_done = -1;
+  bool stop = false;
+  if (err) {
+    status = TC_ERR_BOUNDS;
+  } else if (ncand == 0) {
+    status = TC_ERR_EMPTY_MASK;
+  } else if (best_t == INT_MAX || best_e < 0 || best_e >= p.g.n_edges || !(best_l == best_l)) {
+    status = TC_ERR_BOUNDS;  // no comparable logit (NaN) or a corrupted slot
+  } else {
+    const int2 ed = w.edge(best_e);
+    if (ed.x != best_t) {
+      status = TC_ERR_BOUNDS;
+    } else if (ed.y >= 0) {
+      if (p.cnt[(size_t)b * p.g.n_edges + best_e] <= 0) status = TC_ERR_NO_LIVE_EDGE;
+      else new_node = ed.y;
+    } else {
+      const int32_t pid = w.ptr(s.node);
+      if (pid < 0 || pid >= p.g.n_strings ||
+          ((p.spent[(size_t)b * p.kw + (pid >> 5)] >> (pid & 31)) & 1u)) {
+        status = TC_ERR_NO_LIVE_EDGE;
+      } else {
+        ptr_done = pid;
+        stop = (ed.y == -2);
+        new_node = 0;
+      }
+    }
+  }
+  __syncthreads();  // every thread has decided before the state changes
+  if (ptr_done >= 0) {
+    // The completed pointer is no longer live below any edge of its path.
+    const int32_t q0 = __ldg(p.g.path_off + ptr_done), q1 = __ldg(p.g.path_off + ptr_done + 1);
+    int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
+    for (int32_t q = q0 + tid; q < q1; q += kThreads) {
+      const int32_t e = __ldg(p.g.path + q);
+      if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
+    }
+  }
+  if (tid == 0) {
+    SeqState ns = s;
+    if (status != TC_OK) {
+      ns.status = status;
+      ns.done = 1;
+    } else {
+      ns.node = new_node;
+      ns.len = s.len + 1;
+      if (ptr_done >= 0) {
+        ns.emitted = s.emitted + 1;
+        p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
+      }
+      if (stop) ns.done = 1;
+    }
+    p.st[b] = ns;
+    if (p.stats) {
+      atomicAdd(&p.stats[kStatSeqSteps], 1ull);
+      atomicAdd(&p.stats[kStatCandRows], (unsigned long long)ncand);
+    }
+    if (p.device_form) {
+      if (status == TC_OK && s.len < p.out_stride) {
+        p.tok_out[(size_t)b * p.out_stride + s.len] = best_t;
+        p.logit_out[(size_t)b * p.out_stride + s.len] = best_l;
+      }
+    } else {
+      p.tok_out[(size_t)b * p.out_stride] = status == TC_OK ? best_t : -1;
+      if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = status == TC_OK ? best_l : 0.f;
+    }
+    if (p.status_out) p.status_out[b] = ns.status;
+    if (p.lens_out) p.lens_out[b] = ns.len;
+    if (ns.done && p.ctrl) atomicSub(&p.ctrl->live, 1);
+  }
+}
+
+// Fold the per-warp bests, combine the CTAs of sequence b, and let the last
+// CTA apply the transition; then (device form) the grid-wide loop bookkeeping.
+template <bool kConst>
+__device__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b,
+                          bool active, float wl, int32_t wt, int32_t we, int32_t ncand, int32_t err) {
+  __shared__ float s_wl[kWarps];
+  __shared__ int32_t s_wt[kWarps], s_we[kWarps];
+  __shared__ float s_bl;
+  __shared__ int32_t s_bt, s_be, s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tiles = gridDim.x, t = blockIdx.x;
+  if (p.stats && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
+  if (active) {
+    if (lane == 0) {
+      s_wl[warp] = wl;
+      s_wt[warp] = wt;
+      s_we[warp] = we;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float bl = -INFINITY;
+      int32_t bt = INT_MAX, be = -1;
+      for (int i = 0; i < kWarps; ++i)
+        if (better(s_wl[i], s_wt[i], bl, bt)) { bl = s_wl[i]; bt = s_wt[i]; be = s_we[i]; }
+      int last = 1;
+      if (tiles > 1) {
+        Partial* slot = p.part + (size_t)b * tiles;
+        slot[t] = Partial{bl, bt, be, 0};
+        __threadfence();
+        const uint32_t ticket = atomicAdd(&p.seq_ticket[b], 1u);
+        last = (ticket == (uint32_t)tiles - 1);
+        if (last) {
+          __threadfence();
+          bl = -INFINITY;
+          bt = INT_MAX;
+          be = -1;
+          for (int i = 0; i < tiles; ++i) {
+            const float l = __ldcg(&slot[i].logit);
+            const int32_t tk = __ldcg(&slot[i].tok);
+            const int32_t ee = __ldcg(&slot[i].edge);
+            if (better(l, tk, bl, bt)) { bl = l; bt = tk; be = ee; }
+          }
+          p.seq_ticket[b] = 0;
+        }
+      }
+      s_bl = bl;
+      s_bt = bt;
+      s_be = be;
+      s_last = last;
+    }
+    __syncthreads();
+    if (s_last) finish_sequence<kConst>(p, w, s, b, s_bl, s_bt, s_be, ncand, err);
+  } else if (!p.device_form && t == 0 && tid == 0) {
+    // A stopped or failed sequence reports an idle token.
+    p.tok_out[(size_t)b * p.out_stride] = -1;
+    if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = 0.f;
+    if (p.status_out) p.status_out[b] = s.status;
+    if (p.lens_out) p.lens_out[b] = s.len;
+  }
+
+  if (p.device_form) {
+    __shared__ int32_t s_glast;
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      const uint32_t total = gridDim.x * gridDim.y;
+      const uint32_t g = atomicAdd(&p.ctrl->ticket, 1u);
+      s_glast = (g == total - 1);
+    }
+    __syncthreads();
+    if (s_glast) {
+      __threadfence();
+      const int32_t next = __ldcg(&p.ctrl->step) + 1;
+      const int32_t live = atomicAdd(&p.ctrl->live, 0);
+      const int32_t max_steps = __ldcg(&p.ctrl->max_steps);
+      if (live > 0 && next >= max_steps) {
+        for (int bb = tid; bb < p.B; bb += kThreads) {
+          if (__ldcg(&p.st[bb].done) == 0) {
+            p.st[bb].status = TC_ERR_MAX_STEPS;
+            p.st[bb].done = 1;
+            p.status_out[bb] = TC_ERR_MAX_STEPS;
+          }
+        }
+      }
+      if (tid == 0) {
+        p.ctrl->step = next;
+        p.ctrl->ticket = 0;
+        if (live > 0 && next >= max_steps) p.ctrl->live = 0;
+        cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, (live > 0 && next < max_steps) ? 1u : 0u);
+      }
+    }
+  }
+}
+
+template <int NCH>
+__device__ __forceinline__ const uint16_t* hidden_row(const StepParams& p, int b) {
+  size_t row = (size_t)b;
+  if (p.device_form) row += (size_t)__ldcg(&p.ctrl->step) * (size_t)p.B;
+  return p.hidden + row * (size_t)p.H;
+}
+
+}  // namespace
+
+// Sparse head: one dot product per legal candidate.
+template <bool kConst, int NCH>
+__global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ int32_t s_scan[kWarps];
+  const int b = blockIdx.y, t = blockIdx.x, T = gridDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
+  const SeqState s = p.st[b];
+  const bool active = s.done == 0;
+  const int nch = p.H >> 3;
+  const int local_cap = (p.cand_cap + T - 1) / T;
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
+  int32_t* s_edge = s_tok + local_cap;
+
+  float wl = -INFINITY;
+  int32_t wt = INT_MAX, we = -1;
+  FilterResult fr{0, 0};
+  if (active) {
+    const uint16_t* x = hidden_row<NCH>(p, b);
+    XFrag<NCH> xf;
+    if constexpr (NCH > 0) {
+      xf.load(x, lane);
+    } else {
+      for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
+    }
+    fr = filter_node<kConst>(p, w, s, b, T, t, s_tok, s_edge, s_scan);
+    if (!fr.err) {
+      const int nlocal = fr.ncand > t ? (fr.ncand - t + T - 1) / T : 0;
+      for (int l = warp; l < nlocal; l += kWarps) {
+        const int32_t tok = s_tok[l];
+        const float v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
+        if (better(v, tok, wl, wt)) { wl = v; wt = tok; we = s_edge[l]; }
+      }
+    }
+  }
+  step_tail<kConst>(p, w, s, b, active, wl, wt, we, fr.ncand, fr.err);
+}
+
+// Dense head: every vocabulary row, then the legal mask, then the argmax.
+template <bool kConst, int NCH>
+__global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ int32_t s_scan[kWarps];
+  const int b = blockIdx.y, g = blockIdx.x, G = gridDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
+  const SeqState s = p.st[b];
+  const bool active = s.done == 0;
+  const int nch = p.H >> 3;
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
+  int32_t* s_edge = s_tok + p.cand_cap;
+
+  float wl = -INFINITY;
+  int32_t wt = INT_MAX, we = -1;
+  FilterResult fr{0, 0};
+  if (active) {
+    const uint16_t* x = hidden_row<NCH>(p, b);
+    XFrag<NCH> xf;
+    if constexpr (NCH > 0) {
+      xf.load(x, lane);
+    } else {
+      for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
+    }
+    fr = filter_node<kConst>(p, w, s, b, 1, 0, s_tok, s_edge, s_scan);
+    if (!fr.err) {
+      const int n = fr.ncand;
+      auto consider = [&](int32_t r, float v) {
+        // legal iff r is in the ascending candidate list
+        int lo = 0, hi = n;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (s_tok[mid] < r) lo = mid + 1; else hi = mid;
+        }
+        if (lo < n && s_tok[lo] == r && better(v, r, wl, wt)) { wl = v; wt = r; we = s_edge[lo]; }
+      };
+      const int stride = G * kWarps;
+      int32_t r = g * kWarps + warp;
+      for (; r + stride < p.V; r += 2 * stride) {
+        float va, vb;
+        row_dot2<NCH>(p.emb + (size_t)r * p.H, p.emb + (size_t)(r + stride) * p.H, xf, xs, nch, lane, va, vb);
+        consider(r, va);
+        consider(r + stride, vb);
+      }
+      if (r < p.V) consider(r, row_dot<NCH>(p.emb + (size_t)r * p.H, xf, xs, nch, lane));
+    }
+  }
+  step_tail<kConst>(p, w, s, b, active, wl, wt, we, fr.ncand, fr.err);
+}
+
+__global__ void __launch_bounds__(kThreads) reset_kernel(const ResetParams r) {
+  const int b = blockIdx.y, tid = threadIdx.x;
+  const int E = r.g.n_edges;
+  int32_t* cnt = r.cnt + (size_t)b * E;
+  for (int e = blockIdx.x * kThreads + tid; e < E; e += gridDim.x * kThreads) cnt[e] = __ldg(r.g.static_cnt + e);
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < r.kw; i += kThreads) r.spent[(size_t)b * r.kw + i] = 0u;
+    if (r.toks) {
+      for (int i = tid; i < r.max_steps; i += kThreads) {
+        r.toks[(size_t)b * r.max_steps + i] = -1;
+        r.logits[(size_t)b * r.max_steps + i] = 0.f;
+      }
+    }
+    if (tid == 0) {
+      SeqState s{};
+      s.k = r.k;
+      r.st[b] = s;
+      r.seq_ticket[b] = 0u;
+      if (r.lens_out) r.lens_out[b] = 0;
+      if (r.status_out) r.status_out[b] = TC_OK;
+    }
+    if (b == 0 && tid == 0) {
+      if (r.stats) atomicAdd(&r.stats[kStatResetLaunches], 1ull);
+      r.ctrl->step = 0;
+      r.ctrl->live = r.B;
+      r.ctrl->max_steps = r.max_steps;
+      r.ctrl->ticket = 0u;
+      if (r.cond) cudaGraphSetConditional((cudaGraphConditionalHandle)r.cond, (r.B > 0 && r.max_steps > 0) ? 1u : 0u);
+    }
+  }
+}
+
+// End of a host-driven decode: sequences still live ran out of steps.
+__global__ void __launch_bounds__(kThreads) finalize_kernel(const StepParams p) {
+  for (int b = threadIdx.x; b < p.B; b += kThreads) {
+    SeqState s = p.st[b];
+    if (!s.done) {
+      s.status = TC_ERR_MAX_STEPS;
+      s.done = 1;
+      p.st[b] = s;
+    }
+    if (p.status_out) p.status_out[b] = s.status;
+    if (p.lens_out) p.lens_out[b] = s.len;
+  }
+  if (threadIdx.x == 0 && p.ctrl) p.ctrl->live = 0;
+}
+
+// ---------------------------------------------------------------- launchers
+
+int sparse_tiles(int max_fanout, int B, int num_sms) {
+  int by_fan = (max_fanout + kWarps - 1) / kWarps;
+  int by_grid = (4 * num_sms + B - 1) / B;
+  int t = by_fan < by_grid ? by_fan : by_grid;
+  if (t < 1) t = 1;
+  if (t > kMaxTiles) t = kMaxTiles;
+  return t;
+}
+
+int dense_tiles(int B, int num_sms) {
+  int g = (2 * num_sms) / (B > 0 ? B : 1);
+  if (g < 1) g = 1;
+  if (g > kMaxTiles) g = kMaxTiles;
+  return g;
+}
+
+namespace {
+
+template <bool kConst, int NCH>
+cudaError_t launch_one(const StepParams& p, int head, int tiles, cudaStream_t s) {
+  const int nch = p.H >> 3;
+  const size_t xbytes = NCH == 0 ? (size_t)nch * 16 : 0;
+  const int cap = head == kHeadSparse ? (p.cand_cap + tiles - 1) / tiles : p.cand_cap;
+  const size_t smem = xbytes + 2 * (size_t)cap * sizeof(int32_t);
+  dim3 grid(tiles, p.B), block(kThreads);
+  if (head == kHeadSparse) sparse_step_kernel<kConst, NCH><<<grid, block, smem, s>>>(p);
+  else dense_step_kernel<kConst, NCH><<<grid, block, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <bool kConst, int NCH>
+cudaError_t prepare_one() {
+  constexpr int kSmem = kMaxDynamicSmem;
+  cudaError_t e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dense_step_kernel<kConst, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+}
+
+template <bool kConst>
+cudaError_t launch_h(const StepParams& p, int head, int tiles, cudaStream_t s) {
+  switch (p.H) {
+    case 256: return launch_one<kConst, 1>(p, head, tiles, s);
+    case 2048: return launch_one<kConst, 8>(p, head, tiles, s);
+    case 4096: return launch_one<kConst, 16>(p, head, tiles, s);
+    default: return launch_one<kConst, 0>(p, head, tiles, s);
+  }
+}
+
+}  // namespace
+
+cudaError_t prepare_kernels() {
+  cudaError_t e;
+  if ((e = prepare_one<true, 0>()) != cudaSuccess) return e;
+  if ((e = prepare_one<true, 1>()) != cudaSuccess) return e;
+  if ((e = prepare_one<true, 8>()) != cudaSuccess) return e;
+  if ((e = prepare_one<true, 16>()) != cudaSuccess) return e;
+  if ((e = prepare_one<false, 0>()) != cudaSuccess) return e;
+  if ((e = prepare_one<false, 1>()) != cudaSuccess) return e;
+  if ((e = prepare_one<false, 8>()) != cudaSuccess) return e;
+  return prepare_one<false, 16>();
+}
+
+cudaError_t launch_step(const StepParams& p, bool const_resident, int head, int tiles, cudaStream_t s) {
+  return const_resident ? launch_h<true>(p, head, tiles, s) : launch_h<false>(p, head, tiles, s);
+}
+
+cudaError_t launch_reset(const ResetParams& r, cudaStream_t s) {
+  int bx = (r.g.n_edges + kThreads * 4 - 1) / (kThreads * 4);
+  if (bx < 1) bx = 1;
+  if (bx > 64) bx = 64;
+  reset_kernel<<<dim3(bx, r.B), kThreads, 0, s>>>(r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const StepParams& p, cudaStream_t s) {
+  finalize_kernel<<<1, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t const_upload(const void* d_src, size_t bytes, cudaStream_t s) {
+  return cudaMemcpyToSymbolAsync(c_walk, d_src, bytes, 0, cudaMemcpyDeviceToDevice, s);
+}
+
+}  // namespace tcd
