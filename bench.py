@@ -60,6 +60,10 @@ def parse_args():
     ap.add_argument("--head", choices=["sparse", "dense"], default="sparse")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-extras", action="store_true", help="skip the dense/host-loop/e2e/roofline passes")
+    ap.add_argument("--residency", choices=["auto", "const", "global"], default=None,
+                    help="grammar residency (default: the workload's)")
+    ap.add_argument("--loop", choices=["graph", "host"], default="graph",
+                    help="timed loop: the captured device-resident graph (default) or host-driven steps")
     return ap.parse_args()
 
 
@@ -151,23 +155,21 @@ def oracle_baseline(w, seconds: float, head: str = "sparse"):
     from oracle import grammar as G
     trie = G.compile_catalog(w.catalog, w.sep_id, w.stop_id, w.vocab, max_fanout=w.max_fanout)
     emb = w.embedding()
+    n_batches = max(1, min(w.n_queries // w.batch, max(1, 256 // w.batch)))
+    hid = w.hidden_states(0, n_batches * w.batch)          # generated before the clock starts
     t0 = time.perf_counter()
     steps = tokens = queries = 0
     q = 0
-    hid_cache = None
     while True:
-        if hid_cache is None or q % 64 == 0:
-            hid_cache = w.hidden_states(q * w.batch, 64 * w.batch)
-        base = (q % 64) * w.batch
-        t_start = time.perf_counter()
+        base = q * w.batch
         lens = []
         for b in range(w.batch):
-            toks, _, _ = D.greedy_decode(trie, w.k, emb, hid_cache[:, base + b], w.max_steps, head=head)
+            toks, _, _ = D.greedy_decode(trie, w.k, emb, hid[:, base + b], w.max_steps, head=head)
             lens.append(len(toks))
         tokens += sum(lens)
         steps += max(lens)
         queries += 1
-        q = (q + 1) % max(1, w.n_queries // w.batch)
+        q = (q + 1) % n_batches
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
@@ -226,7 +228,7 @@ def run_ours(args):
     trie = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
     tinfo = trie.info()
     ctx = tcd.Context(emb, max_batch=B, cand_cap=w.cand_cap)
-    res = {"const": tcd.RES_CONST, "global": tcd.RES_GLOBAL, "auto": tcd.RES_AUTO}[w.residency]
+    res = {"const": tcd.RES_CONST, "global": tcd.RES_GLOBAL, "auto": tcd.RES_AUTO}[args.residency or w.residency]
     ctx.bind(trie, res)
 
     n_batches = max(1, w.n_queries // B)
@@ -247,7 +249,8 @@ def run_ours(args):
         flush.zero_()
         if ev is not None:
             ev[0].record(stream)
-        ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head)
+        run = ctx.decode if args.loop == "graph" else ctx.decode_host
+        run(hid_buf, w.k, S, toks, logits, lens, status, head=head)
         if ev is not None:
             ev[1].record(stream)
 

@@ -36,11 +36,9 @@ struct Partial {
 
 // Device control block of the device-resident loop.
 struct Ctrl {
-  int32_t step;       // loop iteration being run
   int32_t live;       // sequences neither stopped nor failed
-  int32_t max_steps;  // step budget
-  uint32_t ticket;    // CTAs of the current launch that have finished
-  int32_t pad[4];
+  uint32_t ticket;    // CTAs of the current launch that have finished (loop-control launches)
+  int32_t pad[6];
 };
 
 // The bound grammar as the kernels see it.
@@ -57,7 +55,7 @@ struct StepParams {
   GrammarView g;
   const uint16_t* emb;      // bf16 [V, H]
   int32_t V, H;
-  const uint16_t* hidden;   // bf16 [B, H] (host form) or [S, B, H] (device form)
+  const uint16_t* hidden;   // bf16 [B, H] (host form) or [S, B, H] (device form: row len_b * B + b)
   SeqState* st;             // [B]
   int32_t* cnt;             // [B, E] live-pointer counts
   uint32_t* spent;          // [B, kw] spent flags
@@ -66,14 +64,16 @@ struct StepParams {
   int32_t cand_cap;         // C
   Partial* part;            // [B, tiles]
   uint32_t* seq_ticket;     // [B]
-  Ctrl* ctrl;               // control block (host form: only `live` is maintained)
+  Ctrl* ctrl;               // control block: live count and the loop-control ticket
+  int32_t max_steps;        // a live sequence with this many tokens stops with TC_ERR_MAX_STEPS
   int32_t* tok_out;         // host form: [b * out_stride]; device form: toks[b * out_stride + len]
   float* logit_out;         // same indexing as tok_out (may be null in host form)
   int32_t* status_out;      // [B] or null
   int32_t* lens_out;        // [B] or null
   int32_t out_stride;
   unsigned long long cond;  // cudaGraphConditionalHandle of the loop (device form)
-  int32_t device_form;      // 1: hidden and output position come from the control block
+  int32_t device_form;      // 1: hidden row and output position follow each sequence's own length
+  int32_t loop_ctrl;        // 1: this launch sets the loop's condition (last step of a loop body)
   unsigned long long* stats;  // optional counters, see StatSlot
 };
 
@@ -108,7 +108,9 @@ int dense_tiles(int B, int num_sms);
 // (current device; call once per device before the first launch or capture).
 cudaError_t prepare_kernels();
 cudaError_t launch_reset(const ResetParams& r, cudaStream_t s);
-cudaError_t launch_step(const StepParams& p, bool const_resident, int head, int tiles, cudaStream_t s);
+// pdl: launch as the programmatic dependent of the previous kernel in the stream.
+cudaError_t launch_step(const StepParams& p, bool const_resident, int head, int tiles, cudaStream_t s,
+                        bool pdl = false);
 cudaError_t launch_finalize(const StepParams& p, cudaStream_t s);
 // Copy a walk image (device memory) into the constant bank, stream-ordered.
 cudaError_t const_upload(const void* d_src, size_t bytes, cudaStream_t s);

@@ -35,6 +35,11 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kGraphCacheSize = 16;
+// Decode steps per iteration of the graph's WHILE body.  Each iteration of a
+// conditional node costs a few microseconds of its own; running several step
+// kernels per iteration amortises it, at the price of up to kLoopUnroll - 1
+// idle step launches after the last sequence stops.
+constexpr int kLoopUnroll = 8;
 
 std::mutex g_const_mu;
 const void* g_const_owner[kMaxDevices];  // grammar whose image the constant bank holds
@@ -168,6 +173,7 @@ StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
   p.seq_ticket = c->d_seq_ticket;
   p.ctrl = c->d_ctrl;
   p.stats = c->d_stats;
+  p.max_steps = INT32_MAX;
   return p;
 }
 
@@ -291,11 +297,17 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
   p.status_out = static_cast<int32_t*>(key.status);
   p.lens_out = static_cast<int32_t*>(key.lens);
   p.out_stride = key.max_steps;
+  p.max_steps = key.max_steps;
   p.cond = (unsigned long long)cond;
   p.device_form = 1;
-  if ((e = launch_step(p, g->residency == TC_RES_CONST, key.head, tiles_for(c, g, key.head, key.batch), cs)) !=
-      cudaSuccess)
-    return fail(e, "step kernel capture");
+  // The body runs kLoopUnroll steps; only the last sets the loop condition.
+  // A sequence that has stopped makes the remaining steps of the body no-ops.
+  for (int u = 0; u < kLoopUnroll; ++u) {
+    p.loop_ctrl = (u == kLoopUnroll - 1);
+    if ((e = launch_step(p, g->residency == TC_RES_CONST, key.head, tiles_for(c, g, key.head, key.batch), cs,
+                         /*pdl=*/u > 0)) != cudaSuccess)
+      return fail(e, "step kernel capture");
+  }
   cudaGraph_t body_ended = nullptr;
   if ((e = cudaStreamEndCapture(cs, &body_ended)) != cudaSuccess) return fail(e, "cudaStreamEndCapture(body)");
   if ((e = cudaGraphInstantiate(&gr->exec, gr->graph, 0)) != cudaSuccess) return fail(e, "cudaGraphInstantiate");
@@ -593,6 +605,7 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
     p.status_out = status;
     p.lens_out = lens;
     p.out_stride = max_steps;
+    p.max_steps = max_steps;
     TC_CUDA(launch_step(p, g->residency == TC_RES_CONST, head, tiles, s));
     TC_CUDA(cudaMemcpyAsync(c->h_live, &c->d_ctrl->live, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
     TC_CUDA(cudaStreamSynchronize(s));

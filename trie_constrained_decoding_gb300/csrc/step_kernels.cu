@@ -8,15 +8,20 @@
 // dot product per legal candidate over a fixed grid).
 //
 // Grid: (tiles, B) CTAs of 256 threads.  Every CTA of sequence b filters the
-// node's edges itself (the filter is a few hundred bytes of cached reads), so
-// no second launch is needed to publish the candidate list.  Candidate rank r
-// belongs to CTA r % tiles; its warps gather embedding rows with 16-byte
-// loads and reduce each dot product with a fixed shuffle tree.  Each CTA
-// leaves its best (logit, token) in a fixed slot; the last CTA of the
-// sequence to arrive (atomic ticket after a fence, no waiting) folds the
-// slots in slot order and applies the transition.  In the device form the
-// last CTA of the whole grid also advances the step counter and sets the
-// loop's conditional-node value, so a loop iteration is a single launch.
+// node's edges itself (a few hundred bytes of cached reads), so no second
+// launch is needed to publish the candidate list.  Candidate rank r belongs
+// to CTA r % tiles; its warps gather embedding rows with 16-byte loads and
+// reduce each dot product with a fixed shuffle tree.  With several CTAs per
+// sequence each leaves its best (logit, token) in a fixed slot and the last
+// CTA to arrive (atomic ticket after a fence, no waiting) folds the slots in
+// slot order and applies the transition.
+//
+// Device form (the graph loop body): sequence b at its own step t = len_b
+// reads hidden[t, b] and writes toks[b, t]; a live sequence's length equals
+// the loop iteration, so no shared step counter is read.  The launch flagged
+// loop_ctrl (the last step of a loop body) also sets the conditional node's
+// value: directly when the grid is one CTA, else from the live count after a
+// grid-wide ticket.
 //
 // Determinism: a logit is a function of (row, x) only - lane l accumulates
 // elements 8*(32*i + l) .. +7 for i = 0, 1, ... in order with fp32 FMAs, then
@@ -156,63 +161,105 @@ __device__ __forceinline__ bool better(float l, int32_t t, float bl, int32_t bt)
   return l > bl || (l == bl && t < bt);
 }
 
-struct FilterResult {
-  int32_t ncand;  // legal candidates at the node
-  int32_t err;    // an index of the grammar image was out of range
+// Shared state of one CTA of a step kernel.
+struct StepShared {
+  int32_t scan[kWarps];
+  float wl[kWarps];
+  int32_t wt[kWarps], we[kWarps];
+  int32_t ncand, err, last, glast;
+  float bl;
+  int32_t bt, be, done_after;
 };
 
-// Block-wide edge filter.  Legal candidate of rank r (edge order, which is
-// ascending token order) is stored at s_tok/s_edge[r / T] when r % T == t.
+// Legality of one edge of the current node (see the filter below).
 template <bool kConst>
-__device__ FilterResult filter_node(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
-                                    int b, int T, int t, int32_t* s_tok, int32_t* s_edge,
-                                    int32_t* s_scan) {
+__device__ __forceinline__ bool edge_legal(const StepParams& p, const WalkRd<kConst>& w, const int32_t* cnt,
+                                           int e, bool sep_ok, bool stop_ok, int2& ed, int& bad) {
+  ed = w.edge(e);
+  const int32_t c = cnt[e];  // issued together with the edge record
+  if (ed.x < 0 || ed.x >= p.V) {
+    bad = 1;
+    return false;
+  }
+  if (ed.y >= 0) {
+    if (ed.y >= p.g.n_nodes) {
+      bad = 1;
+      return false;
+    }
+    return c > 0;
+  }
+  if (ed.y == -1) return sep_ok;
+  if (ed.y == -2) return stop_ok;
+  bad = 1;
+  return false;
+}
+
+// Edge filter ("Masked sampling inside the sampler"): a token edge is legal
+// while a live pointer lies below it; the separator while the terminal's
+// pointer is unspent and another pointer is still owed after it; stop while
+// it is unspent and it is the last one owed.  The legal candidate of rank r
+// (edge order = ascending token order) is stored at s_tok/s_edge[r / T] when
+// r % T == t.  Results in sh.ncand / sh.err, visible after the final barrier.
+template <bool kConst>
+__device__ void filter_node(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int T,
+                            int t, int32_t* s_tok, int32_t* s_edge, StepShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = s.node;
-  if (n < 0 || n >= p.g.n_nodes) return {0, 1};
-  const int beg = w.begin(n), end = w.begin(n + 1);
-  if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > p.cand_cap) return {0, 1};
-  const int pid = w.ptr(n);
-  bool ctl_ok = false;
-  int bad = 0;
-  if (pid >= 0) {
-    if (pid >= p.g.n_strings) {
-      bad = 1;
-    } else {
-      const uint32_t word = p.spent[(size_t)b * p.kw + (pid >> 5)];
-      ctl_ok = ((word >> (pid & 31)) & 1u) == 0;
+  const bool n_ok = n >= 0 && n < p.g.n_nodes;
+  const int nn = n_ok ? n : 0;
+  // Node range and pointer id are independent loads; the spent word and the
+  // edge records below are issued before any of them is consumed.
+  const int beg = w.begin(nn), end = w.begin(nn + 1), pid = w.ptr(nn);
+  const bool ok = n_ok && beg >= 0 && end >= beg && end <= p.g.n_edges && end - beg <= p.cand_cap;
+  if (!ok) {
+    if (tid == 0) {
+      sh.ncand = 0;
+      sh.err = 1;
     }
+    __syncthreads();
+    return;
   }
+  int bad = pid >= p.g.n_strings;
+  const uint32_t word = (pid >= 0 && pid < p.g.n_strings) ? p.spent[(size_t)b * p.kw + (pid >> 5)] : 1u;
+  const bool ctl_ok = pid >= 0 && !bad && ((word >> (pid & 31)) & 1u) == 0;
   const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
   const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
   const int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
+  if (end - beg <= 32) {
+    // One warp filters a small node; the others wait at the barrier.
+    if (warp == 0) {
+      const int e = beg + lane;
+      int2 ed = make_int2(0, 0);
+      const bool legal = e < end && edge_legal<kConst>(p, w, cnt, e, sep_ok, stop_ok, ed, bad);
+      const unsigned bal = __ballot_sync(kFull, legal);
+      if (legal) {
+        const int rank = __popc(bal & ((1u << lane) - 1u));
+        if (rank % T == t) {
+          s_tok[rank / T] = ed.x;
+          s_edge[rank / T] = e;
+        }
+      }
+      const unsigned any_bad = __ballot_sync(kFull, bad);
+      if (lane == 0) {
+        sh.ncand = __popc(bal);
+        sh.err = any_bad != 0u;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   int running = 0;
   for (int base = beg; base < end; base += kThreads) {
     const int e = base + tid;
-    bool legal = false;
     int2 ed = make_int2(0, 0);
-    if (e < end) {
-      ed = w.edge(e);
-      if (ed.x < 0 || ed.x >= p.V) {
-        bad = 1;
-      } else if (ed.y >= 0) {
-        if (ed.y >= p.g.n_nodes) bad = 1;
-        else legal = cnt[e] > 0;
-      } else if (ed.y == -1) {
-        legal = sep_ok;
-      } else if (ed.y == -2) {
-        legal = stop_ok;
-      } else {
-        bad = 1;
-      }
-    }
+    const bool legal = e < end && edge_legal<kConst>(p, w, cnt, e, sep_ok, stop_ok, ed, bad);
     const unsigned bal = __ballot_sync(kFull, legal);
-    if (lane == 0) s_scan[warp] = __popc(bal);
+    if (lane == 0) sh.scan[warp] = __popc(bal);
     __syncthreads();
     int woff = 0, tot = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) {
-      const int c = s_scan[i];
+      const int c = sh.scan[i];
       woff += (i < warp) ? c : 0;
       tot += c;
     }
@@ -227,14 +274,19 @@ __device__ FilterResult filter_node(const StepParams& p, const WalkRd<kConst>& w
     __syncthreads();
   }
   const int any_bad = __syncthreads_or(bad);
-  return {running, any_bad};
+  if (tid == 0) {
+    sh.ncand = running;
+    sh.err = any_bad;
+  }
+  __syncthreads();
 }
 
 // Apply the transition of sequence b with winner (best_l, best_t, best_e).
-// Called by every thread of the sequence's last CTA.
+// Called by every thread of the sequence's last CTA; thread 0 returns the
+// sequence's done flag afterwards.
 template <bool kConst>
-__device__ void finish_sequence(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b,
-                                float best_l, int32_t best_t, int32_t best_e, int32_t ncand, int32_t err) {
+__device__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b,
+                               float best_l, int32_t best_t, int32_t best_e, int32_t ncand, int32_t err) {
   const int tid = threadIdx.x;
   int status = TC_OK;
   int32_t new_node = s.node, ptr_done = -1;
@@ -274,6 +326,7 @@ __device__ void finish_sequence(const StepParams& p, const WalkRd<kConst>& w, co
       if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
     }
   }
+  int done = 0;
   if (tid == 0) {
     SeqState ns = s;
     if (status != TC_OK) {
@@ -304,34 +357,49 @@ __device__ void finish_sequence(const StepParams& p, const WalkRd<kConst>& w, co
     }
     if (p.status_out) p.status_out[b] = ns.status;
     if (p.lens_out) p.lens_out[b] = ns.len;
-    if (ns.done && p.ctrl) atomicSub(&p.ctrl->live, 1);
+    if (ns.done) atomicSub(&p.ctrl->live, 1);
+    done = ns.done;
   }
+  return done;
 }
 
-// Fold the per-warp bests, combine the CTAs of sequence b, and let the last
-// CTA apply the transition; then (device form) the grid-wide loop bookkeeping.
+// A live sequence whose length reached the budget stops here (CTA t == 0, thread 0).
+__device__ void stop_out_of_steps(const StepParams& p, const SeqState& s, int b) {
+  SeqState ns = s;
+  ns.status = TC_ERR_MAX_STEPS;
+  ns.done = 1;
+  p.st[b] = ns;
+  if (!p.device_form) {
+    p.tok_out[(size_t)b * p.out_stride] = -1;
+    if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = 0.f;
+  }
+  if (p.status_out) p.status_out[b] = ns.status;
+  if (p.lens_out) p.lens_out[b] = ns.len;
+  atomicSub(&p.ctrl->live, 1);
+}
+
+// Fold the per-warp bests, combine the CTAs of sequence b, let the last CTA
+// apply the transition; then, in a loop-control launch, set the loop condition.
 template <bool kConst>
-__device__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b,
-                          bool active, float wl, int32_t wt, int32_t we, int32_t ncand, int32_t err) {
-  __shared__ float s_wl[kWarps];
-  __shared__ int32_t s_wt[kWarps], s_we[kWarps];
-  __shared__ float s_bl;
-  __shared__ int32_t s_bt, s_be, s_last;
+__device__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int mode,
+                          float wl, int32_t wt, int32_t we, StepShared& sh) {
+  // mode: 0 = idle (stopped or failed before this step), 1 = active, 2 = out of steps now
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tiles = gridDim.x, t = blockIdx.x;
   if (p.stats && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
-  if (active) {
+  if (tid == 0) sh.done_after = 1;
+  if (mode == 1) {
     if (lane == 0) {
-      s_wl[warp] = wl;
-      s_wt[warp] = wt;
-      s_we[warp] = we;
+      sh.wl[warp] = wl;
+      sh.wt[warp] = wt;
+      sh.we[warp] = we;
     }
     __syncthreads();
     if (tid == 0) {
       float bl = -INFINITY;
       int32_t bt = INT_MAX, be = -1;
       for (int i = 0; i < kWarps; ++i)
-        if (better(s_wl[i], s_wt[i], bl, bt)) { bl = s_wl[i]; bt = s_wt[i]; be = s_we[i]; }
+        if (better(sh.wl[i], sh.wt[i], bl, bt)) { bl = sh.wl[i]; bt = sh.wt[i]; be = sh.we[i]; }
       int last = 1;
       if (tiles > 1) {
         Partial* slot = p.part + (size_t)b * tiles;
@@ -353,74 +421,85 @@ __device__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const Se
           p.seq_ticket[b] = 0;
         }
       }
-      s_bl = bl;
-      s_bt = bt;
-      s_be = be;
-      s_last = last;
+      sh.bl = bl;
+      sh.bt = bt;
+      sh.be = be;
+      sh.last = last;
     }
     __syncthreads();
-    if (s_last) finish_sequence<kConst>(p, w, s, b, s_bl, s_bt, s_be, ncand, err);
-  } else if (!p.device_form && t == 0 && tid == 0) {
-    // A stopped or failed sequence reports an idle token.
-    p.tok_out[(size_t)b * p.out_stride] = -1;
-    if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = 0.f;
-    if (p.status_out) p.status_out[b] = s.status;
-    if (p.lens_out) p.lens_out[b] = s.len;
+    if (sh.last) {
+      const int d = finish_sequence<kConst>(p, w, s, b, sh.bl, sh.bt, sh.be, sh.ncand, sh.err);
+      if (tid == 0) sh.done_after = d;
+    }
+  } else if (t == 0 && tid == 0) {
+    if (mode == 2) {
+      stop_out_of_steps(p, s, b);
+    } else if (!p.device_form) {
+      // A stopped or failed sequence reports an idle token.
+      p.tok_out[(size_t)b * p.out_stride] = -1;
+      if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = 0.f;
+      if (p.status_out) p.status_out[b] = s.status;
+      if (p.lens_out) p.lens_out[b] = s.len;
+    }
   }
 
-  if (p.device_form) {
-    __shared__ int32_t s_glast;
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      const uint32_t total = gridDim.x * gridDim.y;
-      const uint32_t g = atomicAdd(&p.ctrl->ticket, 1u);
-      s_glast = (g == total - 1);
-    }
-    __syncthreads();
-    if (s_glast) {
-      __threadfence();
-      const int32_t next = __ldcg(&p.ctrl->step) + 1;
-      const int32_t live = atomicAdd(&p.ctrl->live, 0);
-      const int32_t max_steps = __ldcg(&p.ctrl->max_steps);
-      if (live > 0 && next >= max_steps) {
-        for (int bb = tid; bb < p.B; bb += kThreads) {
-          if (__ldcg(&p.st[bb].done) == 0) {
-            p.st[bb].status = TC_ERR_MAX_STEPS;
-            p.st[bb].done = 1;
-            p.status_out[bb] = TC_ERR_MAX_STEPS;
-          }
-        }
-      }
+  if (p.loop_ctrl) {
+    if (gridDim.x * gridDim.y == 1) {
+      // The only CTA has finished its only sequence: its state decides.
+      if (tid == 0) cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, sh.done_after ? 0u : 1u);
+    } else {
+      __syncthreads();
       if (tid == 0) {
-        p.ctrl->step = next;
-        p.ctrl->ticket = 0;
-        if (live > 0 && next >= max_steps) p.ctrl->live = 0;
-        cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, (live > 0 && next < max_steps) ? 1u : 0u);
+        __threadfence();
+        const uint32_t total = gridDim.x * gridDim.y;
+        const uint32_t g = atomicAdd(&p.ctrl->ticket, 1u);
+        if (g == total - 1) {
+          __threadfence();
+          const int32_t live = atomicAdd(&p.ctrl->live, 0);
+          p.ctrl->ticket = 0u;
+          cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, live > 0 ? 1u : 0u);
+        }
       }
     }
   }
 }
 
-template <int NCH>
-__device__ __forceinline__ const uint16_t* hidden_row(const StepParams& p, int b) {
+// 0: idle, 1: active, 2: live but out of steps.
+__device__ __forceinline__ int seq_mode(const StepParams& p, const SeqState& s) {
+  if (s.done) return 0;
+  return s.len >= p.max_steps ? 2 : 1;
+}
+
+__device__ __forceinline__ const uint16_t* hidden_row(const StepParams& p, const SeqState& s, int b) {
   size_t row = (size_t)b;
-  if (p.device_form) row += (size_t)__ldcg(&p.ctrl->step) * (size_t)p.B;
+  if (p.device_form) row += (size_t)s.len * (size_t)p.B;
   return p.hidden + row * (size_t)p.H;
 }
 
 }  // namespace
 
 // Sparse head: one dot product per legal candidate.
+// Programmatic dependent launch: a step launched as the programmatic
+// dependent of the previous step may be scheduled while that one runs; it
+// waits here until the previous grid has completed and its writes are
+// visible.  Without a programmatic dependency both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_trigger();
+}
+
 template <bool kConst, int NCH>
 __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ int32_t s_scan[kWarps];
+  __shared__ StepShared sh;
+  pdl_enter();
   const int b = blockIdx.y, t = blockIdx.x, T = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
   const SeqState s = p.st[b];
-  const bool active = s.done == 0;
+  const int mode = seq_mode(p, s);
   const int nch = p.H >> 3;
   const int local_cap = (p.cand_cap + T - 1) / T;
   uint4* xs = reinterpret_cast<uint4*>(smem_raw);
@@ -429,18 +508,18 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
 
   float wl = -INFINITY;
   int32_t wt = INT_MAX, we = -1;
-  FilterResult fr{0, 0};
-  if (active) {
-    const uint16_t* x = hidden_row<NCH>(p, b);
+  if (mode == 1) {
+    const uint16_t* x = hidden_row(p, s, b);
     XFrag<NCH> xf;
     if constexpr (NCH > 0) {
       xf.load(x, lane);
     } else {
       for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
     }
-    fr = filter_node<kConst>(p, w, s, b, T, t, s_tok, s_edge, s_scan);
-    if (!fr.err) {
-      const int nlocal = fr.ncand > t ? (fr.ncand - t + T - 1) / T : 0;
+    filter_node<kConst>(p, w, s, b, T, t, s_tok, s_edge, sh);
+    if (!sh.err) {
+      const int nc = sh.ncand;
+      const int nlocal = nc > t ? (nc - t + T - 1) / T : 0;
       for (int l = warp; l < nlocal; l += kWarps) {
         const int32_t tok = s_tok[l];
         const float v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
@@ -448,19 +527,20 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
       }
     }
   }
-  step_tail<kConst>(p, w, s, b, active, wl, wt, we, fr.ncand, fr.err);
+  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh);
 }
 
 // Dense head: every vocabulary row, then the legal mask, then the argmax.
 template <bool kConst, int NCH>
 __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ int32_t s_scan[kWarps];
+  __shared__ StepShared sh;
+  pdl_wait();  // the next step may launch only near the end: its waiting CTAs would take SM slots
   const int b = blockIdx.y, g = blockIdx.x, G = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
   const SeqState s = p.st[b];
-  const bool active = s.done == 0;
+  const int mode = seq_mode(p, s);
   const int nch = p.H >> 3;
   uint4* xs = reinterpret_cast<uint4*>(smem_raw);
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
@@ -468,18 +548,17 @@ __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p
 
   float wl = -INFINITY;
   int32_t wt = INT_MAX, we = -1;
-  FilterResult fr{0, 0};
-  if (active) {
-    const uint16_t* x = hidden_row<NCH>(p, b);
+  if (mode == 1) {
+    const uint16_t* x = hidden_row(p, s, b);
     XFrag<NCH> xf;
     if constexpr (NCH > 0) {
       xf.load(x, lane);
     } else {
       for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
     }
-    fr = filter_node<kConst>(p, w, s, b, 1, 0, s_tok, s_edge, s_scan);
-    if (!fr.err) {
-      const int n = fr.ncand;
+    filter_node<kConst>(p, w, s, b, 1, 0, s_tok, s_edge, sh);
+    if (!sh.err) {
+      const int n = sh.ncand;
       auto consider = [&](int32_t r, float v) {
         // legal iff r is in the ascending candidate list
         int lo = 0, hi = n;
@@ -500,7 +579,8 @@ __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p
       if (r < p.V) consider(r, row_dot<NCH>(p.emb + (size_t)r * p.H, xf, xs, nch, lane));
     }
   }
-  step_tail<kConst>(p, w, s, b, active, wl, wt, we, fr.ncand, fr.err);
+  pdl_trigger();
+  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh);
 }
 
 __global__ void __launch_bounds__(kThreads) reset_kernel(const ResetParams r) {
@@ -526,11 +606,9 @@ __global__ void __launch_bounds__(kThreads) reset_kernel(const ResetParams r) {
     }
     if (b == 0 && tid == 0) {
       if (r.stats) atomicAdd(&r.stats[kStatResetLaunches], 1ull);
-      r.ctrl->step = 0;
       r.ctrl->live = r.B;
-      r.ctrl->max_steps = r.max_steps;
       r.ctrl->ticket = 0u;
-      if (r.cond) cudaGraphSetConditional((cudaGraphConditionalHandle)r.cond, (r.B > 0 && r.max_steps > 0) ? 1u : 0u);
+      if (r.cond) cudaGraphSetConditional((cudaGraphConditionalHandle)r.cond, r.B > 0 ? 1u : 0u);
     }
   }
 }
@@ -571,15 +649,22 @@ int dense_tiles(int B, int num_sms) {
 namespace {
 
 template <bool kConst, int NCH>
-cudaError_t launch_one(const StepParams& p, int head, int tiles, cudaStream_t s) {
+cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaStream_t s) {
   const int nch = p.H >> 3;
   const size_t xbytes = NCH == 0 ? (size_t)nch * 16 : 0;
   const int cap = head == kHeadSparse ? (p.cand_cap + tiles - 1) / tiles : p.cand_cap;
-  const size_t smem = xbytes + 2 * (size_t)cap * sizeof(int32_t);
-  dim3 grid(tiles, p.B), block(kThreads);
-  if (head == kHeadSparse) sparse_step_kernel<kConst, NCH><<<grid, block, smem, s>>>(p);
-  else dense_step_kernel<kConst, NCH><<<grid, block, smem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(tiles, p.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = xbytes + 2 * (size_t)cap * sizeof(int32_t);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (head == kHeadSparse) return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH>, p);
+  return cudaLaunchKernelEx(&cfg, dense_step_kernel<kConst, NCH>, p);
 }
 
 template <bool kConst, int NCH>
@@ -591,12 +676,12 @@ cudaError_t prepare_one() {
 }
 
 template <bool kConst>
-cudaError_t launch_h(const StepParams& p, int head, int tiles, cudaStream_t s) {
+cudaError_t launch_h(const StepParams& p, int head, int tiles, bool pdl, cudaStream_t s) {
   switch (p.H) {
-    case 256: return launch_one<kConst, 1>(p, head, tiles, s);
-    case 2048: return launch_one<kConst, 8>(p, head, tiles, s);
-    case 4096: return launch_one<kConst, 16>(p, head, tiles, s);
-    default: return launch_one<kConst, 0>(p, head, tiles, s);
+    case 256: return launch_one<kConst, 1>(p, head, tiles, pdl, s);
+    case 2048: return launch_one<kConst, 8>(p, head, tiles, pdl, s);
+    case 4096: return launch_one<kConst, 16>(p, head, tiles, pdl, s);
+    default: return launch_one<kConst, 0>(p, head, tiles, pdl, s);
   }
 }
 
@@ -614,8 +699,8 @@ cudaError_t prepare_kernels() {
   return prepare_one<false, 16>();
 }
 
-cudaError_t launch_step(const StepParams& p, bool const_resident, int head, int tiles, cudaStream_t s) {
-  return const_resident ? launch_h<true>(p, head, tiles, s) : launch_h<false>(p, head, tiles, s);
+cudaError_t launch_step(const StepParams& p, bool const_resident, int head, int tiles, cudaStream_t s, bool pdl) {
+  return const_resident ? launch_h<true>(p, head, tiles, pdl, s) : launch_h<false>(p, head, tiles, pdl, s);
 }
 
 cudaError_t launch_reset(const ResetParams& r, cudaStream_t s) {
