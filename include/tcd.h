@@ -280,6 +280,50 @@ tc_status tc_read_seq_state(tc_ctx* ctx, void* stream, int32_t* node, int32_t* e
  */
 tc_status tc_read_stats(tc_ctx* ctx, void* stream, int64_t* out, int32_t reset);
 
+/*
+ * tc_dense_argmax_noalloc - the dense head's masked argmax without any device
+ * allocation.  The pages have no counterpart: this entry point serves callers
+ * that cannot allocate device memory themselves or let a library do it - code
+ * running under a framework whose caching allocator owns the device-memory
+ * budget, plugin hosts that forbid allocation calls, and latency-critical
+ * paths where cudaMalloc or cudaFree may synchronise the device.
+ *
+ * For each sequence b: logit[v] = sum_h E[v, h] * x[b, h] for every row v
+ * (fp32 accumulation, the same lane map and shuffle tree as tc_step, so the
+ * result equals tc_step's dense head bit for bit), restricted to the tokens in
+ * legal[b, 0 .. n_legal[b]) (ascending ids), then the largest logit with ties
+ * to the lower id.
+ *
+ *  emb_bf16     (device) bf16[vocab, hidden], 16-byte aligned.
+ *  hidden_bf16  (device) bf16[batch, hidden], 16-byte aligned; hidden % 8 == 0,
+ *               hidden <= TC_NOALLOC_MAX_HIDDEN.
+ *  legal        (device) int32[batch, legal_stride]; legal_stride <=
+ *               TC_NOALLOC_MAX_LEGAL.  n_legal (device) int32[batch].
+ *  tok_out      (device) int32[batch]: the winner, or -1 when no listed token
+ *               has a comparable logit (empty list, or NaN logits).
+ *  logit_out    (device) float[batch]: its logit (0 with -1).
+ *  1 <= batch <= TC_NOALLOC_MAX_BATCH.  Sizes beyond the limits return
+ *  TC_ERR_CAPACITY with a message in tc_last_error_message.
+ *
+ * Memory: it calls no allocating routine.  Its scratch is a file-scope
+ * __device__ array of TC_NOALLOC_MAX_SLOTS 8-byte partial results plus
+ * TC_NOALLOC_MAX_BATCH counters (about 64 KiB), which every GPU that loads the
+ * library holds until the process exits.  The first call on a device looks up
+ * the array's device address (once per device, with that device current);
+ * make that first call before any stream capture.  Every call shares the
+ * array and clears the counters it uses with a stream-ordered memset; calls
+ * that overlap on the GPU (for example on two streams) race and give wrong
+ * results.  Runs on the current device, asynchronously on `stream`.
+ */
+#define TC_NOALLOC_MAX_BATCH 64
+#define TC_NOALLOC_MAX_SLOTS 8192
+#define TC_NOALLOC_MAX_HIDDEN 8192
+#define TC_NOALLOC_MAX_LEGAL 4096
+tc_status tc_dense_argmax_noalloc(const void* emb_bf16, int32_t vocab, int32_t hidden,
+                                  const void* hidden_bf16, int32_t batch, const int32_t* legal,
+                                  int32_t legal_stride, const int32_t* n_legal, int32_t* tok_out,
+                                  float* logit_out, void* stream);
+
 /* tc_status_str - a static name for a status code. */
 const char* tc_status_str(tc_status status);
 
