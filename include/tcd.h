@@ -70,7 +70,11 @@ enum {
 /* Output head (tc_step / tc_decode). */
 enum {
   TC_HEAD_SPARSE = 0,     /* one embedding-row dot product per legal candidate */
-  TC_HEAD_DENSE = 1       /* every vocabulary row, then the legal mask, then the argmax (cross-check) */
+  TC_HEAD_DENSE = 1,      /* every vocabulary row, then the legal mask, then the argmax (cross-check) */
+  TC_HEAD_UNION_GEMM = 2, /* batches: the union of all sequences' legal rows as one tcgen05 GEMM,
+                             each sequence's argmax over its own candidates (batch <= 256, hidden % 64 == 0) */
+  TC_HEAD_DENSE_GEMM = 3  /* batches: every vocabulary row as one tcgen05 GEMM, then each sequence's
+                             legal mask and argmax (the dense comparison for TC_HEAD_UNION_GEMM) */
 };
 
 /* Bytes of __constant__ memory reserved for one walk image. */

@@ -148,3 +148,58 @@ def test_batched_host_equals_graph(tcd):
     (h2, h), = _batched_run(tcd, "unstructured", 1, mode="host")
     for x, y in zip(g, h):
         assert np.array_equal(x, y)
+
+
+def _run_head(tcd, name, head, n_batches=1, batch=None, mode="graph"):
+    w = workload(name)
+    B = batch or w.batch
+    ctx, _ = make_ctx(tcd, name, max_batch=B)
+    buf = DecodeBuffers(w.max_steps, B, w.hidden, w.max_steps)
+    out = []
+    for i in range(n_batches):
+        hid = w.hidden_states(i * B, B)
+        buf.load(hid)
+        out.append((hid, buf.run(ctx, w.k, head=head, mode=mode)))
+    ctx.close()
+    return out
+
+
+def test_tiny_union_gemm_bitexact(tcd):
+    """The union-of-legal-rows tcgen05 GEMM on integer-valued inputs: tensor-core
+    fp32 sums of these values are exact, so tokens and logits equal the oracle's."""
+    w = workload("tiny")
+    (hid, out), = _run_head(tcd, "tiny", tcd.HEAD_UNION_GEMM, batch=w.n_queries)
+    assert np.all(out[3] == 0)
+    check_against_oracle("tiny", hid, out, w.k, w.max_steps, exact=True)
+
+
+def test_tiny_gemm_heads_equal_sparse(tcd):
+    w = workload("tiny")
+    (_, sp), = _run_head(tcd, "tiny", tcd.HEAD_SPARSE, batch=w.n_queries)
+    (_, un), = _run_head(tcd, "tiny", tcd.HEAD_UNION_GEMM, batch=w.n_queries)
+    (_, dg), = _run_head(tcd, "tiny", tcd.HEAD_DENSE_GEMM, batch=w.n_queries)
+    for x, y, z in zip(sp, un, dg):
+        assert np.array_equal(x, y) and np.array_equal(x, z)
+
+
+def test_tensor_batch_union_gemm_b256(tcd):
+    """B=256, k=3 over the 1000-tool catalog with the union GEMM head."""
+    w = workload("tensor_batch")
+    (hid, out), = _run_head(tcd, "tensor_batch", tcd.HEAD_UNION_GEMM)
+    assert np.all(out[3] == 0)
+    check_against_oracle("tensor_batch", hid, out, w.k, w.max_steps, exact=False)
+
+
+def test_union_gemm_equals_dense_gemm_b64(tcd):
+    """Both GEMM heads run the same MMA sequence per (sequence, row): bitwise equal."""
+    (_, un), = _run_head(tcd, "batched", tcd.HEAD_UNION_GEMM)
+    (_, dg), = _run_head(tcd, "batched", tcd.HEAD_DENSE_GEMM)
+    for x, y in zip(un, dg):
+        assert np.array_equal(x, y)
+
+
+def test_union_gemm_host_equals_graph(tcd):
+    (_, g), = _run_head(tcd, "batched", tcd.HEAD_UNION_GEMM, mode="graph")
+    (_, h), = _run_head(tcd, "batched", tcd.HEAD_UNION_GEMM, mode="host")
+    for x, y in zip(g, h):
+        assert np.array_equal(x, y)

@@ -27,7 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 TC_OK = 0
 STATUS_NAMES = {}
 RES_AUTO, RES_CONST, RES_GLOBAL = 0, 1, 2
-HEAD_SPARSE, HEAD_DENSE = 0, 1
+HEAD_SPARSE, HEAD_DENSE, HEAD_UNION_GEMM, HEAD_DENSE_GEMM = 0, 1, 2, 3
 TC_ERR_EMPTY_MASK, TC_ERR_NO_LIVE_EDGE, TC_ERR_MAX_STEPS, TC_ERR_BOUNDS = 16, 17, 18, 19
 CONST_CAPACITY_BYTES = 63 * 1024
 

@@ -1,0 +1,38 @@
+// Host-visible interface of the tcgen05 GEMM with a masked-argmax epilogue.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tcd {
+
+// Best candidate of one sequence within one 256-column tile.
+struct GemmPartial {
+  float logit;
+  int32_t col;  // INT32_MAX when the sequence has no candidate in the tile
+};
+
+struct GemmParams {
+  const uint16_t* hidden;    // bf16 activations
+  const int64_t* xrow;       // [B] element offset of each sequence's hidden row; -1: no row (inactive)
+  int32_t B;                 // sequences, <= 256
+  const uint16_t* emb;       // bf16 [V, H]
+  int32_t H;                 // multiple of 64
+  const int32_t* row_list;   // [n_cols] embedding row of each column, or null (column = row)
+  const int32_t* n_cols_ptr; // device column count (read at kernel start), or null
+  int32_t n_cols_fixed;      // column count when n_cols_ptr is null
+  const int32_t* cand_col;   // [B, C] ascending columns of each sequence's legal candidates
+  const int32_t* ncand;      // [B]
+  int32_t C;
+  GemmPartial* part;         // [B, max_tiles]
+  int32_t max_tiles;
+  int32_t* err;              // set to 1 when a wait timed out
+};
+
+size_t gemm_smem_bytes(int m_tiles);
+int gemm_tile_cols();
+// Opt in to the GEMM's dynamic shared memory (current device).
+cudaError_t prepare_gemm();
+cudaError_t launch_union_gemm(const GemmParams& p, int num_ctas, cudaStream_t s);
+
+}  // namespace tcd

@@ -51,6 +51,27 @@ struct GrammarView {
   const int32_t* path;       // [total tokens]
 };
 
+struct GemmPartial;  // gemm_tc.h
+
+// Scratch of the GEMM heads (candidate lists in global memory, the union of
+// legal rows, per-(sequence, column tile) partial results).
+struct HeadScratch {
+  int32_t* cand_tok;        // [B, C] legal tokens of each sequence, ascending
+  int32_t* cand_edge;       // [B, C] their edges
+  int32_t* cand_col;        // [B, C] their GEMM columns (union index, or the token for the dense GEMM)
+  int32_t* ncand;           // [B]
+  int32_t* errf;            // [B] filter found an out-of-range index
+  int64_t* xrow;            // [B] element offset of the sequence's hidden row, -1 if not stepping
+  uint32_t* ubits;          // [ceil(V/32)] union bitmap (all zero between steps)
+  int32_t* ulist;           // [V] union of legal tokens, ascending
+  int32_t* umap;            // [V] token -> union index (valid for members only)
+  int32_t* n_union;         // [1]
+  GemmPartial* part;        // [B, max_tiles]
+  int32_t max_tiles;
+  int32_t union_mode;       // 1: columns are the union; 0: every vocabulary row
+  int32_t* gemm_err;        // [1] GEMM wait timeout
+};
+
 struct StepParams {
   GrammarView g;
   const uint16_t* emb;      // bf16 [V, H]
@@ -75,6 +96,7 @@ struct StepParams {
   int32_t device_form;      // 1: hidden row and output position follow each sequence's own length
   int32_t loop_ctrl;        // 1: this launch sets the loop's condition (last step of a loop body)
   unsigned long long* stats;  // optional counters, see StatSlot
+  HeadScratch hs;           // GEMM heads only
 };
 
 // Cumulative counters kept by the kernels (one atomic per launch / per sequence step).
@@ -97,7 +119,7 @@ struct ResetParams {
   unsigned long long* stats;
 };
 
-enum Head { kHeadSparse = 0, kHeadDense = 1 };
+enum Head { kHeadSparse = 0, kHeadDense = 1, kHeadUnionGemm = 2, kHeadDenseGemm = 3 };
 
 // Number of CTAs per sequence the sparse step uses for a grammar of the given
 // largest fan-out at batch B, and the dense step's CTAs per sequence.
@@ -112,6 +134,9 @@ cudaError_t launch_reset(const ResetParams& r, cudaStream_t s);
 cudaError_t launch_step(const StepParams& p, bool const_resident, int head, int tiles, cudaStream_t s,
                         bool pdl = false);
 cudaError_t launch_finalize(const StepParams& p, cudaStream_t s);
+// One step of a GEMM head: candidate filter, [union compaction], tcgen05 GEMM
+// with masked-argmax epilogue, per-sequence fold and transition.
+cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head, int gemm_ctas, cudaStream_t s);
 // Copy a walk image (device memory) into the constant bank, stream-ordered.
 cudaError_t const_upload(const void* d_src, size_t bytes, cudaStream_t s);
 

@@ -25,6 +25,7 @@
 #include <string>
 #include <vector>
 
+#include "gemm_tc.h"
 #include "kernels.h"
 #include "tcd.h"
 #include "tcd_internal.h"
@@ -145,6 +146,8 @@ struct tc_ctx {
   uint32_t* d_seq_ticket = nullptr;
   Ctrl* d_ctrl = nullptr;
   unsigned long long* d_stats = nullptr;
+  HeadScratch hs{};           // GEMM-head scratch, allocated on first use
+  bool hs_ready = false;
   int32_t* h_live = nullptr;  // pinned
   cudaStream_t capture_stream = nullptr;
   std::vector<tc_graph*> cache;  // most recently used last
@@ -155,6 +158,77 @@ namespace {
 
 int tiles_for(const tc_ctx* c, const DevGrammar* g, int head, int B) {
   return head == TC_HEAD_SPARSE ? sparse_tiles(g->max_fanout, B, c->num_sms) : dense_tiles(B, c->num_sms);
+}
+
+bool is_gemm_head(int head) { return head == TC_HEAD_UNION_GEMM || head == TC_HEAD_DENSE_GEMM; }
+
+int gemm_ctas(const tc_ctx* c) { return std::min(c->num_sms, c->hs.max_tiles); }
+
+// Scratch of the GEMM heads, sized for max_batch sequences and the whole vocabulary.
+tc_status ensure_gemm_scratch(tc_ctx* c) {
+  if (c->hs_ready) return TC_OK;
+  HeadScratch& h = c->hs;
+  const size_t BC = (size_t)c->max_batch * c->cand_cap, V = (size_t)c->V;
+  h.max_tiles = (int32_t)((V + gemm_tile_cols() - 1) / gemm_tile_cols());
+  cudaError_t e = cudaMalloc(&h.cand_tok, BC * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.cand_edge, BC * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.cand_col, BC * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.ncand, (size_t)c->max_batch * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.errf, (size_t)c->max_batch * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.xrow, (size_t)c->max_batch * 8);
+  if (e == cudaSuccess) e = cudaMalloc(&h.ubits, ((V + 31) / 32) * 4);
+  if (e == cudaSuccess) e = cudaMemset(h.ubits, 0, ((V + 31) / 32) * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.ulist, V * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.umap, V * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.n_union, 4);
+  if (e == cudaSuccess) e = cudaMemset(h.n_union, 0, 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.part, (size_t)c->max_batch * h.max_tiles * sizeof(GemmPartial));
+  if (e == cudaSuccess) e = cudaMalloc(&h.gemm_err, 4);
+  if (e == cudaSuccess) e = cudaMemset(h.gemm_err, 0, 4);
+  if (e != cudaSuccess) return cuda_fail(e, "GEMM-head scratch");
+  c->hs_ready = true;
+  return TC_OK;
+}
+
+void free_gemm_scratch(tc_ctx* c) {
+  HeadScratch& h = c->hs;
+  cudaFree(h.cand_tok);
+  cudaFree(h.cand_edge);
+  cudaFree(h.cand_col);
+  cudaFree(h.ncand);
+  cudaFree(h.errf);
+  cudaFree(h.xrow);
+  cudaFree(h.ubits);
+  cudaFree(h.ulist);
+  cudaFree(h.umap);
+  cudaFree(h.n_union);
+  cudaFree(h.part);
+  cudaFree(h.gemm_err);
+  c->hs_ready = false;
+}
+
+// Checks shared by every entry point that runs a step with `head`.
+tc_status check_head(tc_ctx* c, int head, int B) {
+  if (head != TC_HEAD_SPARSE && head != TC_HEAD_DENSE && !is_gemm_head(head)) return TC_ERR_INVALID_ARG;
+  if (is_gemm_head(head)) {
+    if (B > 256 || c->H % 64 != 0) {
+      set_error_message("GEMM heads need batch <= 256 and hidden % 64 == 0");
+      return TC_ERR_UNSUPPORTED;
+    }
+    return ensure_gemm_scratch(c);
+  }
+  return TC_OK;
+}
+
+// One step of any head.
+cudaError_t launch_any_step(tc_ctx* c, DevGrammar* g, const StepParams& p, int head, cudaStream_t s, bool pdl) {
+  const bool cst = g->residency == TC_RES_CONST;
+  if (is_gemm_head(head)) {
+    StepParams q = p;
+    q.hs = c->hs;
+    return launch_gemm_step(q, cst, head, gemm_ctas(c), s);
+  }
+  return launch_step(p, cst, head, tiles_for(c, g, head, p.B), s, pdl);
 }
 
 StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
@@ -216,8 +290,7 @@ tc_status check_decode_args(tc_ctx* c, const void* hidden, int32_t n_steps, int3
   if (batch < 1 || batch > c->max_batch) return TC_ERR_CAPACITY;
   if (k < 1 || k > c->bound->n_strings) return TC_ERR_K_RANGE;
   if (max_steps < 1 || max_steps > n_steps) return TC_ERR_INVALID_ARG;
-  if (head != TC_HEAD_SPARSE && head != TC_HEAD_DENSE) return TC_ERR_INVALID_ARG;
-  return TC_OK;
+  return check_head(c, head, batch);
 }
 
 void destroy_graph(tc_graph* gr) {
@@ -304,8 +377,7 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
   // A sequence that has stopped makes the remaining steps of the body no-ops.
   for (int u = 0; u < kLoopUnroll; ++u) {
     p.loop_ctrl = (u == kLoopUnroll - 1);
-    if ((e = launch_step(p, g->residency == TC_RES_CONST, key.head, tiles_for(c, g, key.head, key.batch), cs,
-                         /*pdl=*/u > 0)) != cudaSuccess)
+    if ((e = launch_any_step(c, g, p, key.head, cs, /*pdl=*/u > 0)) != cudaSuccess)
       return fail(e, "step kernel capture");
   }
   cudaGraph_t body_ended = nullptr;
@@ -355,6 +427,7 @@ extern "C" tc_status tc_ctx_create(int32_t device, const void* emb_bf16, int32_t
   c->cand_cap = cand_cap;
   cudaError_t e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
   if (e == cudaSuccess) e = prepare_kernels();
+  if (e == cudaSuccess) e = prepare_gemm();
   if (e == cudaSuccess) e = cudaMalloc(&c->d_part, sizeof(Partial) * (size_t)max_batch * kMaxTiles);
   if (e == cudaSuccess) e = cudaMalloc(&c->d_seq_ticket, sizeof(uint32_t) * (size_t)max_batch);
   if (e == cudaSuccess) e = cudaMalloc(&c->d_ctrl, sizeof(Ctrl));
@@ -388,6 +461,7 @@ extern "C" void tc_ctx_destroy(tc_ctx* c) {
     g->release();
     delete g;
   }
+  free_gemm_scratch(c);
   cudaFree(c->d_part);
   cudaFree(c->d_seq_ticket);
   cudaFree(c->d_ctrl);
@@ -493,7 +567,6 @@ extern "C" tc_status tc_reset(tc_ctx* c, int32_t batch, int32_t k, void* stream)
 extern "C" tc_status tc_step(tc_ctx* c, const void* hidden, int32_t head, int32_t* tok_out, float* logit_out,
                              int32_t* status_out, void* stream) {
   if (!c || !hidden || !tok_out) return TC_ERR_INVALID_ARG;
-  if (head != TC_HEAD_SPARSE && head != TC_HEAD_DENSE) return TC_ERR_INVALID_ARG;
   if (misaligned(hidden, 16) || misaligned(tok_out, 4) || misaligned(logit_out, 4) || misaligned(status_out, 4)) {
     set_error_message("tc_step: hidden states must be 16-byte aligned and outputs 4-byte aligned");
     return TC_ERR_INVALID_ARG;
@@ -501,8 +574,10 @@ extern "C" tc_status tc_step(tc_ctx* c, const void* hidden, int32_t head, int32_
   DevGrammar* g = c->bound;
   if (!g || g->batch < 1) return TC_ERR_NOT_BOUND;
   DeviceGuard dg(c->device);
+  tc_status rc = check_head(c, head, g->batch);
+  if (rc != TC_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  tc_status rc = ensure_const(c, g, s);
+  rc = ensure_const(c, g, s);
   if (rc != TC_OK) return rc;
   StepParams p = step_params(c, g, g->batch);
   p.hidden = static_cast<const uint16_t*>(hidden);
@@ -510,7 +585,7 @@ extern "C" tc_status tc_step(tc_ctx* c, const void* hidden, int32_t head, int32_
   p.logit_out = logit_out;
   p.status_out = status_out;
   p.out_stride = 1;
-  TC_CUDA(launch_step(p, g->residency == TC_RES_CONST, head, tiles_for(c, g, head, g->batch), s));
+  TC_CUDA(launch_any_step(c, g, p, head, s, false));
   return TC_OK;
 }
 
@@ -595,7 +670,6 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
   TC_CUDA(launch_reset(r, s));
   g->batch = batch;
   g->k = k;
-  const int tiles = tiles_for(c, g, head, batch);
   const size_t row = (size_t)batch * (size_t)c->H;
   for (int32_t t = 0; t < max_steps; ++t) {
     StepParams p = step_params(c, g, batch);
@@ -606,7 +680,7 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
     p.lens_out = lens;
     p.out_stride = max_steps;
     p.max_steps = max_steps;
-    TC_CUDA(launch_step(p, g->residency == TC_RES_CONST, head, tiles, s));
+    TC_CUDA(launch_any_step(c, g, p, head, s, false));
     TC_CUDA(cudaMemcpyAsync(c->h_live, &c->d_ctrl->live, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
     TC_CUDA(cudaStreamSynchronize(s));
     if (*c->h_live <= 0) break;

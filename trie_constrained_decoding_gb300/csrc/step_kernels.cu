@@ -33,6 +33,7 @@
 
 #include <climits>
 
+#include "gemm_tc.h"
 #include "kernels.h"
 #include "tcd.h"
 
@@ -43,6 +44,7 @@ __constant__ int32_t c_walk[TC_CONST_CAPACITY_BYTES / 4];
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int gemm_tile_cols_dev = 256;  // columns per GEMM tile (gemm_tc.cu)
 
 template <bool kConst>
 struct WalkRd {
@@ -628,6 +630,168 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const StepParams p) 
   if (threadIdx.x == 0 && p.ctrl) p.ctrl->live = 0;
 }
 
+// ---------------------------------------------------------------- GEMM heads
+//
+// One step of the union head ("The sparse output layer": in batched form the
+// union of legal rows across the batch is bounded by the trie) or of the dense
+// GEMM head runs as: candidate filter per sequence -> (union only) compaction
+// of the union bitmap into a sorted row list -> tcgen05 GEMM over those rows
+// with a masked-argmax epilogue -> per-sequence fold of the column-tile
+// partials and the transition.
+
+// Grid (1, B): filter the node of sequence b into global candidate lists.
+template <bool kConst>
+__global__ void __launch_bounds__(kThreads) cand_filter_kernel(const StepParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ StepShared sh;
+  const int b = blockIdx.y, tid = threadIdx.x;
+  const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
+  const SeqState s = p.st[b];
+  const int mode = seq_mode(p, s);
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw);
+  int32_t* s_edge = s_tok + p.cand_cap;
+  const HeadScratch& hs = p.hs;
+  if (mode != 1) {
+    if (tid == 0) {
+      hs.xrow[b] = -1;
+      hs.ncand[b] = 0;
+      hs.errf[b] = 0;
+    }
+    return;
+  }
+  filter_node<kConst>(p, w, s, b, 1, 0, s_tok, s_edge, sh);
+  const int n = sh.err ? 0 : sh.ncand;
+  int32_t* ct = hs.cand_tok + (size_t)b * p.cand_cap;
+  int32_t* ce = hs.cand_edge + (size_t)b * p.cand_cap;
+  int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
+  for (int i = tid; i < n; i += kThreads) {
+    const int32_t tok = s_tok[i];
+    ct[i] = tok;
+    ce[i] = s_edge[i];
+    if (hs.union_mode) atomicOr(&hs.ubits[tok >> 5], 1u << (tok & 31));
+    else cc[i] = tok;
+  }
+  if (tid == 0) {
+    hs.ncand[b] = n;
+    hs.errf[b] = sh.err;
+    hs.xrow[b] = (int64_t)(((size_t)(p.device_form ? s.len : 0) * (size_t)p.B + (size_t)b) * (size_t)p.H);
+  }
+}
+
+// One CTA of 1024 threads: union bitmap -> ascending row list, token -> index
+// map, bitmap cleared for the next step; then every candidate's column.
+constexpr int kCompactThreads = 1024;
+__global__ void __launch_bounds__(kCompactThreads) union_compact_kernel(const StepParams p) {
+  __shared__ int32_t s_warp[kCompactThreads / 32];
+  const HeadScratch& hs = p.hs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int words = (p.V + 31) >> 5;
+  const int per = (words + kCompactThreads - 1) / kCompactThreads;
+  const int w0 = tid * per, w1 = min(words, w0 + per);
+  int cnt = 0;
+  for (int i = w0; i < w1; ++i) cnt += __popc(hs.ubits[i]);
+  // block-wide exclusive scan of cnt
+  int incl = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = s_warp[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(kFull, v, o);
+      if (lane >= o) v += u;
+    }
+    s_warp[lane] = v;  // inclusive per-warp totals
+  }
+  __syncthreads();
+  int idx = (warp > 0 ? s_warp[warp - 1] : 0) + incl - cnt;
+  for (int i = w0; i < w1; ++i) {
+    uint32_t bits = hs.ubits[i];
+    if (bits) hs.ubits[i] = 0u;
+    while (bits) {
+      const int bit = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const int tok = i * 32 + bit;
+      hs.ulist[idx] = tok;
+      hs.umap[tok] = idx;
+      ++idx;
+    }
+  }
+  if (tid == 0) *hs.n_union = s_warp[kCompactThreads / 32 - 1];
+  __syncthreads();
+  for (int b = 0; b < p.B; ++b) {
+    const int n = hs.ncand[b];
+    const int32_t* ct = hs.cand_tok + (size_t)b * p.cand_cap;
+    int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
+    for (int i = tid; i < n; i += kCompactThreads) cc[i] = hs.umap[ct[i]];
+  }
+}
+
+// Grid (1, B): fold sequence b's column-tile partials, map the winning column
+// back to its token and edge, and apply the transition (step_tail).
+template <bool kConst>
+__global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams p) {
+  __shared__ StepShared sh;
+  const int b = blockIdx.y, tid = threadIdx.x;
+  const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
+  const SeqState s = p.st[b];
+  const int mode = seq_mode(p, s);
+  const HeadScratch& hs = p.hs;
+  float wl = -INFINITY;
+  int32_t wt = INT_MAX, we = -1;
+  if (mode == 1) {
+    const int n = hs.ncand[b];
+    const int err = hs.errf[b];
+    const int n_cols = hs.union_mode ? *hs.n_union : p.V;
+    const int n_tiles = (n_cols + gemm_tile_cols_dev - 1) / gemm_tile_cols_dev;
+    int32_t bc = INT_MAX;
+    if (!err && n > 0) {
+      const GemmPartial* part = hs.part + (size_t)b * hs.max_tiles;
+      for (int t = tid; t < n_tiles && t < hs.max_tiles; t += kThreads) {
+        const GemmPartial q = part[t];
+        if (q.col != INT_MAX && better(q.logit, q.col, wl, bc)) {
+          wl = q.logit;
+          bc = q.col;
+        }
+      }
+      // warp-wide fold: (logit, column) is a total order, so every lane ends with the same best
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ol = __shfl_xor_sync(kFull, wl, o);
+        const int32_t oc = __shfl_xor_sync(kFull, bc, o);
+        if (better(ol, oc, wl, bc)) {
+          wl = ol;
+          bc = oc;
+        }
+      }
+      if (bc != INT_MAX) {
+        // columns ascend with tokens, so the column order breaks ties like the token order
+        const int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
+        int lo = 0, hi = n;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (cc[mid] < bc) lo = mid + 1; else hi = mid;
+        }
+        if (lo < n && cc[lo] == bc) {
+          wt = hs.cand_tok[(size_t)b * p.cand_cap + lo];
+          we = hs.cand_edge[(size_t)b * p.cand_cap + lo];
+        } else {
+          wl = -INFINITY;  // cannot happen: the column came from this sequence's list
+        }
+      }
+    }
+    if (tid == 0) {
+      sh.ncand = n;
+      sh.err = err;
+    }
+    __syncthreads();
+  }
+  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh);
+}
+
 // ---------------------------------------------------------------- launchers
 
 int sparse_tiles(int max_fanout, int B, int num_sms) {
@@ -708,6 +872,42 @@ cudaError_t launch_reset(const ResetParams& r, cudaStream_t s) {
   if (bx < 1) bx = 1;
   if (bx > 64) bx = 64;
   reset_kernel<<<dim3(bx, r.B), kThreads, 0, s>>>(r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head, int gemm_ctas, cudaStream_t s) {
+  StepParams q = p;
+  q.hs.union_mode = head == kHeadUnionGemm;
+  const size_t fsmem = 2 * (size_t)p.cand_cap * sizeof(int32_t);
+  StepParams no_ctrl = q;
+  no_ctrl.loop_ctrl = 0;
+  no_ctrl.stats = nullptr;
+  if (const_resident) cand_filter_kernel<true><<<dim3(1, p.B), kThreads, fsmem, s>>>(no_ctrl);
+  else cand_filter_kernel<false><<<dim3(1, p.B), kThreads, fsmem, s>>>(no_ctrl);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (q.hs.union_mode) {
+    union_compact_kernel<<<1, kCompactThreads, 0, s>>>(no_ctrl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  GemmParams gp{};
+  gp.hidden = p.hidden;
+  gp.xrow = q.hs.xrow;
+  gp.B = p.B;
+  gp.emb = p.emb;
+  gp.H = p.H;
+  gp.row_list = q.hs.union_mode ? q.hs.ulist : nullptr;
+  gp.n_cols_ptr = q.hs.union_mode ? q.hs.n_union : nullptr;
+  gp.n_cols_fixed = p.V;
+  gp.cand_col = q.hs.cand_col;
+  gp.ncand = q.hs.ncand;
+  gp.C = p.cand_cap;
+  gp.part = q.hs.part;
+  gp.max_tiles = q.hs.max_tiles;
+  gp.err = q.hs.gemm_err;
+  if ((e = launch_union_gemm(gp, gemm_ctas, s)) != cudaSuccess) return e;
+  if (const_resident) gemm_finish_kernel<true><<<dim3(1, p.B), kThreads, 0, s>>>(q);
+  else gemm_finish_kernel<false><<<dim3(1, p.B), kThreads, 0, s>>>(q);
   return cudaGetLastError();
 }
 
