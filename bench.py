@@ -57,7 +57,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="large_head", choices=sorted(I.WORKLOADS))
-    ap.add_argument("--head", choices=["sparse", "dense"], default="sparse")
+    ap.add_argument("--head", choices=["sparse", "dense", "union", "dense_gemm"], default="sparse",
+                    help="output head: sparse rows, dense GEMV + mask, union-of-legal-rows tcgen05 GEMM, "
+                         "or full-vocabulary tcgen05 GEMM + mask")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-extras", action="store_true", help="skip the dense/host-loop/e2e/roofline passes")
     ap.add_argument("--residency", choices=["auto", "const", "global"], default=None,
@@ -219,7 +221,8 @@ def run_ours(args):
     dev = torch.cuda.current_device()
     stream = torch.cuda.current_stream()
     w = I.WORKLOADS[args.workload]()
-    head = tcd.HEAD_SPARSE if args.head == "sparse" else tcd.HEAD_DENSE
+    head = {"sparse": tcd.HEAD_SPARSE, "dense": tcd.HEAD_DENSE, "union": tcd.HEAD_UNION_GEMM,
+            "dense_gemm": tcd.HEAD_DENSE_GEMM}[args.head]
     B, S, H = w.batch, w.max_steps, w.hidden
 
     emb_bits = w.embedding()
@@ -231,7 +234,7 @@ def run_ours(args):
     res = {"const": tcd.RES_CONST, "global": tcd.RES_GLOBAL, "auto": tcd.RES_AUTO}[args.residency or w.residency]
     ctx.bind(trie, res)
 
-    n_batches = max(1, w.n_queries // B)
+    n_batches = max(1, min(w.n_queries // B, 2048 // B))
     K, W = args.steps, args.warmup
     qids = query_ids(n_batches, rank, world, K + W)
     hh = host_hidden(w, qids)
@@ -347,6 +350,7 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     B, S, H = w.batch, w.max_steps, w.hidden
     out = {}
     n_roof = min(len(qids), 200 if B == 1 else 8)
+    gemm_head = head in (tcd.HEAD_UNION_GEMM, tcd.HEAD_DENSE_GEMM)
 
     # --- step kernel alone: tc_step (same kernel body, host-argument form), one
     # event pair per launch; L2 flushed before every launch (cold) or not (warm).
@@ -389,7 +393,8 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     warm_ms = kernel_pass(False)
     warm_mean = sum(warm_ms) / len(warm_ms)
     roof = {"bound": "hbm", "achieved": achieved, "peak": None, "unit": "GB/s", "frac": None, "traffic": None,
-            "kernel": "sparse_step_kernel" if head == tcd.HEAD_SPARSE else "dense_step_kernel",
+            "kernel": {tcd.HEAD_SPARSE: "sparse_step_kernel", tcd.HEAD_DENSE: "dense_step_kernel"}.get(
+                head, "GEMM-head step (filter, union compaction, tcgen05 GEMM, finish)"),
             "algorithmic_bytes_per_launch": algo_bytes / launches,
             "mean_launch_us_cold_l2": mean_ms * 1000.0, "mean_launch_us_warm_l2": warm_mean * 1000.0,
             "achieved_warm_gbs": algo_bytes / launches / (warm_mean / 1000.0) / 1e9,
@@ -399,7 +404,8 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
                     "bytes = candidate rows x 2H + hidden state 2H per sequence step"}
 
     # --- dense head + mask over the same queries (subset)
-    if head == tcd.HEAD_SPARSE:
+    if head in (tcd.HEAD_SPARSE, tcd.HEAD_UNION_GEMM):
+        dense_head = tcd.HEAD_DENSE if B == 1 else tcd.HEAD_DENSE_GEMM
         n_dense = min(len(qids), 20 if B == 1 else 2)
         ctx.stats(reset=True)
         evs = []
@@ -408,14 +414,19 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=tcd.HEAD_DENSE)
+            ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=dense_head)
             b.record(stream)
             evs.append((a, b))
         torch.cuda.synchronize()
         st = ctx.stats(reset=True)
         ms = sum(a.elapsed_time(b) for a, b in evs)
+        out["dense_head"] = "dense GEMV + mask" if dense_head == tcd.HEAD_DENSE else "tcgen05 dense GEMM + mask"
         out["dense_head_steps_per_s"] = st["step_launches"] / (ms / 1000.0)
-        out["dense_head_gbs"] = st["seq_steps"] * (w.vocab * 2.0 * H) / (ms / 1000.0) / 1e9
+        # bytes of embedding the dense head must read per step: all V rows once
+        # per sequence for the GEMV, once per step for the GEMM
+        per_step = w.vocab * 2.0 * H
+        reads = st["seq_steps"] * per_step if dense_head == tcd.HEAD_DENSE else st["step_launches"] * per_step
+        out["dense_head_gbs"] = reads / (ms / 1000.0) / 1e9
 
     # --- host-driven loop (one synchronising read per step) over a subset
     n_host = min(len(qids), 100 if B == 1 else 4)

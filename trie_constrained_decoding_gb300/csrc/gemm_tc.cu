@@ -155,13 +155,16 @@ __global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmPara
 
   const int n_cols = p.n_cols_ptr ? *p.n_cols_ptr : p.n_cols_fixed;
   const int n_tiles = (n_cols + kTileN - 1) / kTileN;
-  const int KT = p.H / kTileK;
+  const int KS = p.ksplit;              // K splits per column tile (divides H / 64)
+  const int KT = p.H / kTileK / KS;     // k-steps per task
   constexpr uint32_t idesc = idesc_bf16(128, kTileN);
   long long g = 0;  // global k-step counter of this CTA (stage = g % kStages)
   bool failed = false;
 
-  for (int tile = blockIdx.x; tile < n_tiles && !failed; tile += gridDim.x) {
+  for (int task = blockIdx.x; task < n_tiles * KS && !failed; task += gridDim.x) {
+    const int tile = task / KS, split = task % KS;
     const int n0 = tile * kTileN;
+    const int kbase = split * KT;
     for (int r = tid; r < kTileN; r += kThreadsG) {
       const int col = n0 + r;
       hdr->rows[r] = col < n_cols ? (p.row_list ? p.row_list[col] : col) : -1;
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmPara
     auto load_stage = [&](int kt, int stage) {
       const uint32_t a_base = tiles_s + stage * stage_bytes;
       const uint32_t b_base = a_base + MT * kATileBytes;
-      const int k0 = kt * kTileK;
+      const int k0 = (kbase + kt) * kTileK;
       for (int i = tid; i < MT * 128 * 8; i += kThreadsG) {
         const int r = i >> 3, c = i & 7;
         const int64_t off = r < p.B ? p.xrow[r] : -1;
@@ -258,12 +261,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmPara
       }
       float bl = -INFINITY;
       int32_t bc = INT32_MAX;
+      float* sp = KS > 1 && has ? p.split_part + ((size_t)split * p.B + b) * p.C : nullptr;
 #pragma unroll 1
       for (int ch = 0; ch < kTileN / 32; ++ch) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(m * kTileN + ch * 32), v);
         const int c0 = n0 + ch * 32;
         uint32_t bits = 0;
+        int pos = lo;  // candidate index of the next set bit
         while (lo < nc && cand[lo] < c0 + 32) {
           bits |= 1u << (cand[lo] - c0);
           ++lo;
@@ -272,14 +277,16 @@ __global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmPara
         for (int j = 0; j < 32; ++j) {
           if ((bits >> j) & 1u) {
             const float x = __uint_as_float(v[j]);
-            if (gbetter(x, c0 + j, bl, bc)) {
+            if (sp) {
+              sp[pos++] = x;  // this split's partial sum of candidate pos
+            } else if (gbetter(x, c0 + j, bl, bc)) {
               bl = x;
               bc = c0 + j;
             }
           }
         }
       }
-      if (has) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
+      if (has && KS == 1) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
     }
     tc_fence_before();
     __syncthreads();  // TMEM is read before the next tile's MMAs overwrite it
@@ -314,7 +321,9 @@ cudaError_t prepare_gemm() {
 int gemm_tile_cols() { return kTileN; }
 
 cudaError_t launch_union_gemm(const GemmParams& p, int num_ctas, cudaStream_t s) {
-  if (p.H % kTileK != 0 || p.B < 1 || p.B > 256) return cudaErrorInvalidValue;
+  if (p.H % kTileK != 0 || p.B < 1 || p.B > 256 || p.ksplit < 1 || (p.H / kTileK) % p.ksplit != 0 ||
+      (p.ksplit > 1 && !p.split_part))
+    return cudaErrorInvalidValue;
   const int mt = p.B > 128 ? 2 : 1;
   if (mt == 1) union_gemm_kernel<1><<<num_ctas, kThreadsG, gemm_smem_bytes(1), s>>>(p);
   else union_gemm_kernel<2><<<num_ctas, kThreadsG, gemm_smem_bytes(2), s>>>(p);

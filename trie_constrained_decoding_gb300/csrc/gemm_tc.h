@@ -24,8 +24,10 @@ struct GemmParams {
   const int32_t* cand_col;   // [B, C] ascending columns of each sequence's legal candidates
   const int32_t* ncand;      // [B]
   int32_t C;
-  GemmPartial* part;         // [B, max_tiles]
+  GemmPartial* part;         // [B, max_tiles] (ksplit == 1)
   int32_t max_tiles;
+  int32_t ksplit;            // K splits per column tile; H / 64 must be a multiple
+  float* split_part;         // [ksplit, B, C] candidate partial sums (ksplit > 1)
   int32_t* err;              // set to 1 when a wait timed out
 };
 

@@ -68,6 +68,8 @@ struct HeadScratch {
   int32_t* n_union;         // [1]
   GemmPartial* part;        // [B, max_tiles]
   int32_t max_tiles;
+  int32_t ksplit;           // K splits of the union GEMM (fixed by the hidden size)
+  float* split_part;        // [ksplit, B, C] per-split candidate sums of the union GEMM
   int32_t union_mode;       // 1: columns are the union; 0: every vocabulary row
   int32_t* gemm_err;        // [1] GEMM wait timeout
 };

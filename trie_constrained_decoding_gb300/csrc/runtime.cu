@@ -162,7 +162,10 @@ int tiles_for(const tc_ctx* c, const DevGrammar* g, int head, int B) {
 
 bool is_gemm_head(int head) { return head == TC_HEAD_UNION_GEMM || head == TC_HEAD_DENSE_GEMM; }
 
-int gemm_ctas(const tc_ctx* c) { return std::min(c->num_sms, c->hs.max_tiles); }
+int gemm_ctas(const tc_ctx* c, int head) {
+  const int tasks = c->hs.max_tiles * (head == TC_HEAD_UNION_GEMM ? c->hs.ksplit : 1);
+  return std::min(c->num_sms, tasks);
+}
 
 // Scratch of the GEMM heads, sized for max_batch sequences and the whole vocabulary.
 tc_status ensure_gemm_scratch(tc_ctx* c) {
@@ -183,6 +186,11 @@ tc_status ensure_gemm_scratch(tc_ctx* c) {
   if (e == cudaSuccess) e = cudaMalloc(&h.n_union, 4);
   if (e == cudaSuccess) e = cudaMemset(h.n_union, 0, 4);
   if (e == cudaSuccess) e = cudaMalloc(&h.part, (size_t)c->max_batch * h.max_tiles * sizeof(GemmPartial));
+  // The union GEMM splits K into tasks of 4 k-steps (256 elements) when the
+  // hidden size allows; the split count depends only on the hidden size, so a
+  // sequence's sums never depend on its batch-mates.
+  h.ksplit = (c->H / 64) % 4 == 0 ? c->H / 256 : 1;
+  if (e == cudaSuccess && h.ksplit > 1) e = cudaMalloc(&h.split_part, (size_t)h.ksplit * BC * 4);
   if (e == cudaSuccess) e = cudaMalloc(&h.gemm_err, 4);
   if (e == cudaSuccess) e = cudaMemset(h.gemm_err, 0, 4);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM-head scratch");
@@ -203,6 +211,7 @@ void free_gemm_scratch(tc_ctx* c) {
   cudaFree(h.umap);
   cudaFree(h.n_union);
   cudaFree(h.part);
+  cudaFree(h.split_part);
   cudaFree(h.gemm_err);
   c->hs_ready = false;
 }
@@ -226,7 +235,7 @@ cudaError_t launch_any_step(tc_ctx* c, DevGrammar* g, const StepParams& p, int h
   if (is_gemm_head(head)) {
     StepParams q = p;
     q.hs = c->hs;
-    return launch_gemm_step(q, cst, head, gemm_ctas(c), s);
+    return launch_gemm_step(q, cst, head, gemm_ctas(c, head), s);
   }
   return launch_step(p, cst, head, tiles_for(c, g, head, p.B), s, pdl);
 }

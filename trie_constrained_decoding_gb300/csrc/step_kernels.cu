@@ -748,7 +748,20 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
     const int n_cols = hs.union_mode ? *hs.n_union : p.V;
     const int n_tiles = (n_cols + gemm_tile_cols_dev - 1) / gemm_tile_cols_dev;
     int32_t bc = INT_MAX;
-    if (!err && n > 0) {
+    if (!err && n > 0 && hs.union_mode && hs.ksplit > 1) {
+      // Split-K: each candidate's logit is the sum of its per-split partial
+      // sums, added in split order (a fixed order, independent of the batch).
+      for (int i = tid; i < n; i += kThreads) {
+        float v = 0.f;
+        for (int sidx = 0; sidx < hs.ksplit; ++sidx)
+          v += hs.split_part[((size_t)sidx * p.B + b) * p.cand_cap + i];
+        const int32_t col = hs.cand_col[(size_t)b * p.cand_cap + i];
+        if (better(v, col, wl, bc)) {
+          wl = v;
+          bc = col;
+        }
+      }
+    } else if (!err && n > 0) {
       const GemmPartial* part = hs.part + (size_t)b * hs.max_tiles;
       for (int t = tid; t < n_tiles && t < hs.max_tiles; t += kThreads) {
         const GemmPartial q = part[t];
@@ -757,30 +770,30 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
           bc = q.col;
         }
       }
-      // warp-wide fold: (logit, column) is a total order, so every lane ends with the same best
+    }
+    // warp-wide fold: (logit, column) is a total order, so every lane ends with the same best
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ol = __shfl_xor_sync(kFull, wl, o);
-        const int32_t oc = __shfl_xor_sync(kFull, bc, o);
-        if (better(ol, oc, wl, bc)) {
-          wl = ol;
-          bc = oc;
-        }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ol = __shfl_xor_sync(kFull, wl, o);
+      const int32_t oc = __shfl_xor_sync(kFull, bc, o);
+      if (better(ol, oc, wl, bc)) {
+        wl = ol;
+        bc = oc;
       }
-      if (bc != INT_MAX) {
-        // columns ascend with tokens, so the column order breaks ties like the token order
-        const int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
-        int lo = 0, hi = n;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (cc[mid] < bc) lo = mid + 1; else hi = mid;
-        }
-        if (lo < n && cc[lo] == bc) {
-          wt = hs.cand_tok[(size_t)b * p.cand_cap + lo];
-          we = hs.cand_edge[(size_t)b * p.cand_cap + lo];
-        } else {
-          wl = -INFINITY;  // cannot happen: the column came from this sequence's list
-        }
+    }
+    if (bc != INT_MAX) {
+      // columns ascend with tokens, so the column order breaks ties like the token order
+      const int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
+      int lo = 0, hi = n;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cc[mid] < bc) lo = mid + 1; else hi = mid;
+      }
+      if (lo < n && cc[lo] == bc) {
+        wt = hs.cand_tok[(size_t)b * p.cand_cap + lo];
+        we = hs.cand_edge[(size_t)b * p.cand_cap + lo];
+      } else {
+        wl = -INFINITY;  // cannot happen: the column came from this sequence's list
       }
     }
     if (tid == 0) {
@@ -904,6 +917,8 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
   gp.C = p.cand_cap;
   gp.part = q.hs.part;
   gp.max_tiles = q.hs.max_tiles;
+  gp.ksplit = q.hs.union_mode ? q.hs.ksplit : 1;
+  gp.split_part = q.hs.split_part;
   gp.err = q.hs.gemm_err;
   if ((e = launch_union_gemm(gp, gemm_ctas, s)) != cudaSuccess) return e;
   if (const_resident) gemm_finish_kernel<true><<<dim3(1, p.B), kThreads, 0, s>>>(q);

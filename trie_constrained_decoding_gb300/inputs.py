@@ -314,7 +314,7 @@ def tensor_batch() -> Workload:
     """The 1000-tool prefix catalog, vocab 151936, hidden 4096, B=256, k=3 (union GEMM path)."""
     w = batched()
     w.name = "tensor_batch"
-    w.k, w.batch, w.n_queries = 3, 256, 256
+    w.k, w.batch, w.n_queries = 3, 256, 4096
     return w
 
 
