@@ -125,6 +125,9 @@ struct GemmSmemHeader {
   uint32_t tmem_base;
   int32_t abort;
   int32_t rows[kTileN];     // embedding row of each column of the current tile
+  int64_t xoff[256];        // hidden-row offset of each sequence (-1: no row)
+  uint32_t cbits[256][kTileN / 32];  // per sequence: its candidate columns in the current tile
+  int32_t cpos[256];        // per sequence: index of its first candidate in the current tile
 };
 
 template <int MT>
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmPara
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  for (int r = tid; r < MT * 128; r += kThreadsG) hdr->xoff[r] = r < p.B ? p.xrow[r] : -1;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmPara
       const int k0 = (kbase + kt) * kTileK;
       for (int i = tid; i < MT * 128 * 8; i += kThreadsG) {
         const int r = i >> 3, c = i & 7;
-        const int64_t off = r < p.B ? p.xrow[r] : -1;
+        const int64_t off = hdr->xoff[r];
         const uint16_t* src = off >= 0 ? p.hidden + off + k0 + c * 8 : p.hidden;
         cp_async16(a_base + r * kRowBytes + ((c ^ (r & 7)) << 4), src, off >= 0 ? 16u : 0u);
       }
@@ -194,6 +198,29 @@ __global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmPara
     for (int s = 0; s < kStages - 1; ++s) {
       if (s < KT) load_stage(s, (int)((g + s) % kStages));
       cp_async_commit();
+    }
+    // While those copies fly: which columns of this tile are each sequence's
+    // candidates (thread t serves sequences t and 128 + t in the epilogue).
+    for (int m = 0; m < MT; ++m) {
+      const int b = m * 128 + tid;
+#pragma unroll
+      for (int q = 0; q < kTileN / 32; ++q) hdr->cbits[b][q] = 0u;
+      int lo = 0;
+      if (hdr->xoff[b] >= 0) {
+        const int nc = p.ncand[b];
+        const int32_t* cand = p.cand_col + (size_t)b * p.C;
+        int hi = nc;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (cand[mid] < n0) lo = mid + 1; else hi = mid;
+        }
+        for (int i = lo; i < nc; ++i) {
+          const int c = cand[i] - n0;
+          if (c >= kTileN) break;
+          hdr->cbits[b][c >> 5] |= 1u << (c & 31);
+        }
+      }
+      hdr->cpos[b] = lo;
     }
     for (int kt = 0; kt < KT; ++kt) {
       const long long gk = g + kt;
@@ -248,31 +275,17 @@ __global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmPara
     // Epilogue: masked argmax of each sequence over its candidates in this tile.
     for (int m = 0; m < MT; ++m) {
       const int b = m * 128 + warp * 32 + lane;
-      const bool has = b < p.B && p.xrow[b] >= 0;
-      int lo = 0, nc = 0;
-      const int32_t* cand = p.cand_col + (size_t)(has ? b : 0) * p.C;
-      if (has) {
-        nc = p.ncand[b];
-        int hi = nc;  // first candidate column >= n0
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (cand[mid] < n0) lo = mid + 1; else hi = mid;
-        }
-      }
+      const bool has = hdr->xoff[b] >= 0;
       float bl = -INFINITY;
       int32_t bc = INT32_MAX;
       float* sp = KS > 1 && has ? p.split_part + ((size_t)split * p.B + b) * p.C : nullptr;
+      int pos = hdr->cpos[b];  // candidate index of the next set bit
 #pragma unroll 1
       for (int ch = 0; ch < kTileN / 32; ++ch) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(m * kTileN + ch * 32), v);
         const int c0 = n0 + ch * 32;
-        uint32_t bits = 0;
-        int pos = lo;  // candidate index of the next set bit
-        while (lo < nc && cand[lo] < c0 + 32) {
-          bits |= 1u << (cand[lo] - c0);
-          ++lo;
-        }
+        const uint32_t bits = hdr->cbits[b][ch];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if ((bits >> j) & 1u) {

@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kThreads) cand_filter_kernel(const StepParams 
 }
 
 // One CTA of 1024 threads: union bitmap -> ascending row list, token -> index
-// map, bitmap cleared for the next step; then every candidate's column.
+// map, bitmap cleared for the next step.
 constexpr int kCompactThreads = 1024;
 __global__ void __launch_bounds__(kCompactThreads) union_compact_kernel(const StepParams p) {
   __shared__ int32_t s_warp[kCompactThreads / 32];
@@ -721,13 +721,16 @@ __global__ void __launch_bounds__(kCompactThreads) union_compact_kernel(const St
     }
   }
   if (tid == 0) *hs.n_union = s_warp[kCompactThreads / 32 - 1];
-  __syncthreads();
-  for (int b = 0; b < p.B; ++b) {
-    const int n = hs.ncand[b];
-    const int32_t* ct = hs.cand_tok + (size_t)b * p.cand_cap;
-    int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
-    for (int i = tid; i < n; i += kCompactThreads) cc[i] = hs.umap[ct[i]];
-  }
+}
+
+// Grid (1, B): the GEMM column of each of sequence b's candidates.
+__global__ void __launch_bounds__(kThreads) cand_column_kernel(const StepParams p) {
+  const HeadScratch& hs = p.hs;
+  const int b = blockIdx.y;
+  const int n = hs.ncand[b];
+  const int32_t* ct = hs.cand_tok + (size_t)b * p.cand_cap;
+  int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
+  for (int i = threadIdx.x; i < n; i += kThreads) cc[i] = hs.umap[ct[i]];
 }
 
 // Grid (1, B): fold sequence b's column-tile partials, map the winning column
@@ -747,18 +750,20 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
     const int err = hs.errf[b];
     const int n_cols = hs.union_mode ? *hs.n_union : p.V;
     const int n_tiles = (n_cols + gemm_tile_cols_dev - 1) / gemm_tile_cols_dev;
-    int32_t bc = INT_MAX;
-    if (!err && n > 0 && hs.union_mode && hs.ksplit > 1) {
+    int32_t bc = INT_MAX;  // winning column (tile partials)
+    int32_t bi = INT_MAX;  // winning candidate index (split sums)
+    const bool split = hs.union_mode && hs.ksplit > 1;
+    if (!err && n > 0 && split) {
       // Split-K: each candidate's logit is the sum of its per-split partial
       // sums, added in split order (a fixed order, independent of the batch).
+      // Candidates ascend by token, so the candidate index orders ties like the token.
       for (int i = tid; i < n; i += kThreads) {
         float v = 0.f;
         for (int sidx = 0; sidx < hs.ksplit; ++sidx)
           v += hs.split_part[((size_t)sidx * p.B + b) * p.cand_cap + i];
-        const int32_t col = hs.cand_col[(size_t)b * p.cand_cap + i];
-        if (better(v, col, wl, bc)) {
+        if (better(v, i, wl, bi)) {
           wl = v;
-          bc = col;
+          bi = i;
         }
       }
     } else if (!err && n > 0) {
@@ -771,17 +776,23 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
         }
       }
     }
-    // warp-wide fold: (logit, column) is a total order, so every lane ends with the same best
+    // warp-wide fold: (logit, column or index) is a total order, so every lane ends with the same best
+    int32_t key = split ? bi : bc;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ol = __shfl_xor_sync(kFull, wl, o);
-      const int32_t oc = __shfl_xor_sync(kFull, bc, o);
-      if (better(ol, oc, wl, bc)) {
+      const int32_t ok = __shfl_xor_sync(kFull, key, o);
+      if (better(ol, ok, wl, key)) {
         wl = ol;
-        bc = oc;
+        key = ok;
       }
     }
-    if (bc != INT_MAX) {
+    if (split) {
+      if (key != INT_MAX) {
+        wt = hs.cand_tok[(size_t)b * p.cand_cap + key];
+        we = hs.cand_edge[(size_t)b * p.cand_cap + key];
+      }
+    } else if ((bc = key) != INT_MAX) {
       // columns ascend with tokens, so the column order breaks ties like the token order
       const int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
       int lo = 0, hi = n;
@@ -901,6 +912,8 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
   if (e != cudaSuccess) return e;
   if (q.hs.union_mode) {
     union_compact_kernel<<<1, kCompactThreads, 0, s>>>(no_ctrl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cand_column_kernel<<<dim3(1, p.B), kThreads, 0, s>>>(no_ctrl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   GemmParams gp{};
