@@ -125,6 +125,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def recorded_traffic(source: str, profile: str):
+    """DRAM bytes per launch recorded by the last ncu capture of a kernel, or
+    None when the kernel's source file has changed since that capture."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+        src = open(os.path.join(ROOT, "trie_constrained_decoding_gb300", "csrc", source), "rb").read()
+    except OSError:
+        return None
+    want = hashlib.sha256(src).hexdigest()
+    sha = traffic = None
+    for line in text.splitlines():
+        if line.startswith(f"source-sha256 {source}:"):
+            sha = line.split(":", 1)[1].strip()
+        if line.startswith("dram-bytes-per-launch:"):
+            traffic = float(line.split(":", 1)[1])
+    return traffic if sha == want else None
+
+
 def read_peaks():
     try:
         with open(PEAKS_PATH) as f:
@@ -311,6 +330,11 @@ def run_ours(args):
         roof["frac"] = roof["achieved"] / peak
         roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if peak_kind == "measured" \
             else "fallback 6.8 TB/s"
+        if head == tcd.HEAD_SPARSE and args.workload == "large_head":
+            roof["traffic"] = recorded_traffic("step_kernels.cu", "sparse_step_kernel_large_head.md")
+            roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, cold caches, "
+                                      "profiles/sparse_step_kernel_large_head.md" if roof["traffic"] is not None
+                                      else "kernel source changed since the last ncu capture")
     cpu = None
     if world == 1 and not args.no_extras:
         cpu = oracle_baseline(w, args.cpu_seconds)
