@@ -12,8 +12,9 @@ constexpr int kMaxTiles = 1024;        // upper bound of CTAs per sequence (part
 constexpr int kMaxHidden = 16384;
 constexpr int kMaxCandCap = 4096;
 // Dynamic shared memory a step kernel may request: x staged for the generic
-// hidden size plus two int32 candidate lists of up to kMaxCandCap entries.
-constexpr int kMaxDynamicSmem = kMaxHidden * 2 + 2 * kMaxCandCap * 4;
+// hidden size, two int32 candidate lists of up to kMaxCandCap entries, and
+// (dense head) 128 KiB of row stages.
+constexpr int kMaxDynamicSmem = kMaxHidden * 2 + 2 * kMaxCandCap * 4 + 128 + 128 * 1024;
 
 // Per-sequence decode state (device memory, one record per sequence).
 struct SeqState {

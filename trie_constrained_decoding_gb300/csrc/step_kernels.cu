@@ -533,10 +533,58 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
 }
 
 // Dense head: every vocabulary row, then the legal mask, then the argmax.
+//
+// Each CTA owns a contiguous block of rows and streams it through shared
+// memory in stages of up to 8 rows with bulk asynchronous copies (one copy per
+// stage, completion counted on the stage's mbarrier), so DRAM sees long
+// sequential reads and the bytes in flight do not depend on registers.  Warp w
+// computes row w of a stage with the same lane map and reduction tree as the
+// sparse head's row_dot, so both heads produce bit-identical logits.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__host__ __device__ __forceinline__ void dense_rows_per_stage(int H, int& R, int& S) {
+  R = (64 * 1024) / (2 * H);
+  R = R > kWarps ? kWarps : (R < 1 ? 1 : R);
+  S = (128 * 1024) / (R * 2 * H);
+  S = S > 4 ? 4 : (S < 2 ? 2 : S);
+}
+
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < (1 << 20); ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+template <int NCH>
+__device__ __forceinline__ float row_dot_smem(const uint4* row, const XFrag<NCH>& xf, const uint4* xs, int nch,
+                                              int lane) {
+  float acc = 0.f;
+  if constexpr (NCH > 0) {
+    uint4 e[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) e[i] = row[i * 32 + lane];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xf.v[i], acc);
+  } else {
+    for (int c = lane; c < nch; c += 32) acc = dot8(row[c], xs[c], acc);
+  }
+  return warp_sum(acc);
+}
+
 template <bool kConst, int NCH>
 __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ StepShared sh;
+  __shared__ __align__(8) uint64_t full[4];
   pdl_wait();  // the next step may launch only near the end: its waiting CTAs would take SM slots
   const int b = blockIdx.y, g = blockIdx.x, G = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -547,6 +595,8 @@ __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p
   uint4* xs = reinterpret_cast<uint4*>(smem_raw);
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
   int32_t* s_edge = s_tok + p.cand_cap;
+  const size_t lists_end = (size_t)(NCH == 0 ? nch * 16 : 0) + 2 * (size_t)p.cand_cap * sizeof(int32_t);
+  unsigned char* stages = smem_raw + ((lists_end + 127) & ~(size_t)127);
 
   float wl = -INFINITY;
   int32_t wt = INT_MAX, we = -1;
@@ -570,15 +620,58 @@ __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p
         }
         if (lo < n && s_tok[lo] == r && better(v, r, wl, wt)) { wl = v; wt = r; we = s_edge[lo]; }
       };
-      const int stride = G * kWarps;
-      int32_t r = g * kWarps + warp;
-      for (; r + stride < p.V; r += 2 * stride) {
-        float va, vb;
-        row_dot2<NCH>(p.emb + (size_t)r * p.H, p.emb + (size_t)(r + stride) * p.H, xf, xs, nch, lane, va, vb);
-        consider(r, va);
-        consider(r + stride, vb);
+      int R, S;
+      dense_rows_per_stage(p.H, R, S);
+      const size_t row_bytes = (size_t)p.H * 2;
+      const int rpc = (p.V + G - 1) / G;
+      const int r_begin = g * rpc;
+      const int r_end = min(p.V, r_begin + rpc);
+      const int n_chunks = r_end > r_begin ? (r_end - r_begin + R - 1) / R : 0;
+      auto issue = [&](int c) {
+        const int st = c % S;
+        const int r0 = r_begin + c * R;
+        const int nr = min(R, r_end - r0);
+        const uint32_t bytes = (uint32_t)(nr * row_bytes);
+        const uint32_t bar = smem_addr(&full[st]);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_addr(stages + (size_t)st * R * row_bytes)),
+                     "l"(p.emb + (size_t)r0 * p.H), "r"(bytes), "r"(bar)
+                     : "memory");
+      };
+      if (tid == 0) {
+        for (int i = 0; i < S; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[i])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int c = 0; c < S && c < n_chunks; ++c) issue(c);
       }
-      if (r < p.V) consider(r, row_dot<NCH>(p.emb + (size_t)r * p.H, xf, xs, nch, lane));
+      __syncthreads();
+      int failed = 0;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int st = c % S;
+        const bool ok = stage_wait(smem_addr(&full[st]), (uint32_t)((c / S) & 1));
+        if (__syncthreads_or(!ok)) {
+          failed = 1;
+          break;
+        }
+        const int r0 = r_begin + c * R;
+        if (warp < min(R, r_end - r0)) {
+          const uint4* row = reinterpret_cast<const uint4*>(stages + (size_t)st * R * row_bytes + (size_t)warp * row_bytes);
+          consider(r0 + warp, row_dot_smem<NCH>(row, xf, xs, nch, lane));
+        }
+        __syncthreads();  // every warp is done with this stage before it is refilled
+        if (tid == 0 && c + S < n_chunks) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue(c + S);
+        }
+      }
+      if (failed) {
+        // A copy never completed: wait (bounded) for the ones still in flight, then report.
+        if (tid == 0) {
+          for (int c = 0; c < n_chunks; ++c) stage_wait(smem_addr(&full[c % S]), (uint32_t)((c / S) & 1));
+          sh.err = 1;
+        }
+        __syncthreads();
+      }
     }
   }
   pdl_trigger();
@@ -828,7 +921,7 @@ int sparse_tiles(int max_fanout, int B, int num_sms) {
 }
 
 int dense_tiles(int B, int num_sms) {
-  int g = (2 * num_sms) / (B > 0 ? B : 1);
+  int g = num_sms / (B > 0 ? B : 1);  // one CTA per SM: each streams 128 KB of stages
   if (g < 1) g = 1;
   if (g > kMaxTiles) g = kMaxTiles;
   return g;
@@ -841,10 +934,16 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
   const int nch = p.H >> 3;
   const size_t xbytes = NCH == 0 ? (size_t)nch * 16 : 0;
   const int cap = head == kHeadSparse ? (p.cand_cap + tiles - 1) / tiles : p.cand_cap;
+  size_t smem = xbytes + 2 * (size_t)cap * sizeof(int32_t);
+  if (head != kHeadSparse) {
+    int R, S;
+    dense_rows_per_stage(p.H, R, S);
+    smem = ((smem + 127) & ~(size_t)127) + (size_t)S * R * 2 * p.H;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(tiles, p.B);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = xbytes + 2 * (size_t)cap * sizeof(int32_t);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
