@@ -159,6 +159,20 @@ def query_ids(n_queries: int, rank: int, world: int, count: int):
     return [(rank + world * i) % n_queries for i in range(count)]
 
 
+def aggregate_ranks(dist, dev_ms: float, steps: int, tokens: int, device: str):
+    """Whole-job figures: the slowest rank's time and the steps/tokens of all ranks.
+
+    Only timing scalars cross ranks; the decode itself has no collective."""
+    import torch
+    if dist is None:
+        return dev_ms, float(steps), float(tokens)
+    t_max = torch.tensor([dev_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    sums = torch.tensor([float(steps), float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(sums, op=dist.ReduceOp.SUM)
+    return float(t_max[0]), float(sums[0]), float(sums[1])
+
+
 def host_hidden(w, qids):
     """bf16 bits [len(qids), steps, batch, hidden] of the queries' hidden states."""
     B = w.batch
@@ -303,15 +317,7 @@ def run_ours(args):
     tokens = st["seq_steps"]
     gpu_launches = st["step_launches"] + st["reset_launches"]
 
-    tot = torch.tensor([dev_ms, float(decode_steps), float(tokens)], dtype=torch.float64, device=f"cuda:{dev}")
-    if dist:
-        t_max = tot[0:1].clone()
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-        sums = tot[1:3].clone()
-        dist.all_reduce(sums, op=dist.ReduceOp.SUM)
-        dev_ms_max, all_steps, all_tokens = float(t_max[0]), float(sums[0]), float(sums[1])
-    else:
-        dev_ms_max, all_steps, all_tokens = dev_ms, float(decode_steps), float(tokens)
+    dev_ms_max, all_steps, all_tokens = aggregate_ranks(dist, dev_ms, decode_steps, tokens, f"cuda:{dev}")
     value = all_steps / (dev_ms_max / 1000.0)
 
     extras = {}
