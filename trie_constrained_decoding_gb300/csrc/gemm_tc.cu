@@ -6,20 +6,28 @@
 //
 //   D[b, n] = sum_h X[b, h] * E[rows[n], h]        b < B (sequences), n < n_cols
 //
-// A = X (one 128-row tile per 128 sequences, up to two), B = the embedding rows
-// listed for the tile's 256 columns (rows[n] = n for the dense head), both bf16
-// K-major in shared memory in the 128-byte swizzled layout, staged by cp.async
-// (the rows are gathered, so a rectangular TMA box does not describe them).
-// One thread issues tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) into TMEM:
-// 128 lanes x 256 columns per M tile.  The epilogue reads TMEM with tcgen05.ld;
-// thread t of warp w owns sequence 128*m + 32*w + t and keeps, over the columns
-// of its own legal candidates only, the largest logit (lowest column on ties;
-// columns ascend with token ids) - one (logit, column) partial per sequence and
-// column tile.  Persistent CTAs loop over column tiles.
-//
-// Every wait on an mbarrier is bounded; on a timeout the kernel records an
-// error, drains its own copies, frees its TMEM and returns.
+// Warp-specialised persistent kernel, 192 threads per CTA:
+//  - warp 0 (producer) fills a ring of shared-memory stages with TMA: the
+//    activation tile (128 sequences x 64 K-elements per M tile) with a tiled
+//    2-D load, the embedding tile (128 columns x 64) either with one tiled load
+//    (dense head: contiguous rows) or with one four-row gather per lane (union
+//    head: listed rows), all 128-byte swizzled, completion counted on the
+//    stage's "full" mbarrier;
+//  - warp 1, one thread, issues tcgen05.mma kind::f16 (bf16 in, fp32 in TMEM,
+//    M = 128 per tile, N = 128, K = 16 per instruction) and commits each stage
+//    back to its "empty" barrier and each finished task to an accumulator-full
+//    barrier; TMEM holds two accumulators so one task's epilogue overlaps the
+//    next task's MMAs;
+//  - warps 2-5 (epilogue) read the accumulator with tcgen05.ld: the thread on
+//    TMEM lane t of M tile m owns sequence 128 m + t and keeps, over the
+//    columns of its own legal candidates only, the largest logit (lowest
+//    column on ties; columns ascend with token ids), or, when K is split, its
+//    candidates' partial sums.
+// A task is one 128-column tile and one K split.  Every wait is bounded; on a
+// timeout the kernel records an error, stops issuing and frees its TMEM.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "gemm_tc.h"
@@ -27,14 +35,35 @@
 namespace tcd {
 namespace {
 
-constexpr int kThreadsG = 128;
-constexpr int kTileN = 256;
-constexpr int kTileK = 64;         // bf16 elements = one 128-byte swizzle row
-constexpr int kStages = 3;
+constexpr int kThreadsG = 192;
+constexpr int kTileN = 128;
+constexpr int kTileK = 64;  // bf16 elements = one 128-byte swizzle row
 constexpr uint32_t kRowBytes = 128;
-constexpr uint32_t kATileBytes = 128 * kRowBytes;    // 16 KiB per 128-row M tile
-constexpr uint32_t kBTileBytes = kTileN * kRowBytes;  // 32 KiB
-constexpr long long kWaitLimit = 1ll << 20;          // try_wait polls before giving up
+constexpr uint32_t kATileBytes = 128 * kRowBytes;     // 16 KiB per 128-row M tile
+constexpr uint32_t kBTileBytes = kTileN * kRowBytes;  // 16 KiB
+constexpr long long kWaitLimit = 1ll << 22;           // try_wait polls before giving up
+
+template <int MT>
+struct Cfg {
+  static constexpr int kStages = MT == 2 ? 4 : 6;
+  static constexpr uint32_t kStageBytes = MT * kATileBytes + kBTileBytes;
+  static constexpr int kAccCols = MT * kTileN;  // TMEM columns of one accumulator
+  static constexpr int kTmemCols = 2 * kAccCols;
+};
+
+struct GemmHdr {
+  uint64_t full[6];
+  uint64_t empty[6];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  int32_t abort;
+  int32_t row0;
+  int32_t pad;
+  int32_t active[256];               // sequence takes this step
+  uint32_t cbits[256][kTileN / 32];  // per sequence: its candidate columns in the current tile
+  int32_t cpos[256];                 // per sequence: index of its first candidate in the current tile
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -44,33 +73,43 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
   return false;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
+                                            int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -80,10 +119,10 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;                  // leading byte offset (unused for swizzled K-major): 16 B
-  d |= (uint64_t)(1024u >> 4) << 32;       // stride byte offset: 1024 B
-  d |= (uint64_t)1 << 46;                  // version
-  d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major): 16 B
+  d |= (uint64_t)(1024u >> 4) << 32;  // stride byte offset: 1024 B
+  d |= (uint64_t)1 << 46;             // version
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
   return d;
 }
 
@@ -120,207 +159,238 @@ __device__ __forceinline__ bool gbetter(float l, int32_t c, float bl, int32_t bc
   return l > bl || (l == bl && c < bc);
 }
 
-struct GemmSmemHeader {
-  uint64_t empty[kStages];  // one arrival per tcgen05.commit of a k-step
-  uint32_t tmem_base;
-  int32_t abort;
-  int32_t rows[kTileN];     // embedding row of each column of the current tile
-  int64_t xoff[256];        // hidden-row offset of each sequence (-1: no row)
-  uint32_t cbits[256][kTileN / 32];  // per sequence: its candidate columns in the current tile
-  int32_t cpos[256];        // per sequence: index of its first candidate in the current tile
-};
-
 template <int MT>
-__global__ void __launch_bounds__(kThreadsG, 1) union_gemm_kernel(const GemmParams p) {
+__global__ void __launch_bounds__(kThreadsG, 1)
+    union_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmG) {
+  using C = Cfg<MT>;
+  constexpr int S = C::kStages;
   extern __shared__ __align__(1024) unsigned char gsm[];
-  // Operand tiles first (1024-byte aligned), header after them.
-  const uint32_t stage_bytes = MT * kATileBytes + kBTileBytes;
   unsigned char* tiles = gsm + ((1024 - (smem_u32(gsm) & 1023)) & 1023);
-  GemmSmemHeader* hdr = reinterpret_cast<GemmSmemHeader*>(tiles + kStages * stage_bytes);
+  GemmHdr* hdr = reinterpret_cast<GemmHdr*>(tiles + S * C::kStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tiles_s = smem_u32(tiles);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&hdr->empty[s]), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&hdr->full[s]), 1);
+      mbar_init(smem_u32(&hdr->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&hdr->tfull[a]), 1);
+      mbar_init(smem_u32(&hdr->tempty[a]), 128);
+    }
     hdr->abort = 0;
+    hdr->row0 = p.row0_ptr ? *p.row0_ptr : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {
+  for (int r = tid; r < MT * 128; r += kThreadsG) hdr->active[r] = (r < p.B && p.xrow[r] >= 0) ? 1 : 0;
+  if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&hdr->tmem_base)),
-                 "r"(MT * kTileN)
+                 "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  for (int r = tid; r < MT * 128; r += kThreadsG) hdr->xoff[r] = r < p.B ? p.xrow[r] : -1;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
+  const int row0 = hdr->row0;
 
   const int n_cols = p.n_cols_ptr ? *p.n_cols_ptr : p.n_cols_fixed;
   const int n_tiles = (n_cols + kTileN - 1) / kTileN;
-  const int KS = p.ksplit;              // K splits per column tile (divides H / 64)
-  const int KT = p.H / kTileK / KS;     // k-steps per task
-  constexpr uint32_t idesc = idesc_bf16(128, kTileN);
-  long long g = 0;  // global k-step counter of this CTA (stage = g % kStages)
-  bool failed = false;
+  const int KS = p.ksplit;           // K splits per column tile (divides H / 64)
+  const int KT = p.H / kTileK / KS;  // k-steps per task
+  const int n_tasks = n_tiles * KS;
+  const bool gather = p.row_list != nullptr;
 
-  for (int task = blockIdx.x; task < n_tiles * KS && !failed; task += gridDim.x) {
-    const int tile = task / KS, split = task % KS;
-    const int n0 = tile * kTileN;
-    const int kbase = split * KT;
-    for (int r = tid; r < kTileN; r += kThreadsG) {
-      const int col = n0 + r;
-      hdr->rows[r] = col < n_cols ? (p.row_list ? p.row_list[col] : col) : -1;
-    }
-    __syncthreads();
-
-    auto load_stage = [&](int kt, int stage) {
-      const uint32_t a_base = tiles_s + stage * stage_bytes;
-      const uint32_t b_base = a_base + MT * kATileBytes;
-      const int k0 = (kbase + kt) * kTileK;
-      for (int i = tid; i < MT * 128 * 8; i += kThreadsG) {
-        const int r = i >> 3, c = i & 7;
-        const int64_t off = hdr->xoff[r];
-        const uint16_t* src = off >= 0 ? p.hidden + off + k0 + c * 8 : p.hidden;
-        cp_async16(a_base + r * kRowBytes + ((c ^ (r & 7)) << 4), src, off >= 0 ? 16u : 0u);
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    long long it = 0;
+    for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+      const int tile = task / KS, split = task % KS;
+      const int n0 = tile * kTileN;
+      int rr0 = 0, rr1 = 0, rr2 = 0, rr3 = 0;  // this lane's four gathered rows
+      if (gather) {
+        const int c = n0 + 4 * lane;
+        rr0 = c + 0 < n_cols ? p.row_list[c + 0] : 0;
+        rr1 = c + 1 < n_cols ? p.row_list[c + 1] : 0;
+        rr2 = c + 2 < n_cols ? p.row_list[c + 2] : 0;
+        rr3 = c + 3 < n_cols ? p.row_list[c + 3] : 0;
       }
-      for (int i = tid; i < kTileN * 8; i += kThreadsG) {
-        const int r = i >> 3, c = i & 7;
-        const int row = hdr->rows[r];
-        const uint16_t* src = row >= 0 ? p.emb + (size_t)row * p.H + k0 + c * 8 : p.emb;
-        cp_async16(b_base + r * kRowBytes + ((c ^ (r & 7)) << 4), src, row >= 0 ? 16u : 0u);
-      }
-    };
-
-    // Prologue: the first kStages-1 k-steps of this tile.  Every stage is free:
-    // the previous tile ended by waiting for its last MMA.
-    for (int s = 0; s < kStages - 1; ++s) {
-      if (s < KT) load_stage(s, (int)((g + s) % kStages));
-      cp_async_commit();
-    }
-    // While those copies fly: which columns of this tile are each sequence's
-    // candidates (thread t serves sequences t and 128 + t in the epilogue).
-    for (int m = 0; m < MT; ++m) {
-      const int b = m * 128 + tid;
-#pragma unroll
-      for (int q = 0; q < kTileN / 32; ++q) hdr->cbits[b][q] = 0u;
-      int lo = 0;
-      if (hdr->xoff[b] >= 0) {
-        const int nc = p.ncand[b];
-        const int32_t* cand = p.cand_col + (size_t)b * p.C;
-        int hi = nc;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (cand[mid] < n0) lo = mid + 1; else hi = mid;
+      bool stop = false;
+      for (int kt = 0; kt < KT; ++kt, ++it) {
+        const int stage = (int)(it % S);
+        const uint32_t ph = (uint32_t)((it / S) & 1);
+        if (!mbar_wait(smem_u32(&hdr->empty[stage]), ph ^ 1u)) {
+          hdr->abort = 1;
+          stop = true;
+          break;
         }
-        for (int i = lo; i < nc; ++i) {
-          const int c = cand[i] - n0;
-          if (c >= kTileN) break;
-          hdr->cbits[b][c >> 5] |= 1u << (c & 31);
-        }
-      }
-      hdr->cpos[b] = lo;
-    }
-    for (int kt = 0; kt < KT; ++kt) {
-      const long long gk = g + kt;
-      const int nxt = kt + kStages - 1;
-      if (nxt < KT) {
-        // The stage of k-step nxt last held k-step nxt - kStages = kt - 1.
-        if (kt >= 1) {
-          const long long gp = gk - 1;
-          if (!mbar_wait(smem_u32(&hdr->empty[gp % kStages]), (uint32_t)((gp / kStages) & 1))) hdr->abort = 1;
-        }
-        load_stage(nxt, (int)((gk + kStages - 1) % kStages));
-      }
-      cp_async_commit();
-      cp_async_wait<kStages - 1>();
-      fence_proxy_async();
-      __syncthreads();
-      if (hdr->abort) {
-        failed = true;
-        break;
-      }
-      if (tid == 0) {
-        tc_fence_after();
-        const int stage = (int)(gk % kStages);
-        const uint32_t a_base = tiles_s + stage * stage_bytes;
+        const uint32_t a_base = tiles_s + stage * C::kStageBytes;
         const uint32_t b_base = a_base + MT * kATileBytes;
+        const uint32_t fb = smem_u32(&hdr->full[stage]);
+        const int k0 = (split * KT + kt) * kTileK;
+        if (lane == 0) {
+          mbar_expect_tx(fb, C::kStageBytes);
+          for (int m = 0; m < MT; ++m) tma_tile_2d(a_base + m * kATileBytes, &tmA, k0, row0 + m * 128, fb);
+          if (!gather) tma_tile_2d(b_base, &tmB, k0, n0, fb);
+        }
+        __syncwarp();
+        if (gather) tma_gather4(b_base + lane * 4 * kRowBytes, &tmG, k0, rr0, rr1, rr2, rr3, fb);
+      }
+      if (stop || hdr->abort) break;
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, kTileN);
+      long long it = 0;
+      int tl = 0;
+      for (int task = blockIdx.x; task < n_tasks; task += gridDim.x, ++tl) {
+        const int acc = tl & 1;
+        if (!mbar_wait(smem_u32(&hdr->tempty[acc]), (uint32_t)(((tl >> 1) & 1) ^ 1))) {
+          hdr->abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * C::kAccCols;
+        bool stop = false;
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int stage = (int)(it % S);
+          if (!mbar_wait(smem_u32(&hdr->full[stage]), (uint32_t)((it / S) & 1))) {
+            hdr->abort = 1;
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = tiles_s + stage * C::kStageBytes;
+          const uint32_t b_base = a_base + MT * kATileBytes;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
+          for (int m = 0; m < MT; ++m) {
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
-            const uint64_t ad = sw128_desc(a_base + m * kATileBytes + kk * 32);
-            const uint64_t bd = sw128_desc(b_base + kk * 32);
-            mma_bf16(tmem + m * kTileN, ad, bd, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTileK / 16; ++kk) {
+              mma_bf16(d + m * kTileN, sw128_desc(a_base + m * kATileBytes + kk * 32), sw128_desc(b_base + kk * 32),
+                       idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(smem_u32(&hdr->empty[stage]));
+        }
+        if (stop) break;
+        mma_commit(smem_u32(&hdr->tfull[acc]));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;        // TMEM lane quarter this warp may read
+    const int et = q * 32 + lane;  // accumulator row = sequence within an M tile
+    int tl = 0;
+    for (int task = blockIdx.x; task < n_tasks; task += gridDim.x, ++tl) {
+      const int tile = task / KS, split = task % KS;
+      const int n0 = tile * kTileN;
+      const int acc = tl & 1;
+      // Which columns of this tile are this thread's sequences' candidates
+      // (computed while the MMAs of this task run).
+      for (int m = 0; m < MT; ++m) {
+        const int b = m * 128 + et;
+#pragma unroll
+        for (int w = 0; w < kTileN / 32; ++w) hdr->cbits[b][w] = 0u;
+        int lo = 0;
+        if (hdr->active[b]) {
+          const int nc = p.ncand[b];
+          const int32_t* cand = p.cand_col + (size_t)b * p.C;
+          int hi = nc;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (cand[mid] < n0) lo = mid + 1; else hi = mid;
+          }
+          for (int i = lo; i < nc; ++i) {
+            const int c = cand[i] - n0;
+            if (c >= kTileN) break;
+            hdr->cbits[b][c >> 5] |= 1u << (c & 31);
           }
         }
-        mma_commit(smem_u32(&hdr->empty[stage]));
+        hdr->cpos[b] = lo;
       }
-    }
-    if (failed) break;
-    // All MMAs of the tile are complete once its last commit has arrived.
-    const long long gl = g + KT - 1;
-    if (!mbar_wait(smem_u32(&hdr->empty[gl % kStages]), (uint32_t)((gl / kStages) & 1))) {
-      hdr->abort = 1;
-    }
-    __syncthreads();
-    if (hdr->abort) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-    g += KT;
-
-    // Epilogue: masked argmax of each sequence over its candidates in this tile.
-    for (int m = 0; m < MT; ++m) {
-      const int b = m * 128 + warp * 32 + lane;
-      const bool has = hdr->xoff[b] >= 0;
-      float bl = -INFINITY;
-      int32_t bc = INT32_MAX;
-      float* sp = KS > 1 && has ? p.split_part + ((size_t)split * p.B + b) * p.C : nullptr;
-      int pos = hdr->cpos[b];  // candidate index of the next set bit
+      if (!mbar_wait(smem_u32(&hdr->tfull[acc]), (uint32_t)((tl >> 1) & 1))) {
+        hdr->abort = 1;
+        break;
+      }
+      tc_fence_after();
+      for (int m = 0; m < MT; ++m) {
+        const int b = m * 128 + et;
+        const bool has = hdr->active[b] != 0;
+        float bl = -INFINITY;
+        int32_t bc = INT32_MAX;
+        float* sp = KS > 1 && has ? p.split_part + ((size_t)split * p.B + b) * p.C : nullptr;
+        int pos = hdr->cpos[b];
 #pragma unroll 1
-      for (int ch = 0; ch < kTileN / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(m * kTileN + ch * 32), v);
-        const int c0 = n0 + ch * 32;
-        const uint32_t bits = hdr->cbits[b][ch];
+        for (int ch = 0; ch < kTileN / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols + m * kTileN + ch * 32), v);
+          const int c0 = n0 + ch * 32;
+          const uint32_t bits = hdr->cbits[b][ch];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if ((bits >> j) & 1u) {
-            const float x = __uint_as_float(v[j]);
-            if (sp) {
-              sp[pos++] = x;  // this split's partial sum of candidate pos
-            } else if (gbetter(x, c0 + j, bl, bc)) {
-              bl = x;
-              bc = c0 + j;
+          for (int j = 0; j < 32; ++j) {
+            if ((bits >> j) & 1u) {
+              const float x = __uint_as_float(v[j]);
+              if (sp) {
+                sp[pos++] = x;  // this split's partial sum of candidate pos
+              } else if (gbetter(x, c0 + j, bl, bc)) {
+                bl = x;
+                bc = c0 + j;
+              }
             }
           }
         }
+        if (has && KS == 1) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
       }
-      if (has && KS == 1) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
+      tc_fence_before();
+      mbar_arrive(smem_u32(&hdr->tempty[acc]));
     }
-    tc_fence_before();
-    __syncthreads();  // TMEM is read before the next tile's MMAs overwrite it
-    tc_fence_after();
   }
 
-  if (failed) {
-    cp_async_wait_all();
-    if (tid == 0) atomicExch(p.err, 1);
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MT * kTileN) : "memory");
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
   }
+  if (tid == 0 && hdr->abort) atomicExch(p.err, 1);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+cudaError_t encode_2d(CUtensorMap* m, const void* base, int64_t rows, int H, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encoder();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes(int mt) {
-  return 1024 + (size_t)kStages * (mt * kATileBytes + kBTileBytes) + sizeof(GemmSmemHeader);
+  return mt == 2 ? 1024 + (size_t)Cfg<2>::kStages * Cfg<2>::kStageBytes + sizeof(GemmHdr)
+                 : 1024 + (size_t)Cfg<1>::kStages * Cfg<1>::kStageBytes + sizeof(GemmHdr);
 }
 
 cudaError_t prepare_gemm() {
@@ -333,13 +403,24 @@ cudaError_t prepare_gemm() {
 
 int gemm_tile_cols() { return kTileN; }
 
-cudaError_t launch_union_gemm(const GemmParams& p, int num_ctas, cudaStream_t s) {
+cudaError_t encode_emb_maps(const void* emb, int V, int H, EmbMaps* out) {
+  cudaError_t e = encode_2d(&out->tiled, emb, V, H, kTileN);
+  if (e != cudaSuccess) return e;
+  return encode_2d(&out->gather, emb, V, H, 1);
+}
+
+cudaError_t launch_union_gemm(const GemmParams& p, const void* hidden, int64_t rows, const EmbMaps& emb,
+                              int num_ctas, cudaStream_t s) {
   if (p.H % kTileK != 0 || p.B < 1 || p.B > 256 || p.ksplit < 1 || (p.H / kTileK) % p.ksplit != 0 ||
       (p.ksplit > 1 && !p.split_part))
     return cudaErrorInvalidValue;
-  const int mt = p.B > 128 ? 2 : 1;
-  if (mt == 1) union_gemm_kernel<1><<<num_ctas, kThreadsG, gemm_smem_bytes(1), s>>>(p);
-  else union_gemm_kernel<2><<<num_ctas, kThreadsG, gemm_smem_bytes(2), s>>>(p);
+  CUtensorMap a;
+  cudaError_t e = encode_2d(&a, hidden, rows, p.H, 128);
+  if (e != cudaSuccess) return e;
+  if (p.B > 128)
+    union_gemm_kernel<2><<<num_ctas, kThreadsG, gemm_smem_bytes(2), s>>>(p, a, emb.tiled, emb.gather);
+  else
+    union_gemm_kernel<1><<<num_ctas, kThreadsG, gemm_smem_bytes(1), s>>>(p, a, emb.tiled, emb.gather);
   return cudaGetLastError();
 }
 

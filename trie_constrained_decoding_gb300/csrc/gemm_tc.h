@@ -1,24 +1,24 @@
 // Host-visible interface of the tcgen05 GEMM with a masked-argmax epilogue.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (types only; the encoder is fetched through the runtime)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace tcd {
 
-// Best candidate of one sequence within one 256-column tile.
+// Best candidate of one sequence within one column tile.
 struct GemmPartial {
   float logit;
   int32_t col;  // INT32_MAX when the sequence has no candidate in the tile
 };
 
 struct GemmParams {
-  const uint16_t* hidden;    // bf16 activations
-  const int64_t* xrow;       // [B] element offset of each sequence's hidden row; -1: no row (inactive)
+  const int64_t* xrow;       // [B] >= 0 for sequences that take this step, -1 otherwise
+  const int32_t* row0_ptr;   // device: first activation row of the step in the activation map (null: 0)
   int32_t B;                 // sequences, <= 256
-  const uint16_t* emb;       // bf16 [V, H]
   int32_t H;                 // multiple of 64
-  const int32_t* row_list;   // [n_cols] embedding row of each column, or null (column = row)
+  const int32_t* row_list;   // [n_cols] embedding row of each column (gathered), or null (column = row)
   const int32_t* n_cols_ptr; // device column count (read at kernel start), or null
   int32_t n_cols_fixed;      // column count when n_cols_ptr is null
   const int32_t* cand_col;   // [B, C] ascending columns of each sequence's legal candidates
@@ -31,10 +31,20 @@ struct GemmParams {
   int32_t* err;              // set to 1 when a wait timed out
 };
 
+// Tensor maps of the embedding: 64 x 128 boxes (contiguous rows) and 64 x 1
+// boxes for four-row gathers; both bf16 with the 128-byte swizzle.
+struct EmbMaps {
+  CUtensorMap tiled;
+  CUtensorMap gather;
+};
+
 size_t gemm_smem_bytes(int m_tiles);
 int gemm_tile_cols();
 // Opt in to the GEMM's dynamic shared memory (current device).
 cudaError_t prepare_gemm();
-cudaError_t launch_union_gemm(const GemmParams& p, int num_ctas, cudaStream_t s);
+cudaError_t encode_emb_maps(const void* emb, int V, int H, EmbMaps* out);
+// hidden: bf16 activations with `rows` rows of H elements (the A operand).
+cudaError_t launch_union_gemm(const GemmParams& p, const void* hidden, int64_t rows, const EmbMaps& emb,
+                              int num_ctas, cudaStream_t s);
 
 }  // namespace tcd

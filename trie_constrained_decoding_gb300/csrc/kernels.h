@@ -53,6 +53,7 @@ struct GrammarView {
 };
 
 struct GemmPartial;  // gemm_tc.h
+struct EmbMaps;      // gemm_tc.h
 
 // Scratch of the GEMM heads (candidate lists in global memory, the union of
 // legal rows, per-(sequence, column tile) partial results).
@@ -73,6 +74,8 @@ struct HeadScratch {
   float* split_part;        // [ksplit, B, C] per-split candidate sums of the union GEMM
   int32_t union_mode;       // 1: columns are the union; 0: every vocabulary row
   int32_t* gemm_err;        // [1] GEMM wait timeout
+  int32_t* row0;            // [1] first activation row of the current step
+  const EmbMaps* emb_maps;  // host: tensor maps of the embedding
 };
 
 struct StepParams {
@@ -80,6 +83,7 @@ struct StepParams {
   const uint16_t* emb;      // bf16 [V, H]
   int32_t V, H;
   const uint16_t* hidden;   // bf16 [B, H] (host form) or [S, B, H] (device form: row len_b * B + b)
+  int64_t hidden_rows;      // rows of `hidden` (B, or S * B)
   SeqState* st;             // [B]
   int32_t* cnt;             // [B, E] live-pointer counts
   uint32_t* spent;          // [B, kw] spent flags

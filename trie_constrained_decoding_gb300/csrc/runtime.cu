@@ -147,6 +147,7 @@ struct tc_ctx {
   Ctrl* d_ctrl = nullptr;
   unsigned long long* d_stats = nullptr;
   HeadScratch hs{};           // GEMM-head scratch, allocated on first use
+  EmbMaps emb_maps{};         // tensor maps of the embedding for the GEMM heads
   bool hs_ready = false;
   int32_t* h_live = nullptr;  // pinned
   cudaStream_t capture_stream = nullptr;
@@ -192,6 +193,10 @@ tc_status ensure_gemm_scratch(tc_ctx* c) {
   h.ksplit = (c->H / 64) % 4 == 0 ? c->H / 256 : 1;
   if (e == cudaSuccess && h.ksplit > 1) e = cudaMalloc(&h.split_part, (size_t)h.ksplit * BC * 4);
   if (e == cudaSuccess) e = cudaMalloc(&h.gemm_err, 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h.row0, 4);
+  if (e == cudaSuccess) e = cudaMemset(h.row0, 0, 4);
+  if (e == cudaSuccess) e = encode_emb_maps(c->emb, c->V, c->H, &c->emb_maps);
+  h.emb_maps = &c->emb_maps;
   if (e == cudaSuccess) e = cudaMemset(h.gemm_err, 0, 4);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM-head scratch");
   c->hs_ready = true;
@@ -213,6 +218,7 @@ void free_gemm_scratch(tc_ctx* c) {
   cudaFree(h.part);
   cudaFree(h.split_part);
   cudaFree(h.gemm_err);
+  cudaFree(h.row0);
   c->hs_ready = false;
 }
 
@@ -374,6 +380,7 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
     return fail(e, "cudaStreamBeginCaptureToGraph(body)");
   StepParams p = step_params(c, g, key.batch);
   p.hidden = static_cast<const uint16_t*>(key.hidden);
+  p.hidden_rows = (int64_t)key.n_steps * key.batch;
   p.tok_out = static_cast<int32_t*>(key.toks);
   p.logit_out = static_cast<float*>(key.logits);
   p.status_out = static_cast<int32_t*>(key.status);
@@ -590,6 +597,7 @@ extern "C" tc_status tc_step(tc_ctx* c, const void* hidden, int32_t head, int32_
   if (rc != TC_OK) return rc;
   StepParams p = step_params(c, g, g->batch);
   p.hidden = static_cast<const uint16_t*>(hidden);
+  p.hidden_rows = g->batch;
   p.tok_out = tok_out;
   p.logit_out = logit_out;
   p.status_out = status_out;
@@ -683,6 +691,7 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
   for (int32_t t = 0; t < max_steps; ++t) {
     StepParams p = step_params(c, g, batch);
     p.hidden = static_cast<const uint16_t*>(hidden) + (size_t)t * row;
+    p.hidden_rows = batch;
     p.tok_out = toks + t;
     p.logit_out = logits + t;
     p.status_out = status;

@@ -44,7 +44,7 @@ __constant__ int32_t c_walk[TC_CONST_CAPACITY_BYTES / 4];
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int gemm_tile_cols_dev = 256;  // columns per GEMM tile (gemm_tc.cu)
+constexpr int gemm_tile_cols_dev = 128;  // columns per GEMM tile (gemm_tc.cu)
 
 template <bool kConst>
 struct WalkRd {
@@ -768,6 +768,9 @@ __global__ void __launch_bounds__(kThreads) cand_filter_kernel(const StepParams 
     hs.ncand[b] = n;
     hs.errf[b] = sh.err;
     hs.xrow[b] = (int64_t)(((size_t)(p.device_form ? s.len : 0) * (size_t)p.B + (size_t)b) * (size_t)p.H);
+    // Every stepping sequence is at the same step: its activation rows start at
+    // len * B (identical writes from all of them).
+    *hs.row0 = p.device_form ? s.len * p.B : 0;
   }
 }
 
@@ -840,7 +843,7 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
   int32_t wt = INT_MAX, we = -1;
   if (mode == 1) {
     const int n = hs.ncand[b];
-    const int err = hs.errf[b];
+    const int err = hs.errf[b] | *hs.gemm_err;  // a GEMM wait that timed out fails the step
     const int n_cols = hs.union_mode ? *hs.n_union : p.V;
     const int n_tiles = (n_cols + gemm_tile_cols_dev - 1) / gemm_tile_cols_dev;
     int32_t bc = INT_MAX;  // winning column (tile partials)
@@ -1016,10 +1019,9 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   GemmParams gp{};
-  gp.hidden = p.hidden;
   gp.xrow = q.hs.xrow;
+  gp.row0_ptr = q.hs.row0;
   gp.B = p.B;
-  gp.emb = p.emb;
   gp.H = p.H;
   gp.row_list = q.hs.union_mode ? q.hs.ulist : nullptr;
   gp.n_cols_ptr = q.hs.union_mode ? q.hs.n_union : nullptr;
@@ -1032,7 +1034,7 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
   gp.ksplit = q.hs.union_mode ? q.hs.ksplit : 1;
   gp.split_part = q.hs.split_part;
   gp.err = q.hs.gemm_err;
-  if ((e = launch_union_gemm(gp, gemm_ctas, s)) != cudaSuccess) return e;
+  if ((e = launch_union_gemm(gp, p.hidden, p.hidden_rows, *q.hs.emb_maps, gemm_ctas, s)) != cudaSuccess) return e;
   if (const_resident) gemm_finish_kernel<true><<<dim3(1, p.B), kThreads, 0, s>>>(q);
   else gemm_finish_kernel<false><<<dim3(1, p.B), kThreads, 0, s>>>(q);
   return cudaGetLastError();
