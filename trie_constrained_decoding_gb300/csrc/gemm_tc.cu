@@ -170,6 +170,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   GemmHdr* hdr = reinterpret_cast<GemmHdr*>(tiles + S * C::kStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tiles_s = smem_u32(tiles);
+  // Launched as a programmatic dependent of the step's previous kernel: wait
+  // for its results before reading any of them, and let the next kernel start
+  // launching now.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -417,11 +422,18 @@ cudaError_t launch_union_gemm(const GemmParams& p, const void* hidden, int64_t r
   CUtensorMap a;
   cudaError_t e = encode_2d(&a, hidden, rows, p.H, 128);
   if (e != cudaSuccess) return e;
-  if (p.B > 128)
-    union_gemm_kernel<2><<<num_ctas, kThreadsG, gemm_smem_bytes(2), s>>>(p, a, emb.tiled, emb.gather);
-  else
-    union_gemm_kernel<1><<<num_ctas, kThreadsG, gemm_smem_bytes(1), s>>>(p, a, emb.tiled, emb.gather);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(kThreadsG);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(p.B > 128 ? 2 : 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.B > 128) return cudaLaunchKernelEx(&cfg, union_gemm_kernel<2>, p, a, emb.tiled, emb.gather);
+  return cudaLaunchKernelEx(&cfg, union_gemm_kernel<1>, p, a, emb.tiled, emb.gather);
 }
 
 }  // namespace tcd

@@ -104,6 +104,7 @@ struct StepParams {
   int32_t loop_ctrl;        // 1: this launch sets the loop's condition (last step of a loop body)
   unsigned long long* stats;  // optional counters, see StatSlot
   HeadScratch hs;           // GEMM heads only
+  int4* pre;                // [B, 32] precomputed candidate lists (one-CTA sparse step), or null
 };
 
 // Cumulative counters kept by the kernels (one atomic per launch / per sequence step).

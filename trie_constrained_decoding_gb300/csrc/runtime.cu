@@ -87,6 +87,7 @@ struct DevGrammar {
   SeqState* d_st = nullptr;
   int32_t* d_cnt = nullptr;
   uint32_t* d_spent = nullptr;
+  int4* d_pre = nullptr;  // [max_batch, 32] next-step candidate lists
   int32_t kw = 1;
   int32_t batch = 0, k = 0;  // of the last reset (0: none)
 
@@ -111,6 +112,7 @@ struct DevGrammar {
     cudaFree(d_st);
     cudaFree(d_cnt);
     cudaFree(d_spent);
+    cudaFree(d_pre);
   }
 };
 
@@ -157,7 +159,12 @@ struct tc_ctx {
 
 namespace {
 
+// Grammars whose nodes have at most 32 edges take the one-CTA sparse step,
+// which also precomputes the next step's candidates.
+bool one_cta_sparse(const DevGrammar* g) { return g->max_fanout <= 32; }
+
 int tiles_for(const tc_ctx* c, const DevGrammar* g, int head, int B) {
+  if (head == TC_HEAD_SPARSE && one_cta_sparse(g)) return 1;
   return head == TC_HEAD_SPARSE ? sparse_tiles(g->max_fanout, B, c->num_sms) : dense_tiles(B, c->num_sms);
 }
 
@@ -263,6 +270,7 @@ StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
   p.ctrl = c->d_ctrl;
   p.stats = c->d_stats;
   p.max_steps = INT32_MAX;
+  p.pre = one_cta_sparse(g) ? g->d_pre : nullptr;
   return p;
 }
 
@@ -534,6 +542,8 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
     if (e == cudaSuccess) e = cudaMalloc(&g->d_st, sizeof(SeqState) * B);
     if (e == cudaSuccess) e = cudaMalloc(&g->d_cnt, sizeof(int32_t) * B * std::max<int32_t>(1, g->n_edges));
     if (e == cudaSuccess) e = cudaMalloc(&g->d_spent, sizeof(uint32_t) * B * g->kw);
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_pre, sizeof(int4) * B * 32);
+    if (e == cudaSuccess) e = cudaMemset(g->d_pre, 0, sizeof(int4) * B * 32);
     if (e == cudaSuccess) e = cudaMemcpy(g->d_img, img.data(), img_bytes, cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
       e = cudaMemcpy(g->d_static_cnt, t->static_cnt.data(), sizeof(int32_t) * t->static_cnt.size(), cudaMemcpyHostToDevice);

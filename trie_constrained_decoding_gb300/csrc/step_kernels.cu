@@ -532,6 +532,270 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh);
 }
 
+// ---------------------------------------------------------------- one-CTA sparse step
+//
+// For grammars whose nodes have at most 32 edges each sequence is served by
+// one CTA, and the step also prepares the next one.  When the winner is a
+// token edge the next node is its child, and the child's legal set depends
+// only on state this step does not change (live counts change only when a
+// pointer completes, the spent flags and the pointer count likewise), so each
+// warp computes its candidate's child legal set while that candidate's
+// embedding row is in flight.  The winner's set is stored as the sequence's
+// precomputed candidate list; the next step reads it together with the
+// sequence state instead of filtering the node (the mask is computed ahead of
+// time, as "GLRMask" computes it in parallel with the forward pass).  After a
+// separator or a stop, or when a set does not fit, the next step filters.
+constexpr int kPreMax = 32;
+
+struct Step1Shared {
+  int4 cand[kPreMax];                 // {token, edge, child, live count} of this step's candidates
+  int4 spec[kPreMax][kPreMax];        // per candidate: its child's legal candidates
+  int32_t spec_n[kPreMax];            // their number, -1 when not available
+  int32_t spec_pid[kPreMax];          // the child's pointer id
+  float wl[kWarps];
+  int32_t wt[kWarps], wslot[kWarps];
+  int32_t ncand, err, pid, done_after;
+};
+
+// Legal candidates of node `node` into out[] (one warp, node fan-out <= 32).
+// Returns the count, or -1 when an index is out of range or the fan-out is larger.
+template <bool kConst>
+__device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
+                                              int b, int beg, int end, int pid, int lane, int4* out) {
+  if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > kPreMax) return -1;
+  int bad = pid >= p.g.n_strings;
+  const uint32_t word = (pid >= 0 && pid < p.g.n_strings) ? p.spent[(size_t)b * p.kw + (pid >> 5)] : 1u;
+  const bool ctl_ok = pid >= 0 && !bad && ((word >> (pid & 31)) & 1u) == 0;
+  const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
+  const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
+  const int e = beg + lane;
+  int2 ed = make_int2(0, 0);
+  int32_t c = 0;
+  bool legal = false;
+  if (e < end) {
+    ed = w.edge(e);
+    c = p.cnt[(size_t)b * p.g.n_edges + e];
+    if (ed.x < 0 || ed.x >= p.V) bad = 1;
+    else if (ed.y >= 0) { if (ed.y >= p.g.n_nodes) bad = 1; else legal = c > 0; }
+    else if (ed.y == -1) legal = sep_ok;
+    else if (ed.y == -2) legal = stop_ok;
+    else bad = 1;
+  }
+  const unsigned bal = __ballot_sync(kFull, legal);
+  if (legal) out[__popc(bal & ((1u << lane) - 1u))] = make_int4(ed.x, e, ed.y, c);
+  if (__ballot_sync(kFull, bad)) return -1;
+  return __popc(bal);
+}
+
+template <bool kConst, int NCH>
+__global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ Step1Shared sh;
+  pdl_enter();
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
+  // The state and this warp's first precomputed candidate are read together.
+  const SeqState s = p.st[b];
+  const int4 pre0 = p.pre[(size_t)b * kPreMax + warp];
+  const int mode = seq_mode(p, s);
+  const int nch = p.H >> 3;
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
+
+  float wl = -INFINITY;
+  int32_t wt = INT_MAX, ws = -1;
+  if (mode == 1) {
+    const uint16_t* x = hidden_row(p, s, b);
+    XFrag<NCH> xf;
+    if constexpr (NCH > 0) {
+      xf.load(x, lane);
+    } else {
+      for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
+    }
+    const bool pre = s.pad0 > 0;
+    if (!pre) {
+      // Filter the node (fan-out <= 32: one warp).
+      if (warp == 0) {
+        const int n = s.node;
+        const bool n_ok = n >= 0 && n < p.g.n_nodes;
+        const int nn = n_ok ? n : 0;
+        const int beg = w.begin(nn), end = w.begin(nn + 1), pid = w.ptr(nn);
+        const int cnt = n_ok ? warp_legal_set<kConst>(p, w, s, b, beg, end, pid, lane, sh.cand) : -1;
+        if (lane == 0) {
+          sh.ncand = cnt < 0 ? 0 : cnt;
+          sh.err = cnt < 0;
+          sh.pid = pid;
+        }
+      }
+    } else if (tid == 0) {
+      sh.ncand = s.pad0 - 1;
+      sh.err = 0;
+      sh.pid = s.pad1;
+    }
+    __syncthreads();
+    const int n = sh.ncand;
+    if (!sh.err) {
+      for (int l = warp; l < n; l += kWarps) {
+        const int4 cd = pre ? (l == warp ? pre0 : p.pre[(size_t)b * kPreMax + l]) : sh.cand[l];
+        // child record first, then the row, then the child's edges
+        const bool spec = cd.z >= 0 && cd.z < p.g.n_nodes;
+        const int cc = spec ? cd.z : 0;
+        const int cb = w.begin(cc), ce = w.begin(cc + 1), cpid = w.ptr(cc);
+        const uint4* r4 = reinterpret_cast<const uint4*>(p.emb + (size_t)cd.x * p.H);
+        float acc = 0.f;
+        if constexpr (NCH > 0) {
+          uint4 e[NCH];
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) e[i] = ld_row(r4 + i * 32 + lane);
+          const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
+          if (lane == 0) {
+            sh.spec_n[l] = sn;
+            sh.spec_pid[l] = cpid;
+          }
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xf.v[i], acc);
+        } else {
+          const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
+          if (lane == 0) {
+            sh.spec_n[l] = sn;
+            sh.spec_pid[l] = cpid;
+          }
+          for (int c = lane; c < nch; c += 32) acc = dot8(ld_row(r4 + c), xs[c], acc);
+        }
+        const float v = warp_sum(acc);
+        if (pre) {
+          if (lane == 0) sh.cand[l] = cd;  // the winner's edge data is read from here below
+        }
+        if (better(v, cd.x, wl, wt)) {
+          wl = v;
+          wt = cd.x;
+          ws = l;
+        }
+      }
+    }
+    if (lane == 0) {
+      sh.wl[warp] = wl;
+      sh.wt[warp] = wt;
+      sh.wslot[warp] = ws;
+    }
+  }
+  if (p.stats && tid == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
+  __syncthreads();
+
+  if (mode == 1) {
+    // Every thread folds the eight warp bests (same order, same result).
+    float bl = -INFINITY;
+    int32_t bt = INT_MAX, bs = -1;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i)
+      if (better(sh.wl[i], sh.wt[i], bl, bt)) { bl = sh.wl[i]; bt = sh.wt[i]; bs = sh.wslot[i]; }
+    const int ncand = sh.ncand;
+    int status = TC_OK;
+    int32_t new_node = s.node, ptr_done = -1;
+    bool stop = false;
+    int4 win = make_int4(0, -1, 0, 0);
+    if (sh.err) {
+      status = TC_ERR_BOUNDS;
+    } else if (ncand == 0) {
+      status = TC_ERR_EMPTY_MASK;
+    } else if (bs < 0 || !(bl == bl)) {
+      status = TC_ERR_BOUNDS;  // no comparable logit (NaN)
+    } else {
+      win = sh.cand[bs];
+      if (win.z >= 0) {
+        if (win.w <= 0) status = TC_ERR_NO_LIVE_EDGE;  // live count read this step
+        else new_node = win.z;
+      } else {
+        const int32_t pid = sh.pid;
+        if (pid < 0 || pid >= p.g.n_strings ||
+            ((p.spent[(size_t)b * p.kw + (pid >> 5)] >> (pid & 31)) & 1u)) {
+          status = TC_ERR_NO_LIVE_EDGE;
+        } else {
+          ptr_done = pid;
+          stop = win.z == -2;
+          new_node = 0;
+        }
+      }
+    }
+    // The winner's child legal set becomes the next step's candidate list.
+    const int next_n = (status == TC_OK && ptr_done < 0) ? sh.spec_n[bs] : -1;
+    if (next_n > 0)
+      for (int i = tid; i < next_n; i += kThreads) p.pre[(size_t)b * kPreMax + i] = sh.spec[bs][i];
+    if (ptr_done >= 0) {
+      const int32_t q0 = __ldg(p.g.path_off + ptr_done), q1 = __ldg(p.g.path_off + ptr_done + 1);
+      int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
+      for (int32_t q = q0 + tid; q < q1; q += kThreads) {
+        const int32_t e = __ldg(p.g.path + q);
+        if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
+      }
+    }
+    if (tid == 0) {
+      SeqState ns = s;
+      if (status != TC_OK) {
+        ns.status = status;
+        ns.done = 1;
+        ns.pad0 = 0;
+      } else {
+        ns.node = new_node;
+        ns.len = s.len + 1;
+        if (ptr_done >= 0) {
+          ns.emitted = s.emitted + 1;
+          p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
+        }
+        if (stop) ns.done = 1;
+        ns.pad0 = next_n >= 0 ? next_n + 1 : 0;
+        ns.pad1 = next_n >= 0 ? sh.spec_pid[bs] : -2;
+      }
+      p.st[b] = ns;
+      if (p.stats) {
+        atomicAdd(&p.stats[kStatSeqSteps], 1ull);
+        atomicAdd(&p.stats[kStatCandRows], (unsigned long long)ncand);
+      }
+      if (p.device_form) {
+        if (status == TC_OK && s.len < p.out_stride) {
+          p.tok_out[(size_t)b * p.out_stride + s.len] = bt;
+          p.logit_out[(size_t)b * p.out_stride + s.len] = bl;
+        }
+      } else {
+        p.tok_out[(size_t)b * p.out_stride] = status == TC_OK ? bt : -1;
+        if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = status == TC_OK ? bl : 0.f;
+      }
+      if (p.status_out) p.status_out[b] = ns.status;
+      if (p.lens_out) p.lens_out[b] = ns.len;
+      if (ns.done) atomicSub(&p.ctrl->live, 1);
+      sh.done_after = ns.done;
+    }
+  } else if (tid == 0) {
+    if (mode == 2) {
+      stop_out_of_steps(p, s, b);
+    } else if (!p.device_form) {
+      p.tok_out[(size_t)b * p.out_stride] = -1;
+      if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = 0.f;
+      if (p.status_out) p.status_out[b] = s.status;
+      if (p.lens_out) p.lens_out[b] = s.len;
+    }
+    sh.done_after = 1;
+  }
+
+  if (p.loop_ctrl) {
+    if (gridDim.y == 1) {
+      if (tid == 0) cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, sh.done_after ? 0u : 1u);
+    } else {
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        const uint32_t g = atomicAdd(&p.ctrl->ticket, 1u);
+        if (g == gridDim.y - 1) {
+          __threadfence();
+          const int32_t live = atomicAdd(&p.ctrl->live, 0);
+          p.ctrl->ticket = 0u;
+          cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, live > 0 ? 1u : 0u);
+        }
+      }
+    }
+  }
+}
+
 // Dense head: every vocabulary row, then the legal mask, then the argmax.
 //
 // Each CTA owns a contiguous block of rows and streams it through shared
@@ -737,6 +1001,7 @@ template <bool kConst>
 __global__ void __launch_bounds__(kThreads) cand_filter_kernel(const StepParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ StepShared sh;
+  pdl_enter();
   const int b = blockIdx.y, tid = threadIdx.x;
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
   const SeqState s = p.st[b];
@@ -779,6 +1044,7 @@ __global__ void __launch_bounds__(kThreads) cand_filter_kernel(const StepParams 
 constexpr int kCompactThreads = 1024;
 __global__ void __launch_bounds__(kCompactThreads) union_compact_kernel(const StepParams p) {
   __shared__ int32_t s_warp[kCompactThreads / 32];
+  pdl_enter();
   const HeadScratch& hs = p.hs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int words = (p.V + 31) >> 5;
@@ -821,6 +1087,7 @@ __global__ void __launch_bounds__(kCompactThreads) union_compact_kernel(const St
 
 // Grid (1, B): the GEMM column of each of sequence b's candidates.
 __global__ void __launch_bounds__(kThreads) cand_column_kernel(const StepParams p) {
+  pdl_enter();
   const HeadScratch& hs = p.hs;
   const int b = blockIdx.y;
   const int n = hs.ncand[b];
@@ -834,6 +1101,7 @@ __global__ void __launch_bounds__(kThreads) cand_column_kernel(const StepParams 
 template <bool kConst>
 __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams p) {
   __shared__ StepShared sh;
+  pdl_enter();
   const int b = blockIdx.y, tid = threadIdx.x;
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
   const SeqState s = p.st[b];
@@ -953,6 +1221,11 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if (head == kHeadSparse && p.pre) {
+    cfg.gridDim = dim3(1, p.B);
+    cfg.dynamicSmemBytes = xbytes;
+    return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH>, p);
+  }
   if (head == kHeadSparse) return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH>, p);
   return cudaLaunchKernelEx(&cfg, dense_step_kernel<kConst, NCH>, p);
 }
@@ -1001,6 +1274,21 @@ cudaError_t launch_reset(const ResetParams& r, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <class... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head, int gemm_ctas, cudaStream_t s) {
   StepParams q = p;
   q.hs.union_mode = head == kHeadUnionGemm;
@@ -1008,15 +1296,15 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
   StepParams no_ctrl = q;
   no_ctrl.loop_ctrl = 0;
   no_ctrl.stats = nullptr;
-  if (const_resident) cand_filter_kernel<true><<<dim3(1, p.B), kThreads, fsmem, s>>>(no_ctrl);
-  else cand_filter_kernel<false><<<dim3(1, p.B), kThreads, fsmem, s>>>(no_ctrl);
-  cudaError_t e = cudaGetLastError();
+  // Every kernel of the step is a programmatic dependent of the one before
+  // (each waits for its predecessor at entry), so launch latency overlaps.
+  cudaError_t e = const_resident
+                      ? launch_pdl(cand_filter_kernel<true>, dim3(1, p.B), dim3(kThreads), fsmem, s, no_ctrl)
+                      : launch_pdl(cand_filter_kernel<false>, dim3(1, p.B), dim3(kThreads), fsmem, s, no_ctrl);
   if (e != cudaSuccess) return e;
   if (q.hs.union_mode) {
-    union_compact_kernel<<<1, kCompactThreads, 0, s>>>(no_ctrl);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    cand_column_kernel<<<dim3(1, p.B), kThreads, 0, s>>>(no_ctrl);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(union_compact_kernel, dim3(1), dim3(kCompactThreads), 0, s, no_ctrl)) != cudaSuccess) return e;
+    if ((e = launch_pdl(cand_column_kernel, dim3(1, p.B), dim3(kThreads), 0, s, no_ctrl)) != cudaSuccess) return e;
   }
   GemmParams gp{};
   gp.xrow = q.hs.xrow;
@@ -1035,9 +1323,8 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
   gp.split_part = q.hs.split_part;
   gp.err = q.hs.gemm_err;
   if ((e = launch_union_gemm(gp, p.hidden, p.hidden_rows, *q.hs.emb_maps, gemm_ctas, s)) != cudaSuccess) return e;
-  if (const_resident) gemm_finish_kernel<true><<<dim3(1, p.B), kThreads, 0, s>>>(q);
-  else gemm_finish_kernel<false><<<dim3(1, p.B), kThreads, 0, s>>>(q);
-  return cudaGetLastError();
+  return const_resident ? launch_pdl(gemm_finish_kernel<true>, dim3(1, p.B), dim3(kThreads), 0, s, q)
+                        : launch_pdl(gemm_finish_kernel<false>, dim3(1, p.B), dim3(kThreads), 0, s, q);
 }
 
 cudaError_t launch_finalize(const StepParams& p, cudaStream_t s) {
