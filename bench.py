@@ -125,6 +125,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def sparse_kernel_name(max_fanout: int) -> str:
+    """The sparse-step kernel the library launches for a grammar: the one-CTA
+    kernel when no node has more than 32 edges."""
+    return "sparse_step1_kernel" if max_fanout <= 32 else "sparse_step_kernel"
+
+
 def recorded_traffic(source: str, profile: str):
     """DRAM bytes per launch recorded by the last ncu capture of a kernel, or
     None when the kernel's source file has changed since that capture."""
@@ -325,7 +331,7 @@ def run_ours(args):
     roof = None
     if not args.no_extras:
         roof, extras = extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids[W:], head, flush,
-                                    hid_buf, toks, logits, lens, status)
+                                    hid_buf, toks, logits, lens, status, tinfo["max_fanout"])
         e2e = extras.pop("e2e")
 
     if rank != 0:
@@ -337,9 +343,10 @@ def run_ours(args):
         roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if peak_kind == "measured" \
             else "fallback 6.8 TB/s"
         if head == tcd.HEAD_SPARSE and args.workload == "large_head":
-            roof["traffic"] = recorded_traffic("step_kernels.cu", "sparse_step_kernel_large_head.md")
+            prof = f"{sparse_kernel_name(tinfo['max_fanout'])}_large_head.md"
+            roof["traffic"] = recorded_traffic("step_kernels.cu", prof)
             roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, cold caches, "
-                                      "profiles/sparse_step_kernel_large_head.md" if roof["traffic"] is not None
+                                      f"profiles/{prof}" if roof["traffic"] is not None
                                       else "kernel source changed since the last ncu capture")
     cpu = None
     if world == 1 and not args.no_extras:
@@ -375,7 +382,7 @@ def run_ours(args):
 
 
 def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, head, flush, hid_buf, toks, logits,
-                 lens, status):
+                 lens, status, max_fanout):
     """Roofline of the step kernel, dense-head comparison, host loop and end-to-end rate."""
     B, S, H = w.batch, w.max_steps, w.hidden
     out = {}
@@ -423,7 +430,7 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     warm_ms = kernel_pass(False)
     warm_mean = sum(warm_ms) / len(warm_ms)
     roof = {"bound": "hbm", "achieved": achieved, "peak": None, "unit": "GB/s", "frac": None, "traffic": None,
-            "kernel": {tcd.HEAD_SPARSE: "sparse_step_kernel", tcd.HEAD_DENSE: "dense_step_kernel"}.get(
+            "kernel": {tcd.HEAD_SPARSE: sparse_kernel_name(max_fanout), tcd.HEAD_DENSE: "dense_step_kernel"}.get(
                 head, "GEMM-head step (filter, union compaction, tcgen05 GEMM, finish)"),
             "algorithmic_bytes_per_launch": algo_bytes / launches,
             "mean_launch_us_cold_l2": mean_ms * 1000.0, "mean_launch_us_warm_l2": warm_mean * 1000.0,

@@ -494,7 +494,7 @@ __device__ __forceinline__ void pdl_enter() {
 
 template <bool kConst, int NCH>
 __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ StepShared sh;
   pdl_enter();
   const int b = blockIdx.y, t = blockIdx.x, T = gridDim.x;
@@ -589,7 +589,7 @@ __device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<
 
 template <bool kConst, int NCH>
 __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ Step1Shared sh;
   pdl_enter();
   const int b = blockIdx.y;
@@ -999,7 +999,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const StepParams p) 
 // Grid (1, B): filter the node of sequence b into global candidate lists.
 template <bool kConst>
 __global__ void __launch_bounds__(kThreads) cand_filter_kernel(const StepParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ StepShared sh;
   pdl_enter();
   const int b = blockIdx.y, tid = threadIdx.x;
