@@ -66,6 +66,8 @@ def parse_args():
                     help="grammar residency (default: the workload's)")
     ap.add_argument("--loop", choices=["graph", "host"], default="graph",
                     help="timed loop: the captured device-resident graph (default) or host-driven steps")
+    ap.add_argument("--jump", action="store_true",
+                    help="forced continuations: emit grammar-forced tokens without the head (sparse/dense heads)")
     return ap.parse_args()
 
 
@@ -190,34 +192,95 @@ def host_hidden(w, qids):
     return {q: np.ascontiguousarray(all_h[q - start]) for q in uniq}
 
 
-def oracle_baseline(w, seconds: float, head: str = "sparse"):
-    """Greedy decode with the oracle on the host, query by query, for about `seconds`."""
+def _oracle_batches(w, seconds: float, batches, hid_of, head: str):
+    """Decode query batches in order with the oracle for about `seconds`;
+    return (decode steps, tokens, batches decoded, seconds)."""
     from oracle import decode as D
     from oracle import grammar as G
     trie = G.compile_catalog(w.catalog, w.sep_id, w.stop_id, w.vocab, max_fanout=w.max_fanout)
-    emb = w.embedding()
-    n_batches = max(1, min(w.n_queries // w.batch, max(1, 256 // w.batch)))
-    hid = w.hidden_states(0, n_batches * w.batch)          # generated before the clock starts
+    emb = hid_of("emb")
     t0 = time.perf_counter()
-    steps = tokens = queries = 0
-    q = 0
+    steps = tokens = done = 0
+    i = 0
     while True:
-        base = q * w.batch
+        hid = hid_of(batches[i])
         lens = []
         for b in range(w.batch):
-            toks, _, _ = D.greedy_decode(trie, w.k, emb, hid[:, base + b], w.max_steps, head=head)
+            toks, _, _ = D.greedy_decode(trie, w.k, emb, hid[:, b], w.max_steps, head=head)
             lens.append(len(toks))
         tokens += sum(lens)
-        steps += max(lens)
-        queries += 1
-        q = (q + 1) % n_batches
+        steps += max(lens)                  # lockstep: the batch steps until its longest sequence stops
+        done += 1
+        i = (i + 1) % len(batches)
         if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
+    return steps, tokens, done, time.perf_counter() - t0
+
+
+def oracle_baseline(w, seconds: float, head: str = "sparse"):
+    """Greedy decode with the oracle on the host, one process, for about `seconds`."""
+    emb = w.embedding()
+    n_batches = max(1, min(w.n_queries // w.batch, max(1, 256 // w.batch)))
+    hid = {q: w.hidden_states(q * w.batch, w.batch) for q in range(n_batches)}   # before the clock starts
+    steps, tokens, done, dt = _oracle_batches(w, seconds, list(range(n_batches)),
+                                              lambda q: emb if q == "emb" else hid[q], head)
     return {"value": steps / dt, "unit": "steps/s", "cores": 1, "kind": "oracle",
             "tokens_per_s": tokens / dt, "seconds": round(dt, 3),
-            "sample": f"{queries} query batches of '{w.name}' (batch {w.batch}), decoded in order by the "
+            "sample": f"{done} query batches of '{w.name}' (batch {w.batch}), decoded in order by the "
                       f"fp64 oracle ({head} head), single process"}
+
+
+def _oracle_worker(name, shm_name, emb_shape, seconds, worker, n_workers, n_batches, head, ready, start, results):
+    from multiprocessing import shared_memory
+    shm = shared_memory.SharedMemory(name=shm_name)
+    try:
+        w = I.WORKLOADS[name]()
+        emb = np.ndarray(emb_shape, dtype=np.uint16, buffer=shm.buf)
+        mine = [q for q in range(n_batches) if q % n_workers == worker] or [worker % n_batches]
+        hid = {q: w.hidden_states(q * w.batch, w.batch) for q in mine}
+        ready.put(worker)
+        start.wait()
+        steps, tokens, done, dt = _oracle_batches(w, seconds, mine, lambda q: emb if q == "emb" else hid[q], head)
+        results.put((worker, steps, tokens, done, dt))
+    finally:
+        del emb
+        shm.close()
+
+
+def oracle_pool_baseline(w, seconds: float, procs: int = 0, head: str = "sparse"):
+    """The oracle as it stands on every host core: one spawned process per core,
+    each decoding its own share of the query batches for about `seconds` (all
+    released together); the rate is the sum of the processes' rates."""
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    procs = procs or os.cpu_count() or 1
+    emb = w.embedding()
+    n_batches = max(1, min(w.n_queries // w.batch, max(procs, 256 // w.batch)))
+    shm = shared_memory.SharedMemory(create=True, size=emb.nbytes)
+    try:
+        np.ndarray(emb.shape, dtype=np.uint16, buffer=shm.buf)[...] = emb
+        ctx = mp.get_context("spawn")
+        ready, results, start = ctx.Queue(), ctx.Queue(), ctx.Event()
+        ps = [ctx.Process(target=_oracle_worker, args=(w.name, shm.name, emb.shape, seconds, i, procs, n_batches,
+                                                       head, ready, start, results)) for i in range(procs)]
+        for p in ps:
+            p.start()
+        for _ in ps:
+            ready.get(timeout=600)
+        start.set()
+        res = [results.get(timeout=600 + 4 * seconds) for _ in ps]
+        for p in ps:
+            p.join(timeout=60)
+    finally:
+        shm.close()
+        shm.unlink()
+    rate = sum(r[1] / r[4] for r in res)
+    trate = sum(r[2] / r[4] for r in res)
+    done = sum(r[3] for r in res)
+    return {"value": rate, "unit": "steps/s", "cores": procs, "kind": "oracle", "tokens_per_s": trate,
+            "sample": f"{done} query batches of '{w.name}' (batch {w.batch}) decoded by the fp64 oracle "
+                      f"({head} head) in {procs} spawned processes (one per host core, "
+                      f"os.cpu_count()={os.cpu_count()}), about {seconds:g} s each"}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -236,7 +299,7 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": w.name, "batch": w.batch, "k": w.k, "vocab": w.vocab, "hidden": w.hidden,
-                       "catalog": len(w.catalog), "note": "CPU oracle (plain Python + numpy fp64)"},
+                       "catalog": len(w.catalog), "note": "CPU oracle (plain Python + numpy fp64), one process: one stream of decode steps, as the GPU arm"},
             "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
             "e2e": {"value": base["value"], "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -262,6 +325,8 @@ def run_ours(args):
     w = I.WORKLOADS[args.workload]()
     head = {"sparse": tcd.HEAD_SPARSE, "dense": tcd.HEAD_DENSE, "union": tcd.HEAD_UNION_GEMM,
             "dense_gemm": tcd.HEAD_DENSE_GEMM}[args.head]
+    if args.jump:
+        head |= tcd.FLAG_JUMP_FORWARD
     B, S, H = w.batch, w.max_steps, w.hidden
 
     emb_bits = w.embedding()
@@ -296,6 +361,20 @@ def run_ours(args):
         if ev is not None:
             ev[1].record(stream)
 
+    # Decode steps of each query batch, counted from an untimed decode of it
+    # (the decode is deterministic): the steps until its last sequence
+    # stopped, i.e. the head decisions of its longest-running sequence (forced
+    # tokens ride along in the same step), plus the step in which a failing
+    # sequence failed.  Idle launches after the last sequence stopped are not
+    # steps.  The timed region's own counters are checked against these below.
+    work = {}
+    for q in sorted(set(qids)):
+        decode_one(q)
+        n = lens.cpu().numpy()
+        lg = logits.cpu().numpy()
+        stt = status.cpu().numpy()
+        forced = np.array([int(np.isnan(lg[b, :n[b]]).sum()) for b in range(B)])
+        work[q] = (int((n - forced + (stt != 0)).max()), int(n.sum()), int((n - forced).sum()), int(forced.sum()))
     for i in range(W):
         decode_one(qids[i])
     torch.cuda.synchronize()
@@ -319,8 +398,11 @@ def run_ours(args):
     dev_ms = sum(a.elapsed_time(b) for a, b in evs)
     st = ctx.stats(reset=True)
     ctx.raise_on_error()
-    decode_steps = st["step_launches"]
-    tokens = st["seq_steps"]
+    timed = [work[q] for q in qids[W:W + K]]
+    decode_steps = sum(x[0] for x in timed)
+    tokens = sum(x[1] for x in timed)
+    # the timed decodes did exactly the counted work
+    counted_ok = (st["seq_steps"] == sum(x[2] for x in timed) and st["forced"] == sum(x[3] for x in timed))
     gpu_launches = st["step_launches"] + st["reset_launches"]
 
     dev_ms_max, all_steps, all_tokens = aggregate_ranks(dist, dev_ms, decode_steps, tokens, f"cuda:{dev}")
@@ -331,7 +413,7 @@ def run_ours(args):
     roof = None
     if not args.no_extras:
         roof, extras = extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids[W:], head, flush,
-                                    hid_buf, toks, logits, lens, status, tinfo["max_fanout"])
+                                    hid_buf, toks, logits, lens, status, tinfo["max_fanout"], work)
         e2e = extras.pop("e2e")
 
     if rank != 0:
@@ -350,8 +432,14 @@ def run_ours(args):
                                       else "kernel source changed since the last ncu capture")
     cpu = None
     if world == 1 and not args.no_extras:
-        cpu = oracle_baseline(w, args.cpu_seconds)
-        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        # One process decodes one stream of query batches, as this bench does on
+        # the GPU; the pool runs one such stream per host core (throughput of
+        # independent streams, like a larger batch).
+        one = oracle_baseline(w, args.cpu_seconds)
+        pool = oracle_pool_baseline(w, args.cpu_seconds)
+        cpu = {k: one[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu["tokens_per_s"] = one["tokens_per_s"]
+        cpu["all_cores_pool"] = {k: pool[k] for k in ("value", "unit", "cores", "tokens_per_s", "sample")}
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": dev_ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -359,8 +447,11 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": B, "k": w.k, "vocab": w.vocab, "hidden": H,
                    "catalog_strings": len(w.catalog), "trie_nodes": tinfo["n_nodes"], "trie_edges": tinfo["n_edges"],
                    "max_fanout": tinfo["max_fanout"], "residency": ["auto", "const", "global"][ctx.residency()],
-                   "head": args.head, "bench_step": "one tc_decode graph launch decoding one query batch to the end",
+                   "head": args.head, "jump_forward": bool(args.jump),
+                   "bench_step": "one tc_decode graph launch decoding one query batch to the end",
                    "decode_steps_per_bench_step": all_steps / (K * world),
+                   "step_launches_per_bench_step": st["step_launches"] / K,
+                   "timed_work_matches_count": counted_ok,
                    "tokens_per_s": all_tokens / (dev_ms_max / 1000.0),
                    "l2": "flushed between timed steps (512 MiB write outside the CUDA events)",
                    "wall_s_timed_region": round(t_wall, 3)},
@@ -382,12 +473,14 @@ def run_ours(args):
 
 
 def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, head, flush, hid_buf, toks, logits,
-                 lens, status, max_fanout):
-    """Roofline of the step kernel, dense-head comparison, host loop and end-to-end rate."""
+                 lens, status, max_fanout, work):
+    """Roofline of the step kernel, dense-head comparison, forced-continuation
+    variant, loop floor, host loop and end-to-end rate."""
     B, S, H = w.batch, w.max_steps, w.hidden
     out = {}
     n_roof = min(len(qids), 200 if B == 1 else 8)
-    gemm_head = head in (tcd.HEAD_UNION_GEMM, tcd.HEAD_DENSE_GEMM)
+    flags = head & tcd.FLAG_JUMP_FORWARD
+    head = head & ~tcd.FLAG_JUMP_FORWARD        # the per-launch and host-loop passes run plain steps
 
     # --- step kernel alone: tc_step (same kernel body, host-argument form), one
     # event pair per launch; L2 flushed before every launch (cold) or not (warm).
@@ -400,7 +493,7 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     for q in qids[:n_roof]:
         hid_buf.copy_(dev_hidden[q])
         ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head)
-        n_steps[q] = int(lens.max().item())
+        n_steps[q] = int((lens + (status != 0).int()).max().item())
 
     def kernel_pass(cold: bool):
         pairs = []
@@ -410,6 +503,8 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
             for t in range(n_steps[q]):
                 if cold:
                     flush.zero_()
+                else:
+                    torch.cuda._sleep(40000)   # keeps the GPU busy while the host enqueues the step
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 ctx.step(hid_buf[t], tok, lg, stt, head=head)
@@ -475,7 +570,44 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     st = ctx.stats(reset=True)
-    out["host_loop_steps_per_s_wall"] = st["step_launches"] / dt
+    out["host_loop_steps_per_s_wall"] = st["step_launches"] / dt   # the host loop launches no idle steps
+
+    # --- forced continuations (TC_FLAG_JUMP_FORWARD) against plain steps, same queries
+    if head in (tcd.HEAD_SPARSE, tcd.HEAD_DENSE):
+        n_j = min(len(qids), 500 if B == 1 else 16)
+        rates = {}
+        for name, fl in (("plain", 0), ("jump_forward", tcd.FLAG_JUMP_FORWARD)):
+            steps = toks_n = 0
+            for q in sorted(set(qids[:n_j])):      # untimed: the exact step counts of each variant
+                hid_buf.copy_(dev_hidden[q])
+                ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head | fl)
+            evs = []
+            ctx.stats(reset=True)
+            for q in qids[:n_j]:
+                hid_buf.copy_(dev_hidden[q])
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head | fl)
+                e1.record(stream)
+                evs.append((e0, e1))
+                n = lens.cpu().numpy()
+                lg = logits.cpu().numpy()
+                forced = np.array([int(np.isnan(lg[b, :n[b]]).sum()) for b in range(B)])
+                steps += int((n - forced).max())
+                toks_n += int(n.sum())
+            torch.cuda.synchronize()
+            ms = sum(x.elapsed_time(y) for x, y in evs)
+            st = ctx.stats(reset=True)
+            rates[name] = {"steps_per_s": steps / (ms / 1000.0), "tokens_per_s": toks_n / (ms / 1000.0),
+                           "forced_tokens": st["forced"], "head_decisions": st["seq_steps"]}
+        out["forced_continuations"] = dict(rates, note=f"{n_j} query batches, L2 flushed before each decode; "
+                                                        "a jump-forward step is one head decision plus the "
+                                                        "forced span after it")
+
+    # --- loop floor: the same graph loop with do-nothing kernels in the steps' place
+    fl_ms, fl_n = tcd.loop_floor(dev, B, 256)
+    out["loop_floor_us_per_launch"] = fl_ms * 1000.0 / fl_n
 
     # --- end to end through the C ABI with host buffers
     n_e2e = min(len(qids), 500 if B == 1 else 8)
@@ -491,7 +623,7 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     a.record(stream)
     for q in qids[:n_e2e]:
         hid_buf.copy_(pin_h[q], non_blocking=True)
-        ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head)
+        ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head | flags)
         pt.copy_(toks, non_blocking=True)
         pl.copy_(logits, non_blocking=True)
         pn.copy_(lens, non_blocking=True)
@@ -499,10 +631,11 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    st = ctx.stats(reset=True)
+    ctx.stats(reset=True)
     h2d = S * B * H * 2
     d2h = B * S * 8 + B * 8
-    out["e2e"] = {"value": st["step_launches"] / (ms / 1000.0), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+    e2e_steps = sum(work[q][0] for q in qids[:n_e2e])
+    out["e2e"] = {"value": e2e_steps / (ms / 1000.0), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                   "d2h_bytes_per_step": d2h,
                   "note": "per bench step: pinned H2D of the query's hidden states, tc_decode, D2H of "
                           "tokens/logits/lengths/status; CUDA events around the whole sequence, L2 not flushed"}

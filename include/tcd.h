@@ -77,6 +77,22 @@ enum {
                              legal mask and argmax (the dense comparison for TC_HEAD_UNION_GEMM) */
 };
 
+/*
+ * Flag or-ed into the `head` argument of tc_decode and tc_decode_graph_create:
+ * forced continuations ("Understanding Inference for Systems Engineers",
+ * section 7.5, forced spans).  After each head decision, while the grammar
+ * admits exactly one token at a sequence's node, that token is emitted in the
+ * same step without reading the head, and its logit slot is set to NaN; the
+ * walk advances through it (pointer completions included).  Emitted tokens
+ * are those of the decode without the flag; a sequence's first token always
+ * comes from the head, and a forced position's hidden state is not read.  One
+ * decode step then covers a decision and the forced span after it, so fewer
+ * steps run.  Sparse and dense heads only (the GEMM heads read all sequences'
+ * hidden states of one step as one tile, which needs them in lockstep):
+ * TC_ERR_UNSUPPORTED otherwise, and from tc_step and tc_decode_host.
+ */
+#define TC_FLAG_JUMP_FORWARD 0x100
+
 /* Bytes of __constant__ memory reserved for one walk image. */
 #define TC_CONST_CAPACITY_BYTES (63 * 1024)
 
@@ -277,11 +293,14 @@ tc_status tc_read_seq_state(tc_ctx* ctx, void* stream, int32_t* node, int32_t* e
 
 /*
  * tc_read_stats - synchronise `stream` and copy the context's cumulative
- * kernel counters into out (host) int64[4]: step-kernel launches, sequence
- * steps (one per live sequence per step), legal candidates evaluated (rows
- * gathered by the sparse head), reset-kernel launches.  reset != 0 zeroes
- * them afterwards.  Used to count launches and algorithmic bytes.
+ * kernel counters into out (host) int64[TC_STAT_SLOTS]: step-kernel launches
+ * (idle launches at the end of a graph loop included), head decisions (one
+ * per live sequence per step), legal candidates evaluated (rows gathered by
+ * the sparse head), reset-kernel launches, and tokens emitted as forced
+ * continuations (TC_FLAG_JUMP_FORWARD).  reset != 0 zeroes them afterwards.
+ * Used to count launches and algorithmic bytes.
  */
+#define TC_STAT_SLOTS 5
 tc_status tc_read_stats(tc_ctx* ctx, void* stream, int64_t* out, int32_t reset);
 
 /*
@@ -327,6 +346,21 @@ tc_status tc_dense_argmax_noalloc(const void* emb_bf16, int32_t vocab, int32_t h
                                   const void* hidden_bf16, int32_t batch, const int32_t* legal,
                                   int32_t legal_stride, const int32_t* n_legal, int32_t* tok_out,
                                   float* logit_out, void* stream);
+
+/*
+ * tc_loop_floor - the launch floor of tc_decode's loop ("Constraint made
+ * cheaper than no constraint": a do-nothing kernel launched in the sampler's
+ * place separates the cost of adding a kernel from the cost of its work).
+ * Builds the decode graph's shape - an arming kernel, then a conditional WHILE
+ * node whose body chains the step's launches, one CTA of 256 threads per
+ * sequence (grid 1 x batch), with programmatic dependent launch - with
+ * do-nothing kernels in the steps' place, runs `iterations` body iterations
+ * once untimed and once timed (CUDA events on `stream`), and returns the timed
+ * launch's milliseconds in *ms_out and its kernel launches in *launches_out.
+ * Synchronous; allocates and frees its own 4-byte counter and stream.
+ */
+tc_status tc_loop_floor(int32_t device, int32_t batch, int32_t iterations, void* stream, float* ms_out,
+                        int64_t* launches_out);
 
 /* tc_status_str - a static name for a status code. */
 const char* tc_status_str(tc_status status);

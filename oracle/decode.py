@@ -12,7 +12,9 @@ Sources:
   the host-side replay re-walks emitted tokens through the trie.
 * "Understanding Inference for Systems Engineers", section 8.2 (teacher
   forcing: compare at every position while following the engine's own path,
-  and judge a differing argmax by the oracle's own top-2 margin).
+  and judge a differing argmax by the oracle's own top-2 margin); section 7.5
+  (forced spans: where the grammar admits exactly one continuation the
+  model's scores are irrelevant, so that token is taken without a head read).
 
 Status strings: "ok" (the stop token was emitted), "empty_mask" (no legal
 token at some step) and "max_steps" (the step budget ran out first).
@@ -38,11 +40,15 @@ FLOOR_SCALE = 2.0 ** -10
 
 
 def greedy_decode(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: np.ndarray,
-                  max_steps: int, head: str = "sparse") -> Tuple[List[int], List[float], str]:
+                  max_steps: int, head: str = "sparse",
+                  jump: bool = False) -> Tuple[List[int], List[float], str]:
     """Decode one sequence.  ``hidden_bits[t]`` is the bf16 hidden state of step t.
 
     ``head="dense"`` uses every vocabulary logit with the mask applied after
-    (the post-logit pipeline); ``"sparse"`` computes only the legal rows."""
+    (the post-logit pipeline); ``"sparse"`` computes only the legal rows.
+    ``jump=True`` takes forced tokens without the head: from the second
+    position on, a position whose legal set holds one token emits it with a
+    NaN logit and computes nothing (the first token always comes from the head)."""
     st = WalkState()
     toks: List[int] = []
     logits: List[float] = []
@@ -50,6 +56,13 @@ def greedy_decode(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
         legal = legal_tokens(trie, st, k)
         if not legal:
             return toks, logits, "empty_mask"
+        if jump and t > 0 and len(legal) == 1:
+            toks.append(legal[0])
+            logits.append(float("nan"))
+            st = advance(trie, st, legal[0], k)
+            if st.done:
+                return toks, logits, "ok"
+            continue
         if head == "dense":
             tok, lg = dense_masked_argmax(emb_bits, hidden_bits[t], legal)
         else:
@@ -60,6 +73,18 @@ def greedy_decode(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
         if st.done:
             return toks, logits, "ok"
     return toks, logits, "max_steps"
+
+
+def forced_positions(trie: PrefixTrie, tokens: Sequence[int], k: int) -> List[int]:
+    """Positions t >= 1 of a walkable output whose legal set holds exactly one
+    token (where a forced-span decode emits without the head)."""
+    st = WalkState()
+    out = []
+    for t, tok in enumerate(tokens):
+        if t > 0 and len(legal_tokens(trie, st, k)) == 1:
+            out.append(t)
+        st = advance(trie, st, int(tok), k)
+    return out
 
 
 def replay_ok(trie: PrefixTrie, tokens: Sequence[int], k: int) -> bool:
@@ -96,7 +121,7 @@ class ForcingReport:
 
 def teacher_force(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: np.ndarray,
                   toks: Sequence[int], logits: Sequence[float], status: str, max_steps: int,
-                  exact: bool = False) -> ForcingReport:
+                  exact: bool = False, jump: bool = False) -> ForcingReport:
     """Check an engine's emitted tokens/logits/status for one sequence.
 
     The oracle follows the engine's tokens.  At each step the token must be
@@ -104,7 +129,9 @@ def teacher_force(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
     equal the exact dot product bit for bit (integer-valued inputs, where the
     fp32 sum is exact); otherwise the logit must be within ``REL_TOL`` and a
     differing token is excused only by an oracle top-2 margin under
-    ``MARGIN_TOL``."""
+    ``MARGIN_TOL``.  With ``jump`` a position t >= 1 whose legal set holds one
+    token must carry a NaN logit (forced, no head read) and every other
+    position a real one."""
     rep = ForcingReport()
     st = WalkState()
     for t, (g_tok, g_log) in enumerate(zip(toks, logits)):
@@ -113,6 +140,17 @@ def teacher_force(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
         if g_tok not in legal:
             rep.fail(f"step {t}: token {g_tok} not legal (legal={legal[:8]}...)")
             return rep
+        if jump:
+            forced = t > 0 and len(legal) == 1
+            if forced != bool(np.isnan(g_log)):
+                rep.fail(f"step {t}: forced={forced} but logit {float(g_log)!r}")
+                return rep
+            if forced:
+                st = advance(trie, st, int(g_tok), k)
+                if st.done and t != len(toks) - 1:
+                    rep.fail(f"step {t}: tokens continue after stop")
+                    return rep
+                continue
         lg = candidate_logits(emb_bits, hidden_bits[t], legal)
         best_tok, best_l = argmax_lower_id(legal, lg)
         gi = legal.index(int(g_tok))

@@ -85,7 +85,7 @@ class DecodeBuffers:
 
 
 def check_against_oracle(name: str, hid_bits: np.ndarray, out, k: int, max_steps: int, exact: bool,
-                         seqs=None):
+                         seqs=None, jump: bool = False):
     """Teacher-force every sequence (or the listed ones); return the reports."""
     w = workload(name)
     trie = oracle_trie(name)
@@ -97,7 +97,7 @@ def check_against_oracle(name: str, hid_bits: np.ndarray, out, k: int, max_steps
         assert np.all(toks[b, n:] == -1), f"seq {b}: tokens after the end"
         st = STATUS_TO_ORACLE.get(int(status[b]), f"code{int(status[b])}")
         rep = D.teacher_force(trie, k, emb_bits, hid_bits[:, b], list(map(int, toks[b, :n])),
-                              list(map(float, logits[b, :n])), st, max_steps, exact=exact)
+                              list(map(float, logits[b, :n])), st, max_steps, exact=exact, jump=jump)
         assert rep.ok, f"seq {b}: {rep.problems[:3]}"
         reports.append(rep)
     return reports

@@ -28,6 +28,8 @@ TC_OK = 0
 STATUS_NAMES = {}
 RES_AUTO, RES_CONST, RES_GLOBAL = 0, 1, 2
 HEAD_SPARSE, HEAD_DENSE, HEAD_UNION_GEMM, HEAD_DENSE_GEMM = 0, 1, 2, 3
+FLAG_JUMP_FORWARD = 0x100      # or-ed into `head` of decode / decode_graph: forced tokens skip the head
+STAT_SLOTS = 5
 TC_ERR_EMPTY_MASK, TC_ERR_NO_LIVE_EDGE, TC_ERR_MAX_STEPS, TC_ERR_BOUNDS = 16, 17, 18, 19
 CONST_CAPACITY_BYTES = 63 * 1024
 
@@ -73,6 +75,8 @@ _graph_destroy = _decl("tc_graph_destroy", None, [_vp])
 _first_error = _decl("tc_first_error", ctypes.c_int, [_vp, _vp, _i32p, _i32p])
 _read_state = _decl("tc_read_seq_state", ctypes.c_int, [_vp, _vp] + [_i32p] * 5)
 _read_stats = _decl("tc_read_stats", ctypes.c_int, [_vp, _vp, _i64p, ctypes.c_int32])
+_loop_floor = _decl("tc_loop_floor", ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
+                                                    ctypes.POINTER(ctypes.c_float), _i64p])
 _status_str = _decl("tc_status_str", ctypes.c_char_p, [ctypes.c_int])
 _last_msg = _decl("tc_last_error_message", ctypes.c_char_p, [])
 
@@ -237,10 +241,10 @@ class Context:
         return out
 
     def stats(self, reset: bool = False, stream=None) -> dict:
-        out = np.zeros(4, dtype=np.int64)
+        out = np.zeros(STAT_SLOTS, dtype=np.int64)
         _check(_read_stats(self._h, _stream_ptr(stream), out.ctypes.data_as(_i64p), int(reset)), "tc_read_stats")
         return {"step_launches": int(out[0]), "seq_steps": int(out[1]), "cand_rows": int(out[2]),
-                "reset_launches": int(out[3])}
+                "reset_launches": int(out[3]), "forced": int(out[4])}
 
     def close(self):
         for g in self._graphs:
@@ -255,3 +259,13 @@ class Context:
             self.close()
         except Exception:
             pass
+
+
+def loop_floor(device: int, batch: int, iterations: int, stream=None):
+    """Milliseconds and kernel launches of the decode loop's graph shape with
+    do-nothing kernels in the steps' place (tc_loop_floor)."""
+    ms = ctypes.c_float()
+    n = ctypes.c_int64()
+    _check(_loop_floor(device, batch, iterations, _stream_ptr(stream), ctypes.byref(ms), ctypes.byref(n)),
+           "tc_loop_floor")
+    return float(ms.value), int(n.value)

@@ -11,6 +11,11 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxTiles = 1024;        // upper bound of CTAs per sequence (partials per sequence)
 constexpr int kMaxHidden = 16384;
 constexpr int kMaxCandCap = 4096;
+// Decode steps per iteration of the graph's WHILE body.  Each iteration of a
+// conditional node costs a few microseconds of its own; running several step
+// kernels per iteration amortises it, at the price of up to kLoopUnroll - 1
+// idle step launches after the last sequence stops.
+constexpr int kLoopUnroll = 8;
 // Dynamic shared memory a step kernel may request: x staged for the generic
 // hidden size, two int32 candidate lists of up to kMaxCandCap entries, and
 // (dense head) 128 KiB of row stages.
@@ -105,10 +110,18 @@ struct StepParams {
   unsigned long long* stats;  // optional counters, see StatSlot
   HeadScratch hs;           // GEMM heads only
   int4* pre;                // [B, 32] precomputed candidate lists (one-CTA sparse step), or null
+  int32_t jump;             // 1: emit forced tokens without the head after each decision (device form only)
 };
 
 // Cumulative counters kept by the kernels (one atomic per launch / per sequence step).
-enum StatSlot { kStatStepLaunches = 0, kStatSeqSteps = 1, kStatCandRows = 2, kStatResetLaunches = 3, kStatSlots = 4 };
+enum StatSlot {
+  kStatStepLaunches = 0,   // step-kernel launches (idle ones included)
+  kStatSeqSteps = 1,       // head decisions: one per live sequence per step
+  kStatCandRows = 2,       // legal candidates the head evaluated
+  kStatResetLaunches = 3,
+  kStatForced = 4,         // tokens emitted as forced continuations (no head read)
+  kStatSlots = 5
+};
 
 struct ResetParams {
   GrammarView g;

@@ -36,11 +36,6 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kGraphCacheSize = 16;
-// Decode steps per iteration of the graph's WHILE body.  Each iteration of a
-// conditional node costs a few microseconds of its own; running several step
-// kernels per iteration amortises it, at the price of up to kLoopUnroll - 1
-// idle step launches after the last sequence stops.
-constexpr int kLoopUnroll = 8;
 
 std::mutex g_const_mu;
 const void* g_const_owner[kMaxDevices];  // grammar whose image the constant bank holds
@@ -313,6 +308,13 @@ tc_status check_decode_args(tc_ctx* c, const void* hidden, int32_t n_steps, int3
   if (batch < 1 || batch > c->max_batch) return TC_ERR_CAPACITY;
   if (k < 1 || k > c->bound->n_strings) return TC_ERR_K_RANGE;
   if (max_steps < 1 || max_steps > n_steps) return TC_ERR_INVALID_ARG;
+  if (head & TC_FLAG_JUMP_FORWARD) {
+    head &= ~TC_FLAG_JUMP_FORWARD;
+    if (head != TC_HEAD_SPARSE && head != TC_HEAD_DENSE) {
+      set_error_message("TC_FLAG_JUMP_FORWARD: sparse and dense heads only");
+      return is_gemm_head(head) ? TC_ERR_UNSUPPORTED : TC_ERR_INVALID_ARG;
+    }
+  }
   return check_head(c, head, batch);
 }
 
@@ -397,11 +399,13 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
   p.max_steps = key.max_steps;
   p.cond = (unsigned long long)cond;
   p.device_form = 1;
+  p.jump = (key.head & TC_FLAG_JUMP_FORWARD) ? 1 : 0;
+  const int head = key.head & ~TC_FLAG_JUMP_FORWARD;
   // The body runs kLoopUnroll steps; only the last sets the loop condition.
   // A sequence that has stopped makes the remaining steps of the body no-ops.
   for (int u = 0; u < kLoopUnroll; ++u) {
     p.loop_ctrl = (u == kLoopUnroll - 1);
-    if ((e = launch_any_step(c, g, p, key.head, cs, /*pdl=*/u > 0)) != cudaSuccess)
+    if ((e = launch_any_step(c, g, p, head, cs, /*pdl=*/u > 0)) != cudaSuccess)
       return fail(e, "step kernel capture");
   }
   cudaGraph_t body_ended = nullptr;
@@ -684,6 +688,11 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
                                     int32_t* status, void* stream) {
   tc_status rc = check_decode_args(c, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status);
   if (rc != TC_OK) return rc;
+  if (head & TC_FLAG_JUMP_FORWARD) {
+    // Host-form steps read every sequence's hidden state of one step: lockstep only.
+    set_error_message("tc_decode_host: TC_FLAG_JUMP_FORWARD needs the device-resident decode (tc_decode)");
+    return TC_ERR_UNSUPPORTED;
+  }
   DeviceGuard dg(c->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   DevGrammar* g = c->bound;
@@ -763,6 +772,7 @@ extern "C" tc_status tc_read_stats(tc_ctx* c, void* stream, int64_t* out, int32_
   if (!c || !out) return TC_ERR_INVALID_ARG;
   DeviceGuard dg(c->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  static_assert(kStatSlots == TC_STAT_SLOTS, "counter slots of the C ABI");
   unsigned long long h[kStatSlots];
   TC_CUDA(cudaMemcpyAsync(h, c->d_stats, sizeof(h), cudaMemcpyDeviceToHost, s));
   TC_CUDA(cudaStreamSynchronize(s));

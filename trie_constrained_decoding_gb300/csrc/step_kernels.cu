@@ -283,6 +283,140 @@ __device__ void filter_node(const StepParams& p, const WalkRd<kConst>& w, const 
   __syncthreads();
 }
 
+// ---------------------------------------------------------------- legal sets of one node, one warp
+
+constexpr int kPreMax = 32;  // largest legal set kept as a precomputed candidate list
+
+// Legal candidates of node `node` into out[] (one warp, node fan-out <= 32).
+// Returns the count, or -1 when an index is out of range or the fan-out is larger.
+template <bool kConst>
+__device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
+                                              int b, int beg, int end, int pid, int lane, int4* out) {
+  if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > kPreMax) return -1;
+  int bad = pid >= p.g.n_strings;
+  const uint32_t word = (pid >= 0 && pid < p.g.n_strings) ? p.spent[(size_t)b * p.kw + (pid >> 5)] : 1u;
+  const bool ctl_ok = pid >= 0 && !bad && ((word >> (pid & 31)) & 1u) == 0;
+  const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
+  const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
+  const int e = beg + lane;
+  int2 ed = make_int2(0, 0);
+  int32_t c = 0;
+  bool legal = false;
+  if (e < end) {
+    ed = w.edge(e);
+    c = p.cnt[(size_t)b * p.g.n_edges + e];
+    if (ed.x < 0 || ed.x >= p.V) bad = 1;
+    else if (ed.y >= 0) { if (ed.y >= p.g.n_nodes) bad = 1; else legal = c > 0; }
+    else if (ed.y == -1) legal = sep_ok;
+    else if (ed.y == -2) legal = stop_ok;
+    else bad = 1;
+  }
+  const unsigned bal = __ballot_sync(kFull, legal);
+  if (legal) out[__popc(bal & ((1u << lane) - 1u))] = make_int4(ed.x, e, ed.y, c);
+  if (__ballot_sync(kFull, bad)) return -1;
+  return __popc(bal);
+}
+
+// Size of the legal set of node [beg, end), capped at 2, and its first legal
+// candidate {token, edge, child, 0} (one warp, any fan-out).  -1 when an index
+// is out of range.
+template <bool kConst>
+__device__ __forceinline__ int warp_count_legal(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
+                                                int b, int beg, int end, int pid, int lane, int4& first) {
+  if (beg < 0 || end < beg || end > p.g.n_edges) return -1;
+  int bad = pid >= p.g.n_strings;
+  const uint32_t word = (pid >= 0 && pid < p.g.n_strings) ? p.spent[(size_t)b * p.kw + (pid >> 5)] : 1u;
+  const bool ctl_ok = pid >= 0 && !bad && ((word >> (pid & 31)) & 1u) == 0;
+  const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
+  const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
+  const int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
+  int count = 0;
+  for (int base = beg; base < end && count < 2; base += 32) {
+    const int e = base + lane;
+    int2 ed = make_int2(0, 0);
+    const bool legal = e < end && edge_legal<kConst>(p, w, cnt, e, sep_ok, stop_ok, ed, bad);
+    const unsigned bal = __ballot_sync(kFull, legal);
+    if (__ballot_sync(kFull, bad)) return -1;
+    if (bal != 0u && count == 0) {
+      const int src = __ffs(bal) - 1;
+      first = make_int4(__shfl_sync(kFull, ed.x, src), base + src, __shfl_sync(kFull, ed.y, src), 0);
+    }
+    count += __popc(bal);
+  }
+  return count < 2 ? count : 2;
+}
+
+// Forced continuations ("Understanding Inference for Systems Engineers",
+// section 7.5, forced spans): while the grammar admits exactly one token at
+// the sequence's node, that token is emitted without reading the head - its
+// logit slot holds NaN - and the walk advances, pointer completions included.
+// Run by one whole warp after the step's own transition; `ns` is the state
+// after that transition, the same in every lane on entry and on return.
+// With `list` (grammars whose nodes have at most kPreMax edges) the legal set
+// that ends the chain is left in list[0, list_n) with its node's pointer id in
+// list_pid (list_n = -1 when the chain ended for another reason); `known`
+// says that list[0] already holds the node's only legal candidate, whose
+// node has pointer id known_pid.
+template <bool kConst>
+__device__ void forced_chain(const StepParams& p, const WalkRd<kConst>& w, int b, SeqState& ns, int lane,
+                             int4* list, bool known, int known_pid, int& list_n, int& list_pid) {
+  list_n = -1;
+  list_pid = -2;
+  unsigned long long forced = 0;
+  while (!ns.done && ns.len < p.max_steps && ns.len < p.out_stride) {
+    int count, pid;
+    int4 only = make_int4(0, -1, 0, 0);
+    if (known) {
+      count = 1;
+      pid = known_pid;
+      only = list[0];
+      known = false;
+    } else {
+      const int n = ns.node;
+      if (n < 0 || n >= p.g.n_nodes) break;  // the next step reports the bad index
+      const int beg = w.begin(n), end = w.begin(n + 1);
+      pid = w.ptr(n);
+      if (list) {
+        count = warp_legal_set<kConst>(p, w, ns, b, beg, end, pid, lane, list);
+        __syncwarp();
+        if (count == 1) only = list[0];
+      } else {
+        count = warp_count_legal<kConst>(p, w, ns, b, beg, end, pid, lane, only);
+      }
+    }
+    if (count != 1) {
+      if (list) {
+        list_n = count;
+        list_pid = pid;
+      }
+      break;
+    }
+    if (lane == 0) {
+      p.tok_out[(size_t)b * p.out_stride + ns.len] = only.x;
+      p.logit_out[(size_t)b * p.out_stride + ns.len] = __int_as_float(0x7fc00000);
+    }
+    ns.len += 1;
+    ++forced;
+    if (only.z >= 0) {
+      ns.node = only.z;
+    } else {
+      // A control edge is legal only at a terminal whose pointer is unspent.
+      const int32_t q0 = __ldg(p.g.path_off + pid), q1 = __ldg(p.g.path_off + pid + 1);
+      int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
+      for (int32_t q = q0 + lane; q < q1; q += 32) {
+        const int32_t e = __ldg(p.g.path + q);
+        if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
+      }
+      if (lane == 0) p.spent[(size_t)b * p.kw + (pid >> 5)] |= 1u << (pid & 31);
+      ns.emitted += 1;
+      ns.node = 0;
+      if (only.z == -2) ns.done = 1;
+      __syncwarp();  // decrements and the spent flag are seen by the next legal set
+    }
+  }
+  if (forced && lane == 0 && p.stats) atomicAdd(&p.stats[kStatForced], forced);
+}
+
 // Apply the transition of sequence b with winner (best_l, best_t, best_e).
 // Called by every thread of the sequence's last CTA; thread 0 returns the
 // sequence's done flag afterwards.
@@ -328,8 +462,12 @@ __device__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, con
       if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
     }
   }
+  // Forced continuations follow a decision that leaves the sequence live.
+  const bool chain = p.jump && status == TC_OK && !stop;
+  if (chain) __syncthreads();  // the decrements above are seen by the chain's legal sets
   int done = 0;
-  if (tid == 0) {
+  if (tid < 32) {
+    const int lane = tid;
     SeqState ns = s;
     if (status != TC_OK) {
       ns.status = status;
@@ -339,28 +477,37 @@ __device__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, con
       ns.len = s.len + 1;
       if (ptr_done >= 0) {
         ns.emitted = s.emitted + 1;
-        p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
+        if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
       }
       if (stop) ns.done = 1;
     }
-    p.st[b] = ns;
-    if (p.stats) {
-      atomicAdd(&p.stats[kStatSeqSteps], 1ull);
-      atomicAdd(&p.stats[kStatCandRows], (unsigned long long)ncand);
-    }
-    if (p.device_form) {
-      if (status == TC_OK && s.len < p.out_stride) {
-        p.tok_out[(size_t)b * p.out_stride + s.len] = best_t;
-        p.logit_out[(size_t)b * p.out_stride + s.len] = best_l;
+    if (lane == 0) {
+      if (p.stats) {
+        atomicAdd(&p.stats[kStatSeqSteps], 1ull);
+        atomicAdd(&p.stats[kStatCandRows], (unsigned long long)ncand);
       }
-    } else {
-      p.tok_out[(size_t)b * p.out_stride] = status == TC_OK ? best_t : -1;
-      if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = status == TC_OK ? best_l : 0.f;
+      if (p.device_form) {
+        if (status == TC_OK && s.len < p.out_stride) {
+          p.tok_out[(size_t)b * p.out_stride + s.len] = best_t;
+          p.logit_out[(size_t)b * p.out_stride + s.len] = best_l;
+        }
+      } else {
+        p.tok_out[(size_t)b * p.out_stride] = status == TC_OK ? best_t : -1;
+        if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = status == TC_OK ? best_l : 0.f;
+      }
     }
-    if (p.status_out) p.status_out[b] = ns.status;
-    if (p.lens_out) p.lens_out[b] = ns.len;
-    if (ns.done) atomicSub(&p.ctrl->live, 1);
-    done = ns.done;
+    if (chain) {
+      __syncwarp();  // the spent flag set above
+      int ln, lp;
+      forced_chain<kConst>(p, w, b, ns, lane, nullptr, false, 0, ln, lp);
+    }
+    if (lane == 0) {
+      p.st[b] = ns;
+      if (p.status_out) p.status_out[b] = ns.status;
+      if (p.lens_out) p.lens_out[b] = ns.len;
+      if (ns.done) atomicSub(&p.ctrl->live, 1);
+      done = ns.done;
+    }
   }
   return done;
 }
@@ -545,8 +692,6 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
 // sequence state instead of filtering the node (the mask is computed ahead of
 // time, as "GLRMask" computes it in parallel with the forward pass).  After a
 // separator or a stop, or when a set does not fit, the next step filters.
-constexpr int kPreMax = 32;
-
 struct Step1Shared {
   int4 cand[kPreMax];                 // {token, edge, child, live count} of this step's candidates
   int4 spec[kPreMax][kPreMax];        // per candidate: its child's legal candidates
@@ -556,36 +701,6 @@ struct Step1Shared {
   int32_t wt[kWarps], wslot[kWarps];
   int32_t ncand, err, pid, done_after;
 };
-
-// Legal candidates of node `node` into out[] (one warp, node fan-out <= 32).
-// Returns the count, or -1 when an index is out of range or the fan-out is larger.
-template <bool kConst>
-__device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
-                                              int b, int beg, int end, int pid, int lane, int4* out) {
-  if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > kPreMax) return -1;
-  int bad = pid >= p.g.n_strings;
-  const uint32_t word = (pid >= 0 && pid < p.g.n_strings) ? p.spent[(size_t)b * p.kw + (pid >> 5)] : 1u;
-  const bool ctl_ok = pid >= 0 && !bad && ((word >> (pid & 31)) & 1u) == 0;
-  const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
-  const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
-  const int e = beg + lane;
-  int2 ed = make_int2(0, 0);
-  int32_t c = 0;
-  bool legal = false;
-  if (e < end) {
-    ed = w.edge(e);
-    c = p.cnt[(size_t)b * p.g.n_edges + e];
-    if (ed.x < 0 || ed.x >= p.V) bad = 1;
-    else if (ed.y >= 0) { if (ed.y >= p.g.n_nodes) bad = 1; else legal = c > 0; }
-    else if (ed.y == -1) legal = sep_ok;
-    else if (ed.y == -2) legal = stop_ok;
-    else bad = 1;
-  }
-  const unsigned bal = __ballot_sync(kFull, legal);
-  if (legal) out[__popc(bal & ((1u << lane) - 1u))] = make_int4(ed.x, e, ed.y, c);
-  if (__ballot_sync(kFull, bad)) return -1;
-  return __popc(bal);
-}
 
 template <bool kConst, int NCH>
 __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams p) {
@@ -719,7 +834,10 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
     }
     // The winner's child legal set becomes the next step's candidate list.
     const int next_n = (status == TC_OK && ptr_done < 0) ? sh.spec_n[bs] : -1;
-    if (next_n > 0)
+    // Forced continuations follow when that set is a single token, or after a
+    // separator (the root's set is not precomputed).
+    const bool chain = p.jump && status == TC_OK && !stop && (next_n == 1 || ptr_done >= 0);
+    if (!chain && next_n > 0)
       for (int i = tid; i < next_n; i += kThreads) p.pre[(size_t)b * kPreMax + i] = sh.spec[bs][i];
     if (ptr_done >= 0) {
       const int32_t q0 = __ldg(p.g.path_off + ptr_done), q1 = __ldg(p.g.path_off + ptr_done + 1);
@@ -729,41 +847,57 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
         if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
       }
     }
-    if (tid == 0) {
+    if (chain) __syncthreads();  // the decrements above are seen by the chain's legal sets
+    if (warp == 0) {
       SeqState ns = s;
+      int pre_n = next_n, pre_pid = next_n >= 0 ? sh.spec_pid[bs] : -2;
       if (status != TC_OK) {
         ns.status = status;
         ns.done = 1;
-        ns.pad0 = 0;
       } else {
         ns.node = new_node;
         ns.len = s.len + 1;
         if (ptr_done >= 0) {
           ns.emitted = s.emitted + 1;
-          p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
+          if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
         }
         if (stop) ns.done = 1;
-        ns.pad0 = next_n >= 0 ? next_n + 1 : 0;
-        ns.pad1 = next_n >= 0 ? sh.spec_pid[bs] : -2;
       }
-      p.st[b] = ns;
-      if (p.stats) {
-        atomicAdd(&p.stats[kStatSeqSteps], 1ull);
-        atomicAdd(&p.stats[kStatCandRows], (unsigned long long)ncand);
-      }
-      if (p.device_form) {
-        if (status == TC_OK && s.len < p.out_stride) {
-          p.tok_out[(size_t)b * p.out_stride + s.len] = bt;
-          p.logit_out[(size_t)b * p.out_stride + s.len] = bl;
+      if (lane == 0) {
+        if (p.stats) {
+          atomicAdd(&p.stats[kStatSeqSteps], 1ull);
+          atomicAdd(&p.stats[kStatCandRows], (unsigned long long)ncand);
         }
-      } else {
-        p.tok_out[(size_t)b * p.out_stride] = status == TC_OK ? bt : -1;
-        if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = status == TC_OK ? bl : 0.f;
+        if (p.device_form) {
+          if (status == TC_OK && s.len < p.out_stride) {
+            p.tok_out[(size_t)b * p.out_stride + s.len] = bt;
+            p.logit_out[(size_t)b * p.out_stride + s.len] = bl;
+          }
+        } else {
+          p.tok_out[(size_t)b * p.out_stride] = status == TC_OK ? bt : -1;
+          if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = status == TC_OK ? bl : 0.f;
+        }
       }
-      if (p.status_out) p.status_out[b] = ns.status;
-      if (p.lens_out) p.lens_out[b] = ns.len;
-      if (ns.done) atomicSub(&p.ctrl->live, 1);
-      sh.done_after = ns.done;
+      if (chain) {
+        __syncwarp();  // the spent flag set above
+        // The winner's own (precomputed) list slot serves as the chain's scratch.
+        int4* list = sh.spec[bs];
+        forced_chain<kConst>(p, w, b, ns, lane, list, next_n == 1, sh.spec_pid[bs], pre_n, pre_pid);
+        if (pre_n > 0 && lane < pre_n) p.pre[(size_t)b * kPreMax + lane] = list[lane];
+      }
+      if (ns.status == TC_OK) {
+        ns.pad0 = pre_n >= 0 ? pre_n + 1 : 0;
+        ns.pad1 = pre_n >= 0 ? pre_pid : -2;
+      } else {
+        ns.pad0 = 0;
+      }
+      if (lane == 0) {
+        p.st[b] = ns;
+        if (p.status_out) p.status_out[b] = ns.status;
+        if (p.lens_out) p.lens_out[b] = ns.len;
+        if (ns.done) atomicSub(&p.ctrl->live, 1);
+        sh.done_after = ns.done;
+      }
     }
   } else if (tid == 0) {
     if (mode == 2) {
