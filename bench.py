@@ -66,6 +66,8 @@ def parse_args():
                     help="grammar residency (default: the workload's)")
     ap.add_argument("--loop", choices=["graph", "host"], default="graph",
                     help="timed loop: the captured device-resident graph (default) or host-driven steps")
+    ap.add_argument("--live-counts", action="store_true",
+                    help="per-sequence live-count arrays instead of the read-only no-repeat state")
     ap.add_argument("--jump", action="store_true",
                     help="forced continuations: emit grammar-forced tokens without the head (sparse/dense heads)")
     return ap.parse_args()
@@ -336,7 +338,8 @@ def run_ours(args):
     tinfo = trie.info()
     ctx = tcd.Context(emb, max_batch=B, cand_cap=w.cand_cap)
     res = {"const": tcd.RES_CONST, "global": tcd.RES_GLOBAL, "auto": tcd.RES_AUTO}[args.residency or w.residency]
-    ctx.bind(trie, res)
+    ctx.bind(trie, res | (tcd.BIND_LIVE_COUNTS if args.live_counts else 0))
+    state_mode = "live counts" if (args.live_counts or w.k > 8) else "read-only (rank ranges + banned set)"
 
     n_batches = max(1, min(w.n_queries // B, 2048 // B))
     K, W = args.steps, args.warmup
@@ -447,7 +450,7 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": B, "k": w.k, "vocab": w.vocab, "hidden": H,
                    "catalog_strings": len(w.catalog), "trie_nodes": tinfo["n_nodes"], "trie_edges": tinfo["n_edges"],
                    "max_fanout": tinfo["max_fanout"], "residency": ["auto", "const", "global"][ctx.residency()],
-                   "head": args.head, "jump_forward": bool(args.jump),
+                   "head": args.head, "jump_forward": bool(args.jump), "no_repeat_state": state_mode,
                    "bench_step": "one tc_decode graph launch decoding one query batch to the end",
                    "decode_steps_per_bench_step": all_steps / (K * world),
                    "step_launches_per_bench_step": st["step_launches"] / K,

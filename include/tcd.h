@@ -67,6 +67,21 @@ enum {
   TC_RES_GLOBAL = 2   /* walk image in global memory, read through the read-only cache */
 };
 
+/*
+ * Flag or-ed into the `residency` argument of tc_bind_grammar: keep the
+ * per-sequence live-count arrays for every k.  Without it a decode or reset
+ * with k <= 8 pointers (and a catalog of at most 65535 strings) uses the
+ * read-only no-repeat state ("Constraint made cheaper than no constraint",
+ * section "The batched engine": a 16-byte per-sequence banned set against
+ * read-only per-edge pointer sets): the pointers below an edge are one range of
+ * depth-first ranks stored in the shared edge record, and each sequence keeps
+ * the ranks of its completed pointers (at most 8 x 16 bits) in its state, so no
+ * per-sequence array is filled at reset or updated on completion.  Both modes
+ * give identical results; larger k always uses the count arrays, which are
+ * allocated on first use.
+ */
+#define TC_BIND_LIVE_COUNTS 0x10
+
 /* Output head (tc_step / tc_decode). */
 enum {
   TC_HEAD_SPARSE = 0,     /* one embedding-row dot product per legal candidate */
@@ -156,6 +171,21 @@ tc_status tc_trie_info(const tc_trie* trie, tc_trie_info_t* out);
 tc_status tc_trie_export(const tc_trie* trie, int32_t* node_begin, int32_t* edge_tok,
                          int32_t* edge_child, int32_t* node_ptr, int32_t* static_cnt,
                          int32_t* path_off, int32_t* path);
+
+/*
+ * tc_trie_export_ranks - the depth-first pointer numbering behind the
+ * read-only no-repeat state ("Constraint made cheaper than no constraint",
+ * section "The batched engine": batched sequences share one read-only trie and
+ * keep only their own small no-repeat state).  Pointers are ranked in
+ * depth-first order (a node's own pointer before those below it, children in
+ * token order), so the pointers below any node hold one contiguous range of
+ * ranks.  Host buffers, either may be NULL:
+ *  ptr_rank  int32[K]  rank of pointer id p
+ *  edge_lo   int32[E]  first rank below a token edge's child (the range has
+ *                      static_cnt[e] ranks); the terminal's own rank for a
+ *                      control edge
+ */
+tc_status tc_trie_export_ranks(const tc_trie* trie, int32_t* ptr_rank, int32_t* edge_lo);
 
 void tc_trie_free(tc_trie* trie);
 

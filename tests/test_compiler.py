@@ -131,8 +131,54 @@ def test_walk_image_size(tcd):
     w = I.tiny()
     info = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab).info()
     N, E = info["n_nodes"], info["n_edges"]
-    assert info["walk_image_bytes"] == 4 * (((N + 2) & ~1) + 2 * E + N)
+    assert info["walk_image_bytes"] == 4 * (((N + 1 + 3) & ~3) + 4 * E + N)
     assert info["walk_image_bytes"] <= tcd.CONST_CAPACITY_BYTES
     b = I.batched()
     info = tcd.Trie.compile(b.catalog, b.sep_id, b.stop_id, b.vocab).info()
     assert info["walk_image_bytes"] > tcd.CONST_CAPACITY_BYTES      # the 1000-tool catalog lives in global memory
+
+
+def _rank_catalogs():
+    out = [(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout) for w in (I.tiny(), I.batched(), I.unstructured())]
+    for cat, sep, stop, V in I.brute_catalogs():
+        out.append((cat, sep, stop, V, 256))
+    for seed in range(6):
+        cat = I.random_small_catalog(I.rng_for(40, extra=seed))
+        out.append((cat, 10, 11, 12, 256))
+    return out
+
+
+def test_depth_first_ranks_give_each_subtree_one_range(tcd):
+    """The read-only no-repeat state ("Constraint made cheaper than no
+    constraint", section "The batched engine") needs the pointers below every
+    edge as one range of ranks.  Checked against the oracle's own trie: the
+    pointer ids whose rank lies in [edge_lo, edge_lo + static_cnt) are exactly
+    the pointers at or below the edge's child, and a control edge's lo is the
+    rank of the terminal's own pointer."""
+    for cat, sep, stop, V, fan in _rank_catalogs():
+        t = tcd.Trie.compile(cat, sep, stop, V, fan)
+        ex, rk = t.export(), t.ranks()
+        K = len(cat)
+        assert sorted(rk["ptr_rank"].tolist()) == list(range(K))
+        by_rank = np.empty(K, dtype=np.int64)
+        by_rank[rk["ptr_rank"]] = np.arange(K)
+        ot = G.compile_catalog(cat, sep, stop, V, max_fanout=fan)
+        # prefix of every node: walk the CSR from the root
+        prefix = {0: ()}
+        order = [0]
+        for n in order:
+            for e in range(ex["node_begin"][n], ex["node_begin"][n + 1]):
+                c = int(ex["edge_child"][e])
+                if c >= 0:
+                    prefix[c] = prefix[n] + (int(ex["edge_tok"][e]),)
+                    order.append(c)
+        for n in order:
+            for e in range(ex["node_begin"][n], ex["node_begin"][n + 1]):
+                c, lo = int(ex["edge_child"][e]), int(rk["edge_lo"][e])
+                if c >= 0:
+                    got = {int(by_rank[r]) for r in range(lo, lo + int(ex["static_cnt"][e]))}
+                    want = set(ot.below[prefix[c]])
+                    assert got == want
+                else:
+                    assert lo == rk["ptr_rank"][ex["node_ptr"][n]]
+        t.close()

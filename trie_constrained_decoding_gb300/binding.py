@@ -27,6 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 TC_OK = 0
 STATUS_NAMES = {}
 RES_AUTO, RES_CONST, RES_GLOBAL = 0, 1, 2
+BIND_LIVE_COUNTS = 0x10        # or-ed into bind's residency: per-sequence live-count arrays for every k
 HEAD_SPARSE, HEAD_DENSE, HEAD_UNION_GEMM, HEAD_DENSE_GEMM = 0, 1, 2, 3
 FLAG_JUMP_FORWARD = 0x100      # or-ed into `head` of decode / decode_graph: forced tokens skip the head
 STAT_SLOTS = 5
@@ -58,6 +59,7 @@ _compile = _decl("tc_compile_trie", ctypes.c_int, [_i32p, _i64p, ctypes.c_int32,
 _info = _decl("tc_trie_info", ctypes.c_int, [_vp, ctypes.POINTER(_TrieInfo)])
 _export = _decl("tc_trie_export", ctypes.c_int, [_vp] + [_i32p] * 7)
 _trie_free = _decl("tc_trie_free", None, [_vp])
+_export_ranks = _decl("tc_trie_export_ranks", ctypes.c_int, [_vp, _i32p, _i32p])
 _ctx_create = _decl("tc_ctx_create", ctypes.c_int, [ctypes.c_int32, _vp, ctypes.c_int32, ctypes.c_int32,
                                                    ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_vp)])
 _ctx_destroy = _decl("tc_ctx_destroy", None, [_vp])
@@ -143,6 +145,14 @@ class Trie:
         out = {k: np.zeros(n, dtype=np.int32) for k, n in arrs.items()}
         _check(_export(self._h, *[out[k].ctypes.data_as(_i32p) for k in arrs]), "tc_trie_export")
         out["path"] = out["path"][:T]
+        return out
+
+    def ranks(self) -> dict:
+        """Depth-first pointer ranks (tc_trie_export_ranks): ptr_rank[K], edge_lo[E]."""
+        i = self.info()
+        out = {"ptr_rank": np.zeros(i["n_strings"], dtype=np.int32), "edge_lo": np.zeros(i["n_edges"], np.int32)}
+        _check(_export_ranks(self._h, out["ptr_rank"].ctypes.data_as(_i32p), out["edge_lo"].ctypes.data_as(_i32p)),
+               "tc_trie_export_ranks")
         return out
 
     def close(self):

@@ -21,6 +21,11 @@ constexpr int kLoopUnroll = 8;
 // (dense head) 128 KiB of row stages.
 constexpr int kMaxDynamicSmem = kMaxHidden * 2 + 2 * kMaxCandCap * 4 + 128 + 128 * 1024;
 
+// Largest k of the read-only no-repeat state: the banned set is up to kBanMax
+// 16-bit pointer ranks, 16 bytes per sequence.
+constexpr int kBanMax = 8;
+constexpr int kBanMaxStrings = 65535;
+
 // Per-sequence decode state (device memory, one record per sequence).
 struct SeqState {
   int32_t node;     // current trie node
@@ -29,7 +34,10 @@ struct SeqState {
   int32_t status;   // TC_OK or the error that stopped the sequence
   int32_t done;     // 1 once the stop token was emitted or an error occurred
   int32_t k;        // pointers owed in total
-  int32_t pad0, pad1;
+  int32_t pad0, pad1;  // one-CTA sparse step: precomputed list size + 1 (0: none) and its node's pointer
+  // Read-only no-repeat mode: ranks of the completed pointers, two per word
+  // (scalar fields: an array member would keep the state out of registers).
+  uint32_t ban0, ban1, ban2, ban3;
 };
 
 // One CTA's best candidate, handed to the sequence's last CTA.
@@ -53,8 +61,8 @@ struct GrammarView {
   int32_t off_edges, off_ptr;
   int32_t n_nodes, n_edges, n_strings;
   const int32_t* static_cnt; // [E]
-  const int32_t* path_off;   // [K+1]
-  const int32_t* path;       // [total tokens]
+  const int32_t* path_off;   // [K+1] by pointer rank
+  const int32_t* path;       // [total tokens]: the token edges of each pointer, in rank order
 };
 
 struct GemmPartial;  // gemm_tc.h
@@ -90,8 +98,8 @@ struct StepParams {
   const uint16_t* hidden;   // bf16 [B, H] (host form) or [S, B, H] (device form: row len_b * B + b)
   int64_t hidden_rows;      // rows of `hidden` (B, or S * B)
   SeqState* st;             // [B]
-  int32_t* cnt;             // [B, E] live-pointer counts
-  uint32_t* spent;          // [B, kw] spent flags
+  int32_t* cnt;             // [B, E] live-pointer counts (count mode)
+  uint32_t* spent;          // [B, kw] spent flags by pointer rank (count mode)
   int32_t kw;               // words of spent flags per sequence
   int32_t B;
   int32_t cand_cap;         // C
@@ -111,6 +119,7 @@ struct StepParams {
   HeadScratch hs;           // GEMM heads only
   int4* pre;                // [B, 32] precomputed candidate lists (one-CTA sparse step), or null
   int32_t jump;             // 1: emit forced tokens without the head after each decision (device form only)
+  int32_t iv;               // 1: read-only no-repeat state (rank ranges + banned ranks); 0: cnt/spent arrays
 };
 
 // Cumulative counters kept by the kernels (one atomic per launch / per sequence step).
@@ -130,6 +139,7 @@ struct ResetParams {
   uint32_t* spent;
   int32_t kw;
   int32_t B, k, max_steps;
+  int32_t iv;               // 1: read-only no-repeat state (no count arrays to fill)
   uint32_t* seq_ticket;
   Ctrl* ctrl;
   int32_t* toks;            // optional [B, max_steps] prefill with -1

@@ -85,6 +85,9 @@ struct DevGrammar {
   int4* d_pre = nullptr;  // [max_batch, 32] next-step candidate lists
   int32_t kw = 1;
   int32_t batch = 0, k = 0;  // of the last reset (0: none)
+  bool force_counts = false;  // TC_BIND_LIVE_COUNTS: per-sequence count arrays for every k
+  int32_t iv = 0;             // state mode of the last reset (1: read-only no-repeat state)
+  size_t cnt_batch = 0;       // sequences the count arrays (allocated on first use) hold
 
   GrammarView view() const {
     GrammarView v;
@@ -266,11 +269,34 @@ StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
   p.stats = c->d_stats;
   p.max_steps = INT32_MAX;
   p.pre = one_cta_sparse(g) ? g->d_pre : nullptr;
+  p.iv = g->iv;
   return p;
+}
+
+// The read-only no-repeat state serves k <= kBanMax pointers (16-bit ranks);
+// larger k, or a grammar bound with TC_BIND_LIVE_COUNTS, uses count arrays.
+bool use_iv(const DevGrammar* g, int k) {
+  return !g->force_counts && k <= kBanMax && g->n_strings <= kBanMaxStrings;
+}
+
+// Count arrays of max_batch sequences, allocated the first time count mode runs.
+tc_status ensure_counts(const tc_ctx* c, DevGrammar* g) {
+  if (g->d_cnt) return TC_OK;
+  const size_t n = (size_t)c->max_batch * (size_t)std::max<int32_t>(1, g->n_edges);
+  cudaError_t e = cudaMalloc(&g->d_cnt, sizeof(int32_t) * n);
+  if (e != cudaSuccess) {
+    g->d_cnt = nullptr;
+    cudaGetLastError();
+    set_error_message("live-count arrays: " + std::string(cudaGetErrorString(e)));
+    return TC_ERR_OOM;
+  }
+  g->cnt_batch = (size_t)c->max_batch;
+  return TC_OK;
 }
 
 ResetParams reset_params(const tc_ctx* c, const DevGrammar* g, int B, int k, int max_steps) {
   ResetParams r{};
+  r.iv = use_iv(g, k) ? 1 : 0;
   r.g = g->view();
   r.st = g->d_st;
   r.cnt = g->d_cnt;
@@ -327,6 +353,10 @@ void destroy_graph(tc_graph* gr) {
 
 // Capture: [constant re-bind] -> reset -> WHILE(cond) { step }.
 tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** out) {
+  if (!use_iv(g, key.k)) {
+    tc_status rc0 = ensure_counts(c, g);  // no allocation during capture
+    if (rc0 != TC_OK) return rc0;
+  }
   auto* gr = new tc_graph();
   gr->ctx = c;
   gr->g = g;
@@ -400,6 +430,7 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
   p.cond = (unsigned long long)cond;
   p.device_form = 1;
   p.jump = (key.head & TC_FLAG_JUMP_FORWARD) ? 1 : 0;
+  p.iv = r.iv;
   const int head = key.head & ~TC_FLAG_JUMP_FORWARD;
   // The body runs kLoopUnroll steps; only the last sets the loop condition.
   // A sequence that has stopped makes the remaining steps of the body no-ops.
@@ -424,6 +455,7 @@ tc_status launch_graph(tc_graph* gr, cudaStream_t s) {
   }
   gr->g->batch = gr->key.batch;
   gr->g->k = gr->key.k;
+  gr->g->iv = use_iv(gr->g, gr->key.k) ? 1 : 0;
   return TC_OK;
 }
 
@@ -501,6 +533,8 @@ extern "C" void tc_ctx_destroy(tc_ctx* c) {
 
 extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t residency, void* stream) {
   if (!c || !t) return TC_ERR_INVALID_ARG;
+  const bool force_counts = (residency & TC_BIND_LIVE_COUNTS) != 0;
+  residency &= ~TC_BIND_LIVE_COUNTS;
   if (residency != TC_RES_AUTO && residency != TC_RES_CONST && residency != TC_RES_GLOBAL) return TC_ERR_INVALID_ARG;
   if (t->vocab > c->V) {
     set_error_message("tc_bind_grammar: the trie's vocabulary is larger than the context's");
@@ -524,7 +558,7 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
   DevGrammar* g = nullptr;
   for (DevGrammar* x : c->grammars)
     if (x->hash == t->content_hash && x->residency == res && x->n_nodes == t->n_nodes() &&
-        x->n_edges == t->n_edges())
+        x->n_edges == t->n_edges() && x->force_counts == force_counts)
       g = x;
   if (!g) {
     g = new DevGrammar();
@@ -537,14 +571,28 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
     g->max_depth = t->max_depth;
     g->layout = L;
     g->kw = (t->n_strings + 31) / 32;
+    g->force_counts = force_counts;
     const std::vector<int32_t> img = build_walk_image(*t, L);
+    // On the device a pointer is named by its depth-first rank: its edge path
+    // is stored at its rank.
+    std::vector<int32_t> path_off((size_t)t->n_strings + 1, 0), path;
+    {
+      std::vector<int32_t> by_rank((size_t)t->n_strings);
+      for (int32_t q = 0; q < t->n_strings; ++q) by_rank[(size_t)t->ptr_rank[q]] = q;
+      path.reserve(t->path.size());
+      for (int32_t r = 0; r < t->n_strings; ++r) {
+        const int32_t q = by_rank[(size_t)r];
+        path_off[(size_t)r] = (int32_t)path.size();
+        path.insert(path.end(), t->path.begin() + t->path_off[q], t->path.begin() + t->path_off[q + 1]);
+      }
+      path_off[(size_t)t->n_strings] = (int32_t)path.size();
+    }
     const size_t B = (size_t)c->max_batch;
     cudaError_t e = cudaMalloc(&g->d_img, img_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&g->d_static_cnt, sizeof(int32_t) * std::max<size_t>(1, t->static_cnt.size()));
     if (e == cudaSuccess) e = cudaMalloc(&g->d_path_off, sizeof(int32_t) * t->path_off.size());
     if (e == cudaSuccess) e = cudaMalloc(&g->d_path, sizeof(int32_t) * std::max<size_t>(1, t->path.size()));
     if (e == cudaSuccess) e = cudaMalloc(&g->d_st, sizeof(SeqState) * B);
-    if (e == cudaSuccess) e = cudaMalloc(&g->d_cnt, sizeof(int32_t) * B * std::max<int32_t>(1, g->n_edges));
     if (e == cudaSuccess) e = cudaMalloc(&g->d_spent, sizeof(uint32_t) * B * g->kw);
     if (e == cudaSuccess) e = cudaMalloc(&g->d_pre, sizeof(int4) * B * 32);
     if (e == cudaSuccess) e = cudaMemset(g->d_pre, 0, sizeof(int4) * B * 32);
@@ -552,9 +600,9 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
     if (e == cudaSuccess)
       e = cudaMemcpy(g->d_static_cnt, t->static_cnt.data(), sizeof(int32_t) * t->static_cnt.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
-      e = cudaMemcpy(g->d_path_off, t->path_off.data(), sizeof(int32_t) * t->path_off.size(), cudaMemcpyHostToDevice);
+      e = cudaMemcpy(g->d_path_off, path_off.data(), sizeof(int32_t) * path_off.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
-      e = cudaMemcpy(g->d_path, t->path.data(), sizeof(int32_t) * t->path.size(), cudaMemcpyHostToDevice);
+      e = cudaMemcpy(g->d_path, path.data(), sizeof(int32_t) * path.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(g->d_st, 0, sizeof(SeqState) * B);
     if (e != cudaSuccess) {
       g->release();
@@ -587,10 +635,17 @@ extern "C" tc_status tc_reset(tc_ctx* c, int32_t batch, int32_t k, void* stream)
   if (batch < 1 || batch > c->max_batch) return TC_ERR_CAPACITY;
   if (k < 1 || k > c->bound->n_strings) return TC_ERR_K_RANGE;
   DeviceGuard dg(c->device);
-  ResetParams r = reset_params(c, c->bound, batch, k, 0);
+  DevGrammar* g = c->bound;
+  if (!use_iv(g, k)) {
+    tc_status rc = ensure_counts(c, g);
+    if (rc != TC_OK) return rc;
+  }
+  ResetParams r = reset_params(c, g, batch, k, 0);
+  r.cnt = g->d_cnt;
   TC_CUDA(launch_reset(r, static_cast<cudaStream_t>(stream)));
-  c->bound->batch = batch;
-  c->bound->k = k;
+  g->batch = batch;
+  g->k = k;
+  g->iv = r.iv;
   return TC_OK;
 }
 
@@ -698,6 +753,10 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
   DevGrammar* g = c->bound;
   rc = ensure_const(c, g, s);
   if (rc != TC_OK) return rc;
+  if (!use_iv(g, k)) {
+    rc = ensure_counts(c, g);
+    if (rc != TC_OK) return rc;
+  }
   ResetParams r = reset_params(c, g, batch, k, max_steps);
   r.toks = toks;
   r.logits = logits;
@@ -706,6 +765,7 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
   TC_CUDA(launch_reset(r, s));
   g->batch = batch;
   g->k = k;
+  g->iv = r.iv;
   const size_t row = (size_t)batch * (size_t)c->H;
   for (int32_t t = 0; t < max_steps; ++t) {
     StepParams p = step_params(c, g, batch);

@@ -54,9 +54,14 @@ struct WalkRd {
     if constexpr (kConst) return c_walk[n];
     else return __ldg(img + n);
   }
-  __device__ __forceinline__ int2 edge(int32_t e) const {
-    if constexpr (kConst) return make_int2(c_walk[off_edges + 2 * e], c_walk[off_edges + 2 * e + 1]);
-    else return __ldg(reinterpret_cast<const int2*>(img + off_edges) + e);
+  // {token, child, first rank below, ranks below} (control edges: the terminal's own rank, 1).
+  // Lanes read different edges, which the constant cache would serialise, so
+  // edge records always come through the read-only data cache (one 16-byte
+  // load each; measured faster than four constant-bank words at B = 1); node
+  // ranges and pointer ids, read alike by a whole warp, come from the constant
+  // bank when the grammar is resident there.
+  __device__ __forceinline__ int4 edge(int32_t e) const {
+    return __ldg(reinterpret_cast<const int4*>(img + off_edges) + e);
   }
   __device__ __forceinline__ int32_t ptr(int32_t n) const {
     if constexpr (kConst) return c_walk[off_ptr + n];
@@ -95,6 +100,12 @@ __device__ __forceinline__ uint4 ld_row(const uint4* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
+}
+
+// Ask L2 to fetch `bytes` (a multiple of 16) at a 16-byte aligned address; no
+// completion to wait for, nothing lands in shared memory.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // x fragment of one lane: chunks 32*i + lane (8 bf16 each).
@@ -173,12 +184,67 @@ struct StepShared {
   int32_t bt, be, done_after;
 };
 
-// Legality of one edge of the current node (see the filter below).
+// The no-repeat state of one sequence as the legality tests read it.
+//
+// Count mode ("Masked sampling inside the sampler"): every edge carries the
+// number of live pointers below it, a per-sequence copy decremented along a
+// pointer's path when it completes, and each pointer a spent flag.
+// Read-only mode ("The batched engine": a small per-sequence banned set
+// against read-only per-edge pointer sets): pointers are numbered in
+// depth-first order, so the pointers below an edge are one rank range held in
+// the shared edge record; an edge is live while that range holds a rank not in
+// the sequence's banned set (the ranks of its completed pointers, at most
+// kBanMax, kept in its state).  Both give the same count of live pointers.
+struct SeqLive {
+  const int32_t* cnt;      // count mode: this sequence's counts; null in read-only mode
+  const uint32_t* spent;   // count mode: this sequence's spent flags
+  uint32_t ban[kBanMax / 2];
+  int32_t nban;
+};
+
+__device__ __forceinline__ SeqLive seq_live(const StepParams& p, const SeqState& s, int b) {
+  SeqLive L;
+  L.cnt = p.iv ? nullptr : p.cnt + (size_t)b * p.g.n_edges;
+  L.spent = p.spent + (size_t)b * p.kw;
+  L.ban[0] = s.ban0;
+  L.ban[1] = s.ban1;
+  L.ban[2] = s.ban2;
+  L.ban[3] = s.ban3;
+  L.nban = s.emitted;
+  return L;
+}
+
+// Banned ranks r with lo <= r < lo + n.
+__device__ __forceinline__ int banned_in(const SeqLive& L, int lo, int n) {
+  int c = 0;
+#pragma unroll
+  for (int j = 0; j < kBanMax; ++j) {
+    const int r = (int)((L.ban[j >> 1] >> ((j & 1) * 16)) & 0xffffu);
+    c += (j < L.nban && (unsigned)(r - lo) < (unsigned)n) ? 1 : 0;
+  }
+  return c;
+}
+
+// Pointer `pid` (a rank) not yet completed by this sequence.
+__device__ __forceinline__ bool ptr_free(const StepParams& p, const SeqLive& L, int pid) {
+  if (pid < 0 || pid >= p.g.n_strings) return false;
+  if (!L.cnt) return banned_in(L, pid, 1) == 0;
+  return ((L.spent[pid >> 5] >> (pid & 31)) & 1u) == 0;
+}
+
+// Live pointers below token edge e with record ed.
+__device__ __forceinline__ int32_t edge_live(const SeqLive& L, int e, const int4& ed, int32_t c) {
+  return L.cnt ? c : ed.w - banned_in(L, ed.z, ed.w);
+}
+
+// Legality of one edge of the current node (see the filter below); `live`
+// receives the live count of a token edge.
 template <bool kConst>
-__device__ __forceinline__ bool edge_legal(const StepParams& p, const WalkRd<kConst>& w, const int32_t* cnt,
-                                           int e, bool sep_ok, bool stop_ok, int2& ed, int& bad) {
+__device__ __forceinline__ bool edge_legal(const StepParams& p, const WalkRd<kConst>& w, const SeqLive& L,
+                                           int e, bool sep_ok, bool stop_ok, int4& ed, int32_t& live, int& bad) {
   ed = w.edge(e);
-  const int32_t c = cnt[e];  // issued together with the edge record
+  const int32_t c = L.cnt ? L.cnt[e] : 0;  // count mode: issued together with the edge record
+  live = 0;
   if (ed.x < 0 || ed.x >= p.V) {
     bad = 1;
     return false;
@@ -188,12 +254,47 @@ __device__ __forceinline__ bool edge_legal(const StepParams& p, const WalkRd<kCo
       bad = 1;
       return false;
     }
-    return c > 0;
+    live = edge_live(L, e, ed, c);
+    return live > 0;
   }
   if (ed.y == -1) return sep_ok;
   if (ed.y == -2) return stop_ok;
   bad = 1;
   return false;
+}
+
+// A completed pointer leaves the live sets: count mode decrements the counts
+// along its path (threads t0, t0 + stride, ...) and sets its spent flag
+// (thread t0 == 0); read-only mode records its rank in ns.ban (every caller,
+// identically).  ns.emitted is not changed here.
+__device__ __forceinline__ void ban_add(SeqState& ns, int pid) {
+  const int j = ns.emitted;
+  const uint32_t v = (uint32_t)pid << ((j & 1) * 16);
+  switch (j >> 1) {
+    case 0: ns.ban0 |= v; break;
+    case 1: ns.ban1 |= v; break;
+    case 2: ns.ban2 |= v; break;
+    default: ns.ban3 |= v; break;
+  }
+}
+
+__device__ __forceinline__ void decrement_path(const StepParams& p, int b, int pid, int t0, int stride) {
+  const int32_t q0 = __ldg(p.g.path_off + pid), q1 = __ldg(p.g.path_off + pid + 1);
+  int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
+  for (int32_t q = q0 + t0; q < q1; q += stride) {
+    const int32_t e = __ldg(p.g.path + q);
+    if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
+  }
+}
+
+__device__ __forceinline__ void complete_pointer(const StepParams& p, int b, int pid, SeqState& ns, int t0,
+                                                 int stride) {
+  if (p.iv) {
+    ban_add(ns, pid);
+    return;
+  }
+  decrement_path(p, b, pid, t0, stride);
+  if (t0 == 0) p.spent[(size_t)b * p.kw + (pid >> 5)] |= 1u << (pid & 31);
 }
 
 // Edge filter ("Masked sampling inside the sampler"): a token edge is legal
@@ -203,7 +304,7 @@ __device__ __forceinline__ bool edge_legal(const StepParams& p, const WalkRd<kCo
 // (edge order = ascending token order) is stored at s_tok/s_edge[r / T] when
 // r % T == t.  Results in sh.ncand / sh.err, visible after the final barrier.
 template <bool kConst>
-__device__ void filter_node(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int T,
+__device__ __forceinline__ void filter_node(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int T,
                             int t, int32_t* s_tok, int32_t* s_edge, StepShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = s.node;
@@ -222,17 +323,17 @@ __device__ void filter_node(const StepParams& p, const WalkRd<kConst>& w, const 
     return;
   }
   int bad = pid >= p.g.n_strings;
-  const uint32_t word = (pid >= 0 && pid < p.g.n_strings) ? p.spent[(size_t)b * p.kw + (pid >> 5)] : 1u;
-  const bool ctl_ok = pid >= 0 && !bad && ((word >> (pid & 31)) & 1u) == 0;
+  const SeqLive L = seq_live(p, s, b);
+  const bool ctl_ok = pid >= 0 && !bad && ptr_free(p, L, pid);
   const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
   const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
-  const int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
+  int32_t live;
   if (end - beg <= 32) {
     // One warp filters a small node; the others wait at the barrier.
     if (warp == 0) {
       const int e = beg + lane;
-      int2 ed = make_int2(0, 0);
-      const bool legal = e < end && edge_legal<kConst>(p, w, cnt, e, sep_ok, stop_ok, ed, bad);
+      int4 ed = make_int4(0, 0, 0, 0);
+      const bool legal = e < end && edge_legal<kConst>(p, w, L, e, sep_ok, stop_ok, ed, live, bad);
       const unsigned bal = __ballot_sync(kFull, legal);
       if (legal) {
         const int rank = __popc(bal & ((1u << lane) - 1u));
@@ -253,8 +354,8 @@ __device__ void filter_node(const StepParams& p, const WalkRd<kConst>& w, const 
   int running = 0;
   for (int base = beg; base < end; base += kThreads) {
     const int e = base + tid;
-    int2 ed = make_int2(0, 0);
-    const bool legal = e < end && edge_legal<kConst>(p, w, cnt, e, sep_ok, stop_ok, ed, bad);
+    int4 ed = make_int4(0, 0, 0, 0);
+    const bool legal = e < end && edge_legal<kConst>(p, w, L, e, sep_ok, stop_ok, ed, live, bad);
     const unsigned bal = __ballot_sync(kFull, legal);
     if (lane == 0) sh.scan[warp] = __popc(bal);
     __syncthreads();
@@ -294,23 +395,14 @@ __device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<
                                               int b, int beg, int end, int pid, int lane, int4* out) {
   if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > kPreMax) return -1;
   int bad = pid >= p.g.n_strings;
-  const uint32_t word = (pid >= 0 && pid < p.g.n_strings) ? p.spent[(size_t)b * p.kw + (pid >> 5)] : 1u;
-  const bool ctl_ok = pid >= 0 && !bad && ((word >> (pid & 31)) & 1u) == 0;
+  const SeqLive L = seq_live(p, s, b);
+  const bool ctl_ok = pid >= 0 && !bad && ptr_free(p, L, pid);
   const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
   const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
   const int e = beg + lane;
-  int2 ed = make_int2(0, 0);
+  int4 ed = make_int4(0, 0, 0, 0);
   int32_t c = 0;
-  bool legal = false;
-  if (e < end) {
-    ed = w.edge(e);
-    c = p.cnt[(size_t)b * p.g.n_edges + e];
-    if (ed.x < 0 || ed.x >= p.V) bad = 1;
-    else if (ed.y >= 0) { if (ed.y >= p.g.n_nodes) bad = 1; else legal = c > 0; }
-    else if (ed.y == -1) legal = sep_ok;
-    else if (ed.y == -2) legal = stop_ok;
-    else bad = 1;
-  }
+  const bool legal = e < end && edge_legal<kConst>(p, w, L, e, sep_ok, stop_ok, ed, c, bad);
   const unsigned bal = __ballot_sync(kFull, legal);
   if (legal) out[__popc(bal & ((1u << lane) - 1u))] = make_int4(ed.x, e, ed.y, c);
   if (__ballot_sync(kFull, bad)) return -1;
@@ -325,16 +417,16 @@ __device__ __forceinline__ int warp_count_legal(const StepParams& p, const WalkR
                                                 int b, int beg, int end, int pid, int lane, int4& first) {
   if (beg < 0 || end < beg || end > p.g.n_edges) return -1;
   int bad = pid >= p.g.n_strings;
-  const uint32_t word = (pid >= 0 && pid < p.g.n_strings) ? p.spent[(size_t)b * p.kw + (pid >> 5)] : 1u;
-  const bool ctl_ok = pid >= 0 && !bad && ((word >> (pid & 31)) & 1u) == 0;
+  const SeqLive L = seq_live(p, s, b);
+  const bool ctl_ok = pid >= 0 && !bad && ptr_free(p, L, pid);
   const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
   const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
-  const int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
   int count = 0;
   for (int base = beg; base < end && count < 2; base += 32) {
     const int e = base + lane;
-    int2 ed = make_int2(0, 0);
-    const bool legal = e < end && edge_legal<kConst>(p, w, cnt, e, sep_ok, stop_ok, ed, bad);
+    int4 ed = make_int4(0, 0, 0, 0);
+    int32_t live;
+    const bool legal = e < end && edge_legal<kConst>(p, w, L, e, sep_ok, stop_ok, ed, live, bad);
     const unsigned bal = __ballot_sync(kFull, legal);
     if (__ballot_sync(kFull, bad)) return -1;
     if (bal != 0u && count == 0) {
@@ -358,7 +450,7 @@ __device__ __forceinline__ int warp_count_legal(const StepParams& p, const WalkR
 // says that list[0] already holds the node's only legal candidate, whose
 // node has pointer id known_pid.
 template <bool kConst>
-__device__ void forced_chain(const StepParams& p, const WalkRd<kConst>& w, int b, SeqState& ns, int lane,
+__device__ __forceinline__ void forced_chain(const StepParams& p, const WalkRd<kConst>& w, int b, SeqState& ns, int lane,
                              int4* list, bool known, int known_pid, int& list_n, int& list_pid) {
   list_n = -1;
   list_pid = -2;
@@ -401,13 +493,7 @@ __device__ void forced_chain(const StepParams& p, const WalkRd<kConst>& w, int b
       ns.node = only.z;
     } else {
       // A control edge is legal only at a terminal whose pointer is unspent.
-      const int32_t q0 = __ldg(p.g.path_off + pid), q1 = __ldg(p.g.path_off + pid + 1);
-      int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
-      for (int32_t q = q0 + lane; q < q1; q += 32) {
-        const int32_t e = __ldg(p.g.path + q);
-        if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
-      }
-      if (lane == 0) p.spent[(size_t)b * p.kw + (pid >> 5)] |= 1u << (pid & 31);
+      complete_pointer(p, b, pid, ns, lane, 32);
       ns.emitted += 1;
       ns.node = 0;
       if (only.z == -2) ns.done = 1;
@@ -421,7 +507,7 @@ __device__ void forced_chain(const StepParams& p, const WalkRd<kConst>& w, int b
 // Called by every thread of the sequence's last CTA; thread 0 returns the
 // sequence's done flag afterwards.
 template <bool kConst>
-__device__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b,
+__device__ __forceinline__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b,
                                float best_l, int32_t best_t, int32_t best_e, int32_t ncand, int32_t err) {
   const int tid = threadIdx.x;
   int status = TC_OK;
@@ -434,16 +520,16 @@ __device__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, con
   } else if (best_t == INT_MAX || best_e < 0 || best_e >= p.g.n_edges || !(best_l == best_l)) {
     status = TC_ERR_BOUNDS;  // no comparable logit (NaN) or a corrupted slot
   } else {
-    const int2 ed = w.edge(best_e);
+    const SeqLive L = seq_live(p, s, b);
+    const int4 ed = w.edge(best_e);
     if (ed.x != best_t) {
       status = TC_ERR_BOUNDS;
     } else if (ed.y >= 0) {
-      if (p.cnt[(size_t)b * p.g.n_edges + best_e] <= 0) status = TC_ERR_NO_LIVE_EDGE;
+      if (edge_live(L, best_e, ed, L.cnt ? L.cnt[best_e] : 0) <= 0) status = TC_ERR_NO_LIVE_EDGE;
       else new_node = ed.y;
     } else {
       const int32_t pid = w.ptr(s.node);
-      if (pid < 0 || pid >= p.g.n_strings ||
-          ((p.spent[(size_t)b * p.kw + (pid >> 5)] >> (pid & 31)) & 1u)) {
+      if (!ptr_free(p, L, pid)) {
         status = TC_ERR_NO_LIVE_EDGE;
       } else {
         ptr_done = pid;
@@ -453,15 +539,8 @@ __device__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, con
     }
   }
   __syncthreads();  // every thread has decided before the state changes
-  if (ptr_done >= 0) {
-    // The completed pointer is no longer live below any edge of its path.
-    const int32_t q0 = __ldg(p.g.path_off + ptr_done), q1 = __ldg(p.g.path_off + ptr_done + 1);
-    int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
-    for (int32_t q = q0 + tid; q < q1; q += kThreads) {
-      const int32_t e = __ldg(p.g.path + q);
-      if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
-    }
-  }
+  // The completed pointer is no longer live below any edge of its path.
+  if (ptr_done >= 0 && !p.iv) decrement_path(p, b, ptr_done, tid, kThreads);
   // Forced continuations follow a decision that leaves the sequence live.
   const bool chain = p.jump && status == TC_OK && !stop;
   if (chain) __syncthreads();  // the decrements above are seen by the chain's legal sets
@@ -476,8 +555,9 @@ __device__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, con
       ns.node = new_node;
       ns.len = s.len + 1;
       if (ptr_done >= 0) {
+        if (p.iv) ban_add(ns, ptr_done);
+        else if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
         ns.emitted = s.emitted + 1;
-        if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
       }
       if (stop) ns.done = 1;
     }
@@ -513,7 +593,7 @@ __device__ int finish_sequence(const StepParams& p, const WalkRd<kConst>& w, con
 }
 
 // A live sequence whose length reached the budget stops here (CTA t == 0, thread 0).
-__device__ void stop_out_of_steps(const StepParams& p, const SeqState& s, int b) {
+__device__ __forceinline__ void stop_out_of_steps(const StepParams& p, const SeqState& s, int b) {
   SeqState ns = s;
   ns.status = TC_ERR_MAX_STEPS;
   ns.done = 1;
@@ -530,7 +610,7 @@ __device__ void stop_out_of_steps(const StepParams& p, const SeqState& s, int b)
 // Fold the per-warp bests, combine the CTAs of sequence b, let the last CTA
 // apply the transition; then, in a loop-control launch, set the loop condition.
 template <bool kConst>
-__device__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int mode,
+__device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int mode,
                           float wl, int32_t wt, int32_t we, StepShared& sh) {
   // mode: 0 = idle (stopped or failed before this step), 1 = active, 2 = out of steps now
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -721,6 +801,8 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
   int32_t wt = INT_MAX, ws = -1;
   if (mode == 1) {
     const uint16_t* x = hidden_row(p, s, b);
+    if (p.device_form && tid == 32 && s.len + 1 < p.max_steps)
+      prefetch_l2(x + (size_t)p.B * p.H, (uint32_t)p.H * 2u);  // the next step's hidden state
     XFrag<NCH> xf;
     if constexpr (NCH > 0) {
       xf.load(x, lane);
@@ -767,6 +849,9 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
             sh.spec_n[l] = sn;
             sh.spec_pid[l] = cpid;
           }
+          __syncwarp();
+          // If this candidate wins, its child's rows are the next step's reads: start them towards L2 now.
+          if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].x * p.H, (uint32_t)p.H * 2u);
 #pragma unroll
           for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xf.v[i], acc);
         } else {
@@ -775,6 +860,9 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
             sh.spec_n[l] = sn;
             sh.spec_pid[l] = cpid;
           }
+          __syncwarp();
+          // If this candidate wins, its child's rows are the next step's reads: start them towards L2 now.
+          if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].x * p.H, (uint32_t)p.H * 2u);
           for (int c = lane; c < nch; c += 32) acc = dot8(ld_row(r4 + c), xs[c], acc);
         }
         const float v = warp_sum(acc);
@@ -822,8 +910,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
         else new_node = win.z;
       } else {
         const int32_t pid = sh.pid;
-        if (pid < 0 || pid >= p.g.n_strings ||
-            ((p.spent[(size_t)b * p.kw + (pid >> 5)] >> (pid & 31)) & 1u)) {
+        if (!ptr_free(p, seq_live(p, s, b), pid)) {
           status = TC_ERR_NO_LIVE_EDGE;
         } else {
           ptr_done = pid;
@@ -839,14 +926,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
     const bool chain = p.jump && status == TC_OK && !stop && (next_n == 1 || ptr_done >= 0);
     if (!chain && next_n > 0)
       for (int i = tid; i < next_n; i += kThreads) p.pre[(size_t)b * kPreMax + i] = sh.spec[bs][i];
-    if (ptr_done >= 0) {
-      const int32_t q0 = __ldg(p.g.path_off + ptr_done), q1 = __ldg(p.g.path_off + ptr_done + 1);
-      int32_t* cnt = p.cnt + (size_t)b * p.g.n_edges;
-      for (int32_t q = q0 + tid; q < q1; q += kThreads) {
-        const int32_t e = __ldg(p.g.path + q);
-        if (e >= 0 && e < p.g.n_edges) cnt[e] -= 1;
-      }
-    }
+    if (ptr_done >= 0 && !p.iv) decrement_path(p, b, ptr_done, tid, kThreads);
     if (chain) __syncthreads();  // the decrements above are seen by the chain's legal sets
     if (warp == 0) {
       SeqState ns = s;
@@ -858,8 +938,9 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
         ns.node = new_node;
         ns.len = s.len + 1;
         if (ptr_done >= 0) {
+          if (p.iv) ban_add(ns, ptr_done);
+          else if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
           ns.emitted = s.emitted + 1;
-          if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
         }
         if (stop) ns.done = 1;
       }
@@ -883,7 +964,12 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
         // The winner's own (precomputed) list slot serves as the chain's scratch.
         int4* list = sh.spec[bs];
         forced_chain<kConst>(p, w, b, ns, lane, list, next_n == 1, sh.spec_pid[bs], pre_n, pre_pid);
-        if (pre_n > 0 && lane < pre_n) p.pre[(size_t)b * kPreMax + lane] = list[lane];
+        if (pre_n > 0 && lane < pre_n) {
+          p.pre[(size_t)b * kPreMax + lane] = list[lane];
+          prefetch_l2(p.emb + (size_t)list[lane].x * p.H, (uint32_t)p.H * 2u);
+        }
+        if (lane == 0 && !ns.done && ns.len < p.max_steps)
+          prefetch_l2(p.hidden + ((size_t)ns.len * p.B + b) * p.H, (uint32_t)p.H * 2u);
       }
       if (ns.status == TC_OK) {
         ns.pad0 = pre_n >= 0 ? pre_n + 1 : 0;
@@ -1079,10 +1165,13 @@ __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p
 __global__ void __launch_bounds__(kThreads) reset_kernel(const ResetParams r) {
   const int b = blockIdx.y, tid = threadIdx.x;
   const int E = r.g.n_edges;
-  int32_t* cnt = r.cnt + (size_t)b * E;
-  for (int e = blockIdx.x * kThreads + tid; e < E; e += gridDim.x * kThreads) cnt[e] = __ldg(r.g.static_cnt + e);
+  if (!r.iv) {  // count mode: a fresh copy of the live counts and no spent flags
+    int32_t* cnt = r.cnt + (size_t)b * E;
+    for (int e = blockIdx.x * kThreads + tid; e < E; e += gridDim.x * kThreads) cnt[e] = __ldg(r.g.static_cnt + e);
+    if (blockIdx.x == 0)
+      for (int i = tid; i < r.kw; i += kThreads) r.spent[(size_t)b * r.kw + i] = 0u;
+  }
   if (blockIdx.x == 0) {
-    for (int i = tid; i < r.kw; i += kThreads) r.spent[(size_t)b * r.kw + i] = 0u;
     if (r.toks) {
       for (int i = tid; i < r.max_steps; i += kThreads) {
         r.toks[(size_t)b * r.max_steps + i] = -1;
@@ -1401,7 +1490,7 @@ cudaError_t launch_step(const StepParams& p, bool const_resident, int head, int 
 }
 
 cudaError_t launch_reset(const ResetParams& r, cudaStream_t s) {
-  int bx = (r.g.n_edges + kThreads * 4 - 1) / (kThreads * 4);
+  int bx = r.iv ? 1 : (r.g.n_edges + kThreads * 4 - 1) / (kThreads * 4);
   if (bx < 1) bx = 1;
   if (bx > 64) bx = 64;
   reset_kernel<<<dim3(bx, r.B), kThreads, 0, s>>>(r);

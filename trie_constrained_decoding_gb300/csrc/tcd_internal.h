@@ -14,6 +14,11 @@ struct tc_trie {
   int32_t n_strings = 0, max_depth = 0, max_fanout = 0, root_fanout = 0;
   int64_t total_tokens = 0;
   std::vector<int32_t> node_begin, edge_tok, edge_child, node_ptr, static_cnt, path_off, path;
+  // Depth-first numbering of the pointers (a node's own pointer before those
+  // below it, children in token order): every subtree holds a contiguous range
+  // of ranks.  edge_lo[e] is the first rank below a token edge's child (the
+  // range has static_cnt[e] ranks), or the terminal's own rank for a control edge.
+  std::vector<int32_t> ptr_rank, edge_lo;
   uint64_t content_hash = 0;
 
   int32_t n_nodes() const { return (int32_t)node_ptr.size(); }
@@ -22,11 +27,15 @@ struct tc_trie {
 
 namespace tcd {
 
-// Device walk image, int32 words: node_begin[N+1] | pad to even | edges {tok, child}[E] | node_ptr[N].
+// Device walk image, int32 words:
+//   node_begin[N+1] | pad to a multiple of 4 | edges {tok, child, lo, n}[E] | node_rank[N]
+// where {lo, n} is the range of pointer ranks below a token edge (or the
+// terminal's own rank and n = 1 for a control edge) and node_rank is the rank
+// of the node's pointer or -1.  On the device a pointer is named by its rank.
 struct WalkLayout {
   int32_t n_nodes, n_edges;
-  int32_t off_edges;   // word offset of the edge records (even)
-  int32_t off_ptr;     // word offset of node_ptr
+  int32_t off_edges;   // word offset of the edge records (multiple of 4: 16-byte records)
+  int32_t off_ptr;     // word offset of node_rank
   int32_t words;       // total words
 };
 WalkLayout walk_layout(int32_t n_nodes, int32_t n_edges);

@@ -24,8 +24,8 @@ WalkLayout walk_layout(int32_t n_nodes, int32_t n_edges) {
   WalkLayout L;
   L.n_nodes = n_nodes;
   L.n_edges = n_edges;
-  L.off_edges = (n_nodes + 1 + 1) & ~1;  // keep the {tok, child} records 8-byte aligned
-  L.off_ptr = L.off_edges + 2 * n_edges;
+  L.off_edges = (n_nodes + 1 + 3) & ~3;  // keep the {tok, child, lo, n} records 16-byte aligned
+  L.off_ptr = L.off_edges + 4 * n_edges;
   L.words = L.off_ptr + n_nodes;
   return L;
 }
@@ -34,10 +34,14 @@ std::vector<int32_t> build_walk_image(const tc_trie& t, const WalkLayout& L) {
   std::vector<int32_t> img((size_t)L.words, 0);
   std::copy(t.node_begin.begin(), t.node_begin.end(), img.begin());
   for (int32_t e = 0; e < L.n_edges; ++e) {
-    img[(size_t)L.off_edges + 2 * (size_t)e] = t.edge_tok[e];
-    img[(size_t)L.off_edges + 2 * (size_t)e + 1] = t.edge_child[e];
+    int32_t* r = img.data() + L.off_edges + 4 * (size_t)e;
+    r[0] = t.edge_tok[e];
+    r[1] = t.edge_child[e];
+    r[2] = t.edge_lo[e];
+    r[3] = t.edge_child[e] >= 0 ? t.static_cnt[e] : 1;
   }
-  std::copy(t.node_ptr.begin(), t.node_ptr.end(), img.begin() + L.off_ptr);
+  for (int32_t n = 0; n < L.n_nodes; ++n)
+    img[(size_t)L.off_ptr + n] = t.node_ptr[n] >= 0 ? t.ptr_rank[t.node_ptr[n]] : -1;
   return img;
 }
 
@@ -214,7 +218,37 @@ extern "C" tc_status tc_compile_trie(const int32_t* ids, const int64_t* offsets,
   for (int32_t e = 0; e < E; ++e)
     if (t->edge_child[e] >= 0) t->static_cnt[e] = subtree[t->edge_child[e]];
 
-  // 5. Per-pointer edge paths (root to terminal), found by binary search of
+  // 5. Depth-first pointer ranks: a node's own pointer first, then its
+  //    children's subtrees in token order; each subtree gets one range.
+  t->ptr_rank.assign((size_t)n_strings, -1);
+  t->edge_lo.assign((size_t)E, -1);
+  {
+    std::vector<int32_t> lo_of((size_t)N, 0);
+    std::vector<std::pair<int32_t, int32_t>> stack;  // (node, next edge to visit)
+    int32_t next_rank = 0;
+    stack.push_back({0, t->node_begin[0]});
+    lo_of[0] = 0;
+    if (t->node_ptr[0] >= 0) t->ptr_rank[t->node_ptr[0]] = next_rank++;
+    while (!stack.empty()) {
+      auto& top = stack.back();
+      const int32_t n = top.first;
+      if (top.second == t->node_begin[n + 1]) {
+        stack.pop_back();
+        continue;
+      }
+      const int32_t e = top.second++;
+      const int32_t c = t->edge_child[e];
+      if (c < 0) continue;
+      lo_of[c] = next_rank;
+      if (t->node_ptr[c] >= 0) t->ptr_rank[t->node_ptr[c]] = next_rank++;
+      stack.push_back({c, t->node_begin[c]});
+    }
+    for (int32_t n = 0; n < N; ++n)
+      for (int32_t e = t->node_begin[n]; e < t->node_begin[n + 1]; ++e)
+        t->edge_lo[e] = t->edge_child[e] >= 0 ? lo_of[t->edge_child[e]] : t->ptr_rank[t->node_ptr[n]];
+  }
+
+  // 6. Per-pointer edge paths (root to terminal), found by binary search of
   //    each node's sorted edge range.
   t->path_off.assign((size_t)n_strings + 1, 0);
   t->path.resize((size_t)total);
@@ -279,6 +313,13 @@ extern "C" tc_status tc_trie_export(const tc_trie* t, int32_t* node_begin, int32
   put(static_cnt, t->static_cnt);
   put(path_off, t->path_off);
   put(path, t->path);
+  return TC_OK;
+}
+
+extern "C" tc_status tc_trie_export_ranks(const tc_trie* t, int32_t* ptr_rank, int32_t* edge_lo) {
+  if (!t) return TC_ERR_INVALID_ARG;
+  if (ptr_rank) std::memcpy(ptr_rank, t->ptr_rank.data(), t->ptr_rank.size() * sizeof(int32_t));
+  if (edge_lo) std::memcpy(edge_lo, t->edge_lo.data(), t->edge_lo.size() * sizeof(int32_t));
   return TC_OK;
 }
 
