@@ -108,7 +108,7 @@ enum {
  */
 #define TC_FLAG_JUMP_FORWARD 0x100
 
-/* Bytes of __constant__ memory reserved for one walk image. */
+/* Bytes of __constant__ memory reserved for the header part of one walk image. */
 #define TC_CONST_CAPACITY_BYTES (63 * 1024)
 
 typedef struct tc_trie tc_trie;   /* compiled catalog, host object */
@@ -123,9 +123,11 @@ typedef struct tc_trie_info_t {
   int32_t root_fanout;      /* edge count of the root */
   int32_t max_depth;        /* longest catalog string, in tokens */
   int32_t vocab, sep_id, stop_id;
-  int32_t reserved;
+  int32_t header_bytes;     /* bytes of the walk image's header part (node ranges and pointer
+                               ranks): what constant residency places in __constant__ memory */
   int64_t total_tokens;     /* sum of the string lengths */
-  int64_t walk_image_bytes; /* bytes of the device walk image (node ranges, edges, node pointer ids) */
+  int64_t walk_image_bytes; /* bytes of the device walk image: the header part and the 32-byte
+                               edge records (token, child, rank range, child header) */
 } tc_trie_info_t;
 
 /* ---------------------------------------------------------------- compiler */

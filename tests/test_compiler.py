@@ -128,14 +128,17 @@ def test_fanout_cap(tcd):
 
 
 def test_walk_image_size(tcd):
+    """Header part: node ranges and pointer ranks (2N + 1 words, what constant
+    residency copies); then 32-byte edge records from a 32-byte boundary."""
     w = I.tiny()
     info = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab).info()
     N, E = info["n_nodes"], info["n_edges"]
-    assert info["walk_image_bytes"] == 4 * (((N + 1 + 3) & ~3) + 4 * E + N)
-    assert info["walk_image_bytes"] <= tcd.CONST_CAPACITY_BYTES
-    b = I.batched()
-    info = tcd.Trie.compile(b.catalog, b.sep_id, b.stop_id, b.vocab).info()
-    assert info["walk_image_bytes"] > tcd.CONST_CAPACITY_BYTES      # the 1000-tool catalog lives in global memory
+    assert info["header_bytes"] == 4 * (2 * N + 1)
+    assert info["walk_image_bytes"] == 4 * (((2 * N + 1 + 7) & ~7) + 8 * E)
+    assert info["header_bytes"] <= tcd.CONST_CAPACITY_BYTES
+    u = I.unstructured()
+    info = tcd.Trie.compile(u.catalog, u.sep_id, u.stop_id, u.vocab, u.max_fanout).info()
+    assert info["header_bytes"] > tcd.CONST_CAPACITY_BYTES      # the hex catalog's headers need global memory
 
 
 def _rank_catalogs():

@@ -172,16 +172,20 @@ def test_argument_errors(tcd):
 def test_residency_selection_and_capacity(tcd):
     b = workload("batched")
     _, emb = embedding(b.vocab, b.hidden, b.emb_kind)
-    ctx = tcd.Context(emb, max_batch=1, cand_cap=256)
+    ctx = tcd.Context(emb, max_batch=1, cand_cap=4096)
     big = tcd.Trie.compile(b.catalog, b.sep_id, b.stop_id, b.vocab)
-    with pytest.raises(tcd.TcError) as e:
-        ctx.bind(big, tcd.RES_CONST)
-    assert e.value.name == "TC_ERR_CONST_CAPACITY"
-    ctx.bind(big, tcd.RES_AUTO)
-    assert ctx.residency() == tcd.RES_GLOBAL
+    ctx.bind(big, tcd.RES_AUTO)                 # 1000-tool headers fit the constant bank
+    assert ctx.residency() == tcd.RES_CONST
     u = workload("unstructured")
     hexes = tcd.Trie.compile(u.catalog, u.sep_id, u.stop_id, u.vocab, 4096)
-    with pytest.raises(tcd.TcError) as e:     # root fan-out above the 256-slot candidate buffer
-        ctx.bind(hexes)
-    assert e.value.name == "TC_ERR_CAPACITY"
+    with pytest.raises(tcd.TcError) as e:       # ~16k nodes: headers above the constant capacity
+        ctx.bind(hexes, tcd.RES_CONST)
+    assert e.value.name == "TC_ERR_CONST_CAPACITY"
+    ctx.bind(hexes, tcd.RES_AUTO)
+    assert ctx.residency() == tcd.RES_GLOBAL
     ctx.close()
+    small = tcd.Context(emb, max_batch=1, cand_cap=256)
+    with pytest.raises(tcd.TcError) as e:       # root fan-out above the 256-slot candidate buffer
+        small.bind(hexes)
+    assert e.value.name == "TC_ERR_CAPACITY"
+    small.close()

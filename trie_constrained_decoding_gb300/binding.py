@@ -43,7 +43,7 @@ class _TrieInfo(ctypes.Structure):
     _fields_ = [("n_nodes", ctypes.c_int32), ("n_edges", ctypes.c_int32), ("n_strings", ctypes.c_int32),
                 ("max_fanout", ctypes.c_int32), ("root_fanout", ctypes.c_int32), ("max_depth", ctypes.c_int32),
                 ("vocab", ctypes.c_int32), ("sep_id", ctypes.c_int32), ("stop_id", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("total_tokens", ctypes.c_int64),
+                ("header_bytes", ctypes.c_int32), ("total_tokens", ctypes.c_int64),
                 ("walk_image_bytes", ctypes.c_int64)]
 
 
@@ -135,7 +135,7 @@ class Trie:
     def info(self) -> dict:
         inf = _TrieInfo()
         _check(_info(self._h, ctypes.byref(inf)), "tc_trie_info")
-        return {name: getattr(inf, name) for name, _ in _TrieInfo._fields_ if name != "reserved"}
+        return {name: getattr(inf, name) for name, _ in _TrieInfo._fields_}
 
     def export(self) -> dict:
         i = self.info()

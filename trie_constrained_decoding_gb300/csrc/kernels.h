@@ -26,7 +26,7 @@ constexpr int kMaxDynamicSmem = kMaxHidden * 2 + 2 * kMaxCandCap * 4 + 128 + 128
 constexpr int kBanMax = 8;
 constexpr int kBanMaxStrings = 65535;
 
-// Per-sequence decode state (device memory, one record per sequence).
+// Per-sequence decode state (device memory, one 48-byte record per sequence).
 struct SeqState {
   int32_t node;     // current trie node
   int32_t emitted;  // pointers completed so far (j)
@@ -34,10 +34,18 @@ struct SeqState {
   int32_t status;   // TC_OK or the error that stopped the sequence
   int32_t done;     // 1 once the stop token was emitted or an error occurred
   int32_t k;        // pointers owed in total
-  int32_t pad0, pad1;  // one-CTA sparse step: precomputed list size + 1 (0: none) and its node's pointer
+  int32_t pre_n;    // one-CTA sparse step: size + 1 of the node's precomputed legal set (0: none)
+  int32_t pre_pid;  // and the node's pointer rank
   // Read-only no-repeat mode: ranks of the completed pointers, two per word
   // (scalar fields: an array member would keep the state out of registers).
   uint32_t ban0, ban1, ban2, ban3;
+};
+
+// A legal candidate as kept in candidate lists: {token, edge, child, live
+// pointers below} and the child's header {edge begin, edge end, pointer rank, 0}.
+struct Cand {
+  int4 a;
+  int4 h;
 };
 
 // One CTA's best candidate, handed to the sequence's last CTA.
@@ -57,8 +65,9 @@ struct Ctrl {
 
 // The bound grammar as the kernels see it.
 struct GrammarView {
-  const int32_t* img;        // walk image in global memory (also the source of the constant copy)
+  const int32_t* img;        // walk image in global memory (its header part is the constant copy)
   int32_t off_edges, off_ptr;
+  int32_t root_beg, root_end, root_pid;  // the root's header
   int32_t n_nodes, n_edges, n_strings;
   const int32_t* static_cnt; // [E]
   const int32_t* path_off;   // [K+1] by pointer rank
@@ -117,7 +126,7 @@ struct StepParams {
   int32_t loop_ctrl;        // 1: this launch sets the loop's condition (last step of a loop body)
   unsigned long long* stats;  // optional counters, see StatSlot
   HeadScratch hs;           // GEMM heads only
-  int4* pre;                // [B, 32] precomputed candidate lists (one-CTA sparse step), or null
+  Cand* pre;                // [B, 32] precomputed candidate lists (one-CTA sparse step), or null
   int32_t jump;             // 1: emit forced tokens without the head after each decision (device form only)
   int32_t iv;               // 1: read-only no-repeat state (rank ranges + banned ranks); 0: cnt/spent arrays
 };

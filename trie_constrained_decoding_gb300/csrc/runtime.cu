@@ -82,7 +82,8 @@ struct DevGrammar {
   SeqState* d_st = nullptr;
   int32_t* d_cnt = nullptr;
   uint32_t* d_spent = nullptr;
-  int4* d_pre = nullptr;  // [max_batch, 32] next-step candidate lists
+  Cand* d_pre = nullptr;  // [max_batch, 32] next-step candidate lists
+  int32_t root_beg = 0, root_end = 0, root_pid = -1;
   int32_t kw = 1;
   int32_t batch = 0, k = 0;  // of the last reset (0: none)
   bool force_counts = false;  // TC_BIND_LIVE_COUNTS: per-sequence count arrays for every k
@@ -94,6 +95,9 @@ struct DevGrammar {
     v.img = d_img;
     v.off_edges = layout.off_edges;
     v.off_ptr = layout.off_ptr;
+    v.root_beg = root_beg;
+    v.root_end = root_end;
+    v.root_pid = root_pid;
     v.n_nodes = n_nodes;
     v.n_edges = n_edges;
     v.n_strings = n_strings;
@@ -316,7 +320,7 @@ tc_status ensure_const(tc_ctx* c, DevGrammar* g, cudaStream_t s) {
   if (g->residency != TC_RES_CONST) return TC_OK;
   std::lock_guard<std::mutex> lk(g_const_mu);
   if (g_const_owner[c->device] == g) return TC_OK;
-  TC_CUDA(const_upload(g->d_img, (size_t)g->layout.words * 4, s));
+  TC_CUDA(const_upload(g->d_img, (size_t)g->layout.header_words * 4, s));
   g_const_owner[c->device] = g;
   return TC_OK;
 }
@@ -383,7 +387,7 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
       cudaSuccess)
     return fail(e, "cudaStreamBeginCaptureToGraph");
   if (g->residency == TC_RES_CONST) {
-    if ((e = const_upload(g->d_img, (size_t)g->layout.words * 4, cs)) != cudaSuccess)
+    if ((e = const_upload(g->d_img, (size_t)g->layout.header_words * 4, cs)) != cudaSuccess)
       return fail(e, "constant re-bind node");
   }
   ResetParams r = reset_params(c, g, key.batch, key.k, key.max_steps);
@@ -547,10 +551,12 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
   }
   const WalkLayout L = walk_layout(t->n_nodes(), t->n_edges());
   const size_t img_bytes = (size_t)L.words * 4;
+  const size_t hdr_bytes = (size_t)L.header_words * 4;  // the part constant residency places in __constant__
   int32_t res = residency;
-  if (res == TC_RES_AUTO) res = img_bytes <= TC_CONST_CAPACITY_BYTES ? TC_RES_CONST : TC_RES_GLOBAL;
-  if (res == TC_RES_CONST && img_bytes > TC_CONST_CAPACITY_BYTES) {
-    set_error_message("tc_bind_grammar: walk image of " + std::to_string(img_bytes) + " bytes exceeds constant capacity");
+  if (res == TC_RES_AUTO) res = hdr_bytes <= TC_CONST_CAPACITY_BYTES ? TC_RES_CONST : TC_RES_GLOBAL;
+  if (res == TC_RES_CONST && hdr_bytes > TC_CONST_CAPACITY_BYTES) {
+    set_error_message("tc_bind_grammar: walk image header of " + std::to_string(hdr_bytes) +
+                      " bytes exceeds constant capacity");
     return TC_ERR_CONST_CAPACITY;
   }
   DeviceGuard dg(c->device);
@@ -572,6 +578,9 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
     g->layout = L;
     g->kw = (t->n_strings + 31) / 32;
     g->force_counts = force_counts;
+    g->root_beg = t->node_begin[0];
+    g->root_end = t->node_begin[1];
+    g->root_pid = t->node_ptr[0] >= 0 ? t->ptr_rank[t->node_ptr[0]] : -1;
     const std::vector<int32_t> img = build_walk_image(*t, L);
     // On the device a pointer is named by its depth-first rank: its edge path
     // is stored at its rank.
@@ -594,8 +603,8 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
     if (e == cudaSuccess) e = cudaMalloc(&g->d_path, sizeof(int32_t) * std::max<size_t>(1, t->path.size()));
     if (e == cudaSuccess) e = cudaMalloc(&g->d_st, sizeof(SeqState) * B);
     if (e == cudaSuccess) e = cudaMalloc(&g->d_spent, sizeof(uint32_t) * B * g->kw);
-    if (e == cudaSuccess) e = cudaMalloc(&g->d_pre, sizeof(int4) * B * 32);
-    if (e == cudaSuccess) e = cudaMemset(g->d_pre, 0, sizeof(int4) * B * 32);
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_pre, sizeof(Cand) * B * 32);
+    if (e == cudaSuccess) e = cudaMemset(g->d_pre, 0, sizeof(Cand) * B * 32);
     if (e == cudaSuccess) e = cudaMemcpy(g->d_img, img.data(), img_bytes, cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
       e = cudaMemcpy(g->d_static_cnt, t->static_cnt.data(), sizeof(int32_t) * t->static_cnt.size(), cudaMemcpyHostToDevice);
@@ -613,7 +622,7 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
   }
   if (res == TC_RES_CONST) {
     std::lock_guard<std::mutex> lk(g_const_mu);
-    TC_CUDA(const_upload(g->d_img, img_bytes, s));
+    TC_CUDA(const_upload(g->d_img, hdr_bytes, s));
     g_const_owner[c->device] = g;
   }
   g->batch = 0;

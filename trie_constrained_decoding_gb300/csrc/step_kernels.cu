@@ -54,14 +54,18 @@ struct WalkRd {
     if constexpr (kConst) return c_walk[n];
     else return __ldg(img + n);
   }
-  // {token, child, first rank below, ranks below} (control edges: the terminal's own rank, 1).
-  // Lanes read different edges, which the constant cache would serialise, so
-  // edge records always come through the read-only data cache (one 16-byte
-  // load each; measured faster than four constant-bank words at B = 1); node
-  // ranges and pointer ids, read alike by a whole warp, come from the constant
-  // bank when the grammar is resident there.
+  // Edge record, first half: {token, child, first rank below, ranks below}
+  // (control edges: the terminal's own rank, 1).  Lanes read different edges,
+  // which the constant cache would serialise, so edge records always come
+  // through the read-only data cache (measured faster than constant-bank words
+  // at B = 1); node ranges and pointer ranks, read alike by a whole warp, come
+  // from the constant bank when the grammar is resident there.
   __device__ __forceinline__ int4 edge(int32_t e) const {
-    return __ldg(reinterpret_cast<const int4*>(img + off_edges) + e);
+    return __ldg(reinterpret_cast<const int4*>(img + off_edges) + 2 * e);
+  }
+  // Second half: the child's header {edge begin, edge end, pointer rank, 0}.
+  __device__ __forceinline__ int4 child_hdr(int32_t e) const {
+    return __ldg(reinterpret_cast<const int4*>(img + off_edges) + 2 * e + 1);
   }
   __device__ __forceinline__ int32_t ptr(int32_t n) const {
     if constexpr (kConst) return c_walk[off_ptr + n];
@@ -392,7 +396,7 @@ constexpr int kPreMax = 32;  // largest legal set kept as a precomputed candidat
 // Returns the count, or -1 when an index is out of range or the fan-out is larger.
 template <bool kConst>
 __device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
-                                              int b, int beg, int end, int pid, int lane, int4* out) {
+                                              int b, int beg, int end, int pid, int lane, Cand* out) {
   if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > kPreMax) return -1;
   int bad = pid >= p.g.n_strings;
   const SeqLive L = seq_live(p, s, b);
@@ -401,20 +405,21 @@ __device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<
   const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
   const int e = beg + lane;
   int4 ed = make_int4(0, 0, 0, 0);
+  const int4 hd = e < end ? w.child_hdr(e) : make_int4(0, 0, -1, 0);  // issued with the first half
   int32_t c = 0;
   const bool legal = e < end && edge_legal<kConst>(p, w, L, e, sep_ok, stop_ok, ed, c, bad);
   const unsigned bal = __ballot_sync(kFull, legal);
-  if (legal) out[__popc(bal & ((1u << lane) - 1u))] = make_int4(ed.x, e, ed.y, c);
+  if (legal) out[__popc(bal & ((1u << lane) - 1u))] = Cand{make_int4(ed.x, e, ed.y, c), hd};
   if (__ballot_sync(kFull, bad)) return -1;
   return __popc(bal);
 }
 
 // Size of the legal set of node [beg, end), capped at 2, and its first legal
-// candidate {token, edge, child, 0} (one warp, any fan-out).  -1 when an index
-// is out of range.
+// candidate (live count 0) with its child's header (one warp, any fan-out).
+// -1 when an index is out of range.
 template <bool kConst>
 __device__ __forceinline__ int warp_count_legal(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
-                                                int b, int beg, int end, int pid, int lane, int4& first) {
+                                                int b, int beg, int end, int pid, int lane, Cand& first) {
   if (beg < 0 || end < beg || end > p.g.n_edges) return -1;
   int bad = pid >= p.g.n_strings;
   const SeqLive L = seq_live(p, s, b);
@@ -431,7 +436,8 @@ __device__ __forceinline__ int warp_count_legal(const StepParams& p, const WalkR
     if (__ballot_sync(kFull, bad)) return -1;
     if (bal != 0u && count == 0) {
       const int src = __ffs(bal) - 1;
-      first = make_int4(__shfl_sync(kFull, ed.x, src), base + src, __shfl_sync(kFull, ed.y, src), 0);
+      const int fe = base + src;
+      first = Cand{make_int4(__shfl_sync(kFull, ed.x, src), fe, __shfl_sync(kFull, ed.y, src), 0), w.child_hdr(fe)};
     }
     count += __popc(bal);
   }
@@ -443,40 +449,40 @@ __device__ __forceinline__ int warp_count_legal(const StepParams& p, const WalkR
 // the sequence's node, that token is emitted without reading the head - its
 // logit slot holds NaN - and the walk advances, pointer completions included.
 // Run by one whole warp after the step's own transition; `ns` is the state
-// after that transition, the same in every lane on entry and on return.
-// With `list` (grammars whose nodes have at most kPreMax edges) the legal set
-// that ends the chain is left in list[0, list_n) with its node's pointer id in
-// list_pid (list_n = -1 when the chain ended for another reason); `known`
-// says that list[0] already holds the node's only legal candidate, whose
-// node has pointer id known_pid.
+// after that transition, the same in every lane on entry and on return, and
+// `hdr` its node's header {edge begin, edge end, pointer rank} (carried from
+// edge records, so the chain reads no node headers).  With `list` (grammars
+// whose nodes have at most kPreMax edges) the legal set that ends the chain is
+// left in list[0, list_n) with its node's pointer rank in list_pid (list_n =
+// -1 when the chain ended for another reason); `known` says that list[0]
+// already holds the node's only legal candidate.
+__device__ __forceinline__ int4 root_hdr(const StepParams& p) {
+  return make_int4(p.g.root_beg, p.g.root_end, p.g.root_pid, 0);
+}
+
 template <bool kConst>
-__device__ __forceinline__ void forced_chain(const StepParams& p, const WalkRd<kConst>& w, int b, SeqState& ns, int lane,
-                             int4* list, bool known, int known_pid, int& list_n, int& list_pid) {
+__device__ __forceinline__ void forced_chain(const StepParams& p, const WalkRd<kConst>& w, int b, SeqState& ns,
+                                             int lane, int4 hdr, Cand* list, bool known, int& list_n,
+                                             int& list_pid) {
   list_n = -1;
   list_pid = -2;
   unsigned long long forced = 0;
   while (!ns.done && ns.len < p.max_steps && ns.len < p.out_stride) {
-    int count, pid;
-    int4 only = make_int4(0, -1, 0, 0);
+    int count;
+    const int pid = hdr.z;
+    Cand only{make_int4(0, -1, 0, 0), make_int4(0, 0, -1, 0)};
     if (known) {
       count = 1;
-      pid = known_pid;
       only = list[0];
       known = false;
+    } else if (list) {
+      count = warp_legal_set<kConst>(p, w, ns, b, hdr.x, hdr.y, pid, lane, list);
+      __syncwarp();
+      if (count == 1) only = list[0];
     } else {
-      const int n = ns.node;
-      if (n < 0 || n >= p.g.n_nodes) break;  // the next step reports the bad index
-      const int beg = w.begin(n), end = w.begin(n + 1);
-      pid = w.ptr(n);
-      if (list) {
-        count = warp_legal_set<kConst>(p, w, ns, b, beg, end, pid, lane, list);
-        __syncwarp();
-        if (count == 1) only = list[0];
-      } else {
-        count = warp_count_legal<kConst>(p, w, ns, b, beg, end, pid, lane, only);
-      }
+      count = warp_count_legal<kConst>(p, w, ns, b, hdr.x, hdr.y, pid, lane, only);
     }
-    if (count != 1) {
+    if (count != 1) {  // (-1: an index out of range, which the next step reports)
       if (list) {
         list_n = count;
         list_pid = pid;
@@ -484,19 +490,21 @@ __device__ __forceinline__ void forced_chain(const StepParams& p, const WalkRd<k
       break;
     }
     if (lane == 0) {
-      p.tok_out[(size_t)b * p.out_stride + ns.len] = only.x;
+      p.tok_out[(size_t)b * p.out_stride + ns.len] = only.a.x;
       p.logit_out[(size_t)b * p.out_stride + ns.len] = __int_as_float(0x7fc00000);
     }
     ns.len += 1;
     ++forced;
-    if (only.z >= 0) {
-      ns.node = only.z;
+    if (only.a.z >= 0) {
+      ns.node = only.a.z;
+      hdr = only.h;
     } else {
       // A control edge is legal only at a terminal whose pointer is unspent.
       complete_pointer(p, b, pid, ns, lane, 32);
       ns.emitted += 1;
       ns.node = 0;
-      if (only.z == -2) ns.done = 1;
+      hdr = root_hdr(p);
+      if (only.a.z == -2) ns.done = 1;
       __syncwarp();  // decrements and the spent flag are seen by the next legal set
     }
   }
@@ -513,6 +521,7 @@ __device__ __forceinline__ int finish_sequence(const StepParams& p, const WalkRd
   int status = TC_OK;
   int32_t new_node = s.node, ptr_done = -1;
   bool stop = false;
+  int4 chain_hdr = make_int4(0, 0, -1, 0);  // header of the node after the transition (jump only)
   if (err) {
     status = TC_ERR_BOUNDS;
   } else if (ncand == 0) {
@@ -522,6 +531,7 @@ __device__ __forceinline__ int finish_sequence(const StepParams& p, const WalkRd
   } else {
     const SeqLive L = seq_live(p, s, b);
     const int4 ed = w.edge(best_e);
+    if (p.jump) chain_hdr = ed.y == -1 ? root_hdr(p) : w.child_hdr(best_e);
     if (ed.x != best_t) {
       status = TC_ERR_BOUNDS;
     } else if (ed.y >= 0) {
@@ -579,7 +589,7 @@ __device__ __forceinline__ int finish_sequence(const StepParams& p, const WalkRd
     if (chain) {
       __syncwarp();  // the spent flag set above
       int ln, lp;
-      forced_chain<kConst>(p, w, b, ns, lane, nullptr, false, 0, ln, lp);
+      forced_chain<kConst>(p, w, b, ns, lane, chain_hdr, nullptr, false, ln, lp);
     }
     if (lane == 0) {
       p.st[b] = ns;
@@ -773,10 +783,9 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
 // time, as "GLRMask" computes it in parallel with the forward pass).  After a
 // separator or a stop, or when a set does not fit, the next step filters.
 struct Step1Shared {
-  int4 cand[kPreMax];                 // {token, edge, child, live count} of this step's candidates
-  int4 spec[kPreMax][kPreMax];        // per candidate: its child's legal candidates
+  Cand cand[kPreMax];                 // this step's candidates
+  Cand spec[kPreMax][kPreMax];        // per candidate: its child's legal candidates
   int32_t spec_n[kPreMax];            // their number, -1 when not available
-  int32_t spec_pid[kPreMax];          // the child's pointer id
   float wl[kWarps];
   int32_t wt[kWarps], wslot[kWarps];
   int32_t ncand, err, pid, done_after;
@@ -792,7 +801,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
   // The state and this warp's first precomputed candidate are read together.
   const SeqState s = p.st[b];
-  const int4 pre0 = p.pre[(size_t)b * kPreMax + warp];
+  const Cand pre0 = p.pre[(size_t)b * kPreMax + warp];
   const int mode = seq_mode(p, s);
   const int nch = p.H >> 3;
   uint4* xs = reinterpret_cast<uint4*>(smem_raw);
@@ -809,7 +818,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
     } else {
       for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
     }
-    const bool pre = s.pad0 > 0;
+    const bool pre = s.pre_n > 0;
     if (!pre) {
       // Filter the node (fan-out <= 32: one warp).
       if (warp == 0) {
@@ -825,53 +834,47 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
         }
       }
     } else if (tid == 0) {
-      sh.ncand = s.pad0 - 1;
+      sh.ncand = s.pre_n - 1;
       sh.err = 0;
-      sh.pid = s.pad1;
+      sh.pid = s.pre_pid;
     }
     __syncthreads();
     const int n = sh.ncand;
     if (!sh.err) {
       for (int l = warp; l < n; l += kWarps) {
-        const int4 cd = pre ? (l == warp ? pre0 : p.pre[(size_t)b * kPreMax + l]) : sh.cand[l];
-        // child record first, then the row, then the child's edges
-        const bool spec = cd.z >= 0 && cd.z < p.g.n_nodes;
-        const int cc = spec ? cd.z : 0;
-        const int cb = w.begin(cc), ce = w.begin(cc + 1), cpid = w.ptr(cc);
-        const uint4* r4 = reinterpret_cast<const uint4*>(p.emb + (size_t)cd.x * p.H);
+        const Cand cd = pre ? (l == warp ? pre0 : p.pre[(size_t)b * kPreMax + l]) : sh.cand[l];
+        // The row, then the child's edges: the candidate carries the child's
+        // header, so no node header is read on this path.
+        const bool spec = cd.a.z >= 0 && cd.a.z < p.g.n_nodes;
+        const int cb = cd.h.x, ce = cd.h.y, cpid = cd.h.z;
+        const uint4* r4 = reinterpret_cast<const uint4*>(p.emb + (size_t)cd.a.x * p.H);
         float acc = 0.f;
         if constexpr (NCH > 0) {
           uint4 e[NCH];
 #pragma unroll
           for (int i = 0; i < NCH; ++i) e[i] = ld_row(r4 + i * 32 + lane);
           const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
-          if (lane == 0) {
-            sh.spec_n[l] = sn;
-            sh.spec_pid[l] = cpid;
-          }
+          if (lane == 0) sh.spec_n[l] = sn;
           __syncwarp();
           // If this candidate wins, its child's rows are the next step's reads: start them towards L2 now.
-          if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].x * p.H, (uint32_t)p.H * 2u);
+          if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].a.x * p.H, (uint32_t)p.H * 2u);
 #pragma unroll
           for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xf.v[i], acc);
         } else {
           const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
-          if (lane == 0) {
-            sh.spec_n[l] = sn;
-            sh.spec_pid[l] = cpid;
-          }
+          if (lane == 0) sh.spec_n[l] = sn;
           __syncwarp();
           // If this candidate wins, its child's rows are the next step's reads: start them towards L2 now.
-          if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].x * p.H, (uint32_t)p.H * 2u);
+          if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].a.x * p.H, (uint32_t)p.H * 2u);
           for (int c = lane; c < nch; c += 32) acc = dot8(ld_row(r4 + c), xs[c], acc);
         }
         const float v = warp_sum(acc);
         if (pre) {
           if (lane == 0) sh.cand[l] = cd;  // the winner's edge data is read from here below
         }
-        if (better(v, cd.x, wl, wt)) {
+        if (better(v, cd.a.x, wl, wt)) {
           wl = v;
-          wt = cd.x;
+          wt = cd.a.x;
           ws = l;
         }
       }
@@ -896,7 +899,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
     int status = TC_OK;
     int32_t new_node = s.node, ptr_done = -1;
     bool stop = false;
-    int4 win = make_int4(0, -1, 0, 0);
+    Cand win{make_int4(0, -1, 0, 0), make_int4(0, 0, -1, 0)};
     if (sh.err) {
       status = TC_ERR_BOUNDS;
     } else if (ncand == 0) {
@@ -905,16 +908,16 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
       status = TC_ERR_BOUNDS;  // no comparable logit (NaN)
     } else {
       win = sh.cand[bs];
-      if (win.z >= 0) {
-        if (win.w <= 0) status = TC_ERR_NO_LIVE_EDGE;  // live count read this step
-        else new_node = win.z;
+      if (win.a.z >= 0) {
+        if (win.a.w <= 0) status = TC_ERR_NO_LIVE_EDGE;  // live count read this step
+        else new_node = win.a.z;
       } else {
         const int32_t pid = sh.pid;
         if (!ptr_free(p, seq_live(p, s, b), pid)) {
           status = TC_ERR_NO_LIVE_EDGE;
         } else {
           ptr_done = pid;
-          stop = win.z == -2;
+          stop = win.a.z == -2;
           new_node = 0;
         }
       }
@@ -930,7 +933,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
     if (chain) __syncthreads();  // the decrements above are seen by the chain's legal sets
     if (warp == 0) {
       SeqState ns = s;
-      int pre_n = next_n, pre_pid = next_n >= 0 ? sh.spec_pid[bs] : -2;
+      int pre_n = next_n, pre_pid = next_n >= 0 ? win.h.z : -2;  // the child's pointer rank
       if (status != TC_OK) {
         ns.status = status;
         ns.done = 1;
@@ -962,20 +965,21 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
       if (chain) {
         __syncwarp();  // the spent flag set above
         // The winner's own (precomputed) list slot serves as the chain's scratch.
-        int4* list = sh.spec[bs];
-        forced_chain<kConst>(p, w, b, ns, lane, list, next_n == 1, sh.spec_pid[bs], pre_n, pre_pid);
+        Cand* list = sh.spec[bs];
+        const int4 hdr = ptr_done >= 0 ? root_hdr(p) : win.h;
+        forced_chain<kConst>(p, w, b, ns, lane, hdr, list, next_n == 1, pre_n, pre_pid);
         if (pre_n > 0 && lane < pre_n) {
           p.pre[(size_t)b * kPreMax + lane] = list[lane];
-          prefetch_l2(p.emb + (size_t)list[lane].x * p.H, (uint32_t)p.H * 2u);
+          prefetch_l2(p.emb + (size_t)list[lane].a.x * p.H, (uint32_t)p.H * 2u);
         }
         if (lane == 0 && !ns.done && ns.len < p.max_steps)
           prefetch_l2(p.hidden + ((size_t)ns.len * p.B + b) * p.H, (uint32_t)p.H * 2u);
       }
       if (ns.status == TC_OK) {
-        ns.pad0 = pre_n >= 0 ? pre_n + 1 : 0;
-        ns.pad1 = pre_n >= 0 ? pre_pid : -2;
+        ns.pre_n = pre_n >= 0 ? pre_n + 1 : 0;
+        ns.pre_pid = pre_n >= 0 ? pre_pid : -2;
       } else {
-        ns.pad0 = 0;
+        ns.pre_n = 0;
       }
       if (lane == 0) {
         p.st[b] = ns;

@@ -28,15 +28,20 @@ struct tc_trie {
 namespace tcd {
 
 // Device walk image, int32 words:
-//   node_begin[N+1] | pad to a multiple of 4 | edges {tok, child, lo, n}[E] | node_rank[N]
-// where {lo, n} is the range of pointer ranks below a token edge (or the
-// terminal's own rank and n = 1 for a control edge) and node_rank is the rank
-// of the node's pointer or -1.  On the device a pointer is named by its rank.
+//   header:  node_begin[N+1] | node_rank[N]            (the part copied to constant memory)
+//   pad to a multiple of 8 words
+//   edges:   {tok, child, lo, n, cbeg, cend, cpid, 0}[E]
+// {lo, n} is the range of pointer ranks below a token edge (the terminal's own
+// rank and 1 for a control edge); {cbeg, cend, cpid} is the header of the
+// edge's child (the root's for a separator, zeros for stop), so a walk never
+// needs a node header lookup.  node_rank is the rank of the node's pointer or
+// -1; on the device a pointer is named by its rank.
 struct WalkLayout {
   int32_t n_nodes, n_edges;
-  int32_t off_edges;   // word offset of the edge records (multiple of 4: 16-byte records)
-  int32_t off_ptr;     // word offset of node_rank
-  int32_t words;       // total words
+  int32_t off_ptr;        // word offset of node_rank
+  int32_t header_words;   // words of the header part
+  int32_t off_edges;      // word offset of the edge records (multiple of 8: 32-byte records)
+  int32_t words;          // total words
 };
 WalkLayout walk_layout(int32_t n_nodes, int32_t n_edges);
 std::vector<int32_t> build_walk_image(const tc_trie& t, const WalkLayout& L);

@@ -24,24 +24,37 @@ WalkLayout walk_layout(int32_t n_nodes, int32_t n_edges) {
   WalkLayout L;
   L.n_nodes = n_nodes;
   L.n_edges = n_edges;
-  L.off_edges = (n_nodes + 1 + 3) & ~3;  // keep the {tok, child, lo, n} records 16-byte aligned
-  L.off_ptr = L.off_edges + 4 * n_edges;
-  L.words = L.off_ptr + n_nodes;
+  L.off_ptr = n_nodes + 1;
+  L.header_words = 2 * n_nodes + 1;
+  L.off_edges = (L.header_words + 7) & ~7;  // 32-byte aligned edge records
+  L.words = L.off_edges + 8 * n_edges;
   return L;
 }
 
 std::vector<int32_t> build_walk_image(const tc_trie& t, const WalkLayout& L) {
   std::vector<int32_t> img((size_t)L.words, 0);
   std::copy(t.node_begin.begin(), t.node_begin.end(), img.begin());
+  auto rank_of = [&](int32_t n) { return t.node_ptr[n] >= 0 ? t.ptr_rank[t.node_ptr[n]] : -1; };
+  for (int32_t n = 0; n < L.n_nodes; ++n) img[(size_t)L.off_ptr + n] = rank_of(n);
   for (int32_t e = 0; e < L.n_edges; ++e) {
-    int32_t* r = img.data() + L.off_edges + 4 * (size_t)e;
+    int32_t* r = img.data() + L.off_edges + 8 * (size_t)e;
+    const int32_t c = t.edge_child[e];
     r[0] = t.edge_tok[e];
-    r[1] = t.edge_child[e];
+    r[1] = c;
     r[2] = t.edge_lo[e];
-    r[3] = t.edge_child[e] >= 0 ? t.static_cnt[e] : 1;
+    r[3] = c >= 0 ? t.static_cnt[e] : 1;
+    if (c >= 0) {
+      r[4] = t.node_begin[c];
+      r[5] = t.node_begin[c + 1];
+      r[6] = rank_of(c);
+    } else if (c == -1) {  // separator: back to the root
+      r[4] = t.node_begin[0];
+      r[5] = t.node_begin[1];
+      r[6] = rank_of(0);
+    } else {
+      r[6] = -1;
+    }
   }
-  for (int32_t n = 0; n < L.n_nodes; ++n)
-    img[(size_t)L.off_ptr + n] = t.node_ptr[n] >= 0 ? t.ptr_rank[t.node_ptr[n]] : -1;
   return img;
 }
 
@@ -295,7 +308,9 @@ extern "C" tc_status tc_trie_info(const tc_trie* t, tc_trie_info_t* out) {
   out->sep_id = t->sep;
   out->stop_id = t->stop;
   out->total_tokens = t->total_tokens;
-  out->walk_image_bytes = (int64_t)walk_layout(t->n_nodes(), t->n_edges()).words * 4;
+  const WalkLayout L = walk_layout(t->n_nodes(), t->n_edges());
+  out->walk_image_bytes = (int64_t)L.words * 4;
+  out->header_bytes = L.header_words * 4;
   return TC_OK;
 }
 
