@@ -18,10 +18,12 @@ Modules:
   lower-id tie-break argmax, and the dense-logits-then-mask baseline.
 * ``oracle.decode``   - the greedy decode loop, the host replay check and the
   teacher-forcing comparison used for floating-point parity.
+* ``oracle.sample``   - sampling with temperature, top-k and top-p and their
+  tie rules, the sampling decode loop and its teacher-forcing checker.
 
 Every function is pinned by a ``-m "not gpu"`` test against something other
 than itself (brute-force enumeration, exact integer arithmetic, constructed
 ties, hand-derived fixtures under ``tests/golden/``).
 """
 
-from . import language, grammar, head, decode  # noqa: F401
+from . import language, grammar, head, decode, sample  # noqa: F401
