@@ -608,6 +608,33 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
                                                         "a jump-forward step is one head decision plus the "
                                                         "forced span after it")
 
+    # --- sampling (temperature 1, top-p 0.9) against the greedy argmax, same queries
+    if head == tcd.HEAD_SPARSE and max_fanout <= 32:
+        n_s = min(len(qids), 500 if B == 1 else 16)
+        uq = {q: torch.from_numpy(w.uniforms(q * B, B)).to(f"cuda:{dev}") for q in sorted(set(qids[:n_s]))}
+        rates = {}
+        for name in ("greedy", "sampling"):
+            steps = 0
+            evs = []
+            for q in qids[:n_s]:
+                hid_buf.copy_(dev_hidden[q])
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if name == "greedy":
+                    ctx.decode(hid_buf, w.k, S, toks, logits, lens, status, head=head)
+                else:
+                    ctx.decode_sample(hid_buf, w.k, S, uq[q], toks, logits, lens, status, temperature=1.0,
+                                      top_k=0, top_p=0.9, head=head)
+                e1.record(stream)
+                evs.append((e0, e1))
+                steps += int((lens + (status != 0).int()).max().item())
+            torch.cuda.synchronize()
+            ms = sum(x.elapsed_time(y) for x, y in evs)
+            rates[name] = {"steps_per_s": steps / (ms / 1000.0)}
+        out["sampling"] = dict(rates, note=f"{n_s} query batches, L2 flushed before each decode; sampling: "
+                                           "temperature 1, top-p 0.9, seeded uniforms")
+
     # --- loop floor: the same graph loop with do-nothing kernels in the steps' place
     fl_ms, fl_n = tcd.loop_floor(dev, B, 256)
     out["loop_floor_us_per_launch"] = fl_ms * 1000.0 / fl_n

@@ -286,6 +286,46 @@ tc_status tc_decode(tc_ctx* ctx, const void* hidden_steps_bf16, int32_t n_steps,
                     int32_t* lens, int32_t* status, void* stream);
 
 /*
+ * Sampling instead of the greedy argmax ("Understanding Inference for Systems
+ * Engineers", section 3.8): the token is drawn from softmax(logit /
+ * temperature) over the legal candidates, restricted first to the top_k
+ * highest logits - a value threshold, so every candidate tied with the top_k-th
+ * largest logit is kept - and then by removing the ascending prefix, in
+ * (logit, token id) order, whose probability mass is at most 1 - top_p (the
+ * largest is never removed, so among equal probabilities the highest id
+ * survives).  The draw is the first kept candidate, in ascending token order,
+ * whose cumulative probability exceeds the caller's uniform u in [0, 1).
+ * top_k = 0 and top_p = 1 switch the restrictions off.  Sums run in a fixed
+ * order, so a draw depends only on the sequence's own inputs.
+ */
+typedef struct tc_sampling_t {
+  float temperature;  /* > 0, finite */
+  int32_t top_k;      /* >= 0; 0: no top-k */
+  float top_p;        /* in [0, 1]; 1: no top-p */
+} tc_sampling_t;
+
+/*
+ * tc_decode_sample - tc_decode with sampling.  uniforms (device) float[batch,
+ * max_steps]: the uniform of sequence b at output position t is
+ * uniforms[b * max_steps + t] (positions filled by forced continuations use
+ * none).  Sparse head only (TC_FLAG_JUMP_FORWARD may be or-ed in), on grammars
+ * whose nodes have at most 32 edges: TC_ERR_UNSUPPORTED otherwise.  The
+ * random numbers are the caller's: the library generates none.
+ */
+tc_status tc_decode_sample(tc_ctx* ctx, const void* hidden_steps_bf16, int32_t n_steps, int32_t batch,
+                           int32_t k, int32_t max_steps, int32_t head, const tc_sampling_t* sampling,
+                           const float* uniforms, int32_t* toks, float* logits, int32_t* lens,
+                           int32_t* status, void* stream);
+
+/*
+ * tc_step_sample - tc_step with sampling; uniforms (device) float[batch], one
+ * per sequence for this step.  Same restrictions as tc_decode_sample.
+ */
+tc_status tc_step_sample(tc_ctx* ctx, const void* hidden_bf16, int32_t head, const tc_sampling_t* sampling,
+                         const float* uniforms, int32_t* tok_out, float* logit_out, int32_t* status_out,
+                         void* stream);
+
+/*
  * tc_decode_host - the same decode driven from the host: tc_reset, then one
  * tc_step per step with a synchronising read of the live count after each,
  * the comparison loop of "The whole loop on the device".  Same arguments and

@@ -47,6 +47,11 @@ class _TrieInfo(ctypes.Structure):
                 ("walk_image_bytes", ctypes.c_int64)]
 
 
+class Sampling(ctypes.Structure):
+    """tc_sampling_t: temperature > 0, top_k >= 0 (0: off), top_p in [0, 1] (1: off)."""
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+
+
 def _decl(name, restype, argtypes):
     f = getattr(_lib, name)
     f.restype = restype
@@ -77,6 +82,11 @@ _graph_destroy = _decl("tc_graph_destroy", None, [_vp])
 _first_error = _decl("tc_first_error", ctypes.c_int, [_vp, _vp, _i32p, _i32p])
 _read_state = _decl("tc_read_seq_state", ctypes.c_int, [_vp, _vp] + [_i32p] * 5)
 _read_stats = _decl("tc_read_stats", ctypes.c_int, [_vp, _vp, _i64p, ctypes.c_int32])
+_decode_sample = _decl("tc_decode_sample", ctypes.c_int,
+                       [_vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                        ctypes.POINTER(Sampling), _vp, _vp, _vp, _vp, _vp, _vp])
+_step_sample = _decl("tc_step_sample", ctypes.c_int, [_vp, _vp, ctypes.c_int32, ctypes.POINTER(Sampling), _vp, _vp,
+                                                      _vp, _vp, _vp])
 _loop_floor = _decl("tc_loop_floor", ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
                                                     ctypes.POINTER(ctypes.c_float), _i64p])
 _status_str = _decl("tc_status_str", ctypes.c_char_p, [ctypes.c_int])
@@ -220,6 +230,22 @@ class Context:
     def decode(self, hidden_steps, k, max_steps, toks, logits, lens, status, head=HEAD_SPARSE, stream=None):
         _check(_decode(*self._dargs(hidden_steps, k, max_steps, head, toks, logits, lens, status),
                        _stream_ptr(stream)), "tc_decode")
+
+    def decode_sample(self, hidden_steps, k, max_steps, uniforms, toks, logits, lens, status, temperature=1.0,
+                      top_k=0, top_p=1.0, head=HEAD_SPARSE, stream=None):
+        """tc_decode_sample: uniforms is a device float32 [batch, max_steps] tensor."""
+        S, B, H = hidden_steps.shape
+        sp = Sampling(float(temperature), int(top_k), float(top_p))
+        _check(_decode_sample(self._h, hidden_steps.data_ptr(), S, B, k, max_steps, head, ctypes.byref(sp),
+                              uniforms.data_ptr(), toks.data_ptr(), logits.data_ptr(), lens.data_ptr(),
+                              status.data_ptr(), _stream_ptr(stream)), "tc_decode_sample")
+
+    def step_sample(self, hidden, uniforms, tok_out, logit_out=None, status_out=None, temperature=1.0, top_k=0,
+                    top_p=1.0, head: int = HEAD_SPARSE, stream=None):
+        sp = Sampling(float(temperature), int(top_k), float(top_p))
+        _check(_step_sample(self._h, hidden.data_ptr(), head, ctypes.byref(sp), uniforms.data_ptr(),
+                            tok_out.data_ptr(), _ptr(logit_out), _ptr(status_out), _stream_ptr(stream)),
+               "tc_step_sample")
 
     def decode_host(self, hidden_steps, k, max_steps, toks, logits, lens, status, head=HEAD_SPARSE, stream=None):
         _check(_decode_host(*self._dargs(hidden_steps, k, max_steps, head, toks, logits, lens, status),

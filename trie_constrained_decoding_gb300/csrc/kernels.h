@@ -129,6 +129,12 @@ struct StepParams {
   Cand* pre;                // [B, 32] precomputed candidate lists (one-CTA sparse step), or null
   int32_t jump;             // 1: emit forced tokens without the head after each decision (device form only)
   int32_t iv;               // 1: read-only no-repeat state (rank ranges + banned ranks); 0: cnt/spent arrays
+  // Sampling instead of the argmax (one-CTA sparse step only)
+  int32_t smp;              // 1: sample
+  float inv_temp;           // 1 / temperature
+  int32_t top_k;            // <= 0: off
+  float top_p;              // >= 1: off
+  const float* u;           // uniforms: device form [b * out_stride + position], host form [b]
 };
 
 // Cumulative counters kept by the kernels (one atomic per launch / per sequence step).

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -118,15 +119,28 @@ struct DevGrammar {
   }
 };
 
+// Sampling arguments as the kernels take them (smp = 0: greedy).
+struct SampleArgs {
+  int32_t smp = 0;
+  float inv_temp = 1.f;
+  int32_t top_k = 0;
+  float top_p = 1.f;
+  const float* u = nullptr;
+  bool operator==(const SampleArgs& o) const {
+    return smp == o.smp && (!smp || (inv_temp == o.inv_temp && top_k == o.top_k && top_p == o.top_p && u == o.u));
+  }
+};
+
 struct GraphKey {
   const DevGrammar* g;
   const void* hidden;
   int32_t n_steps, batch, k, max_steps, head;
   void *toks, *logits, *lens, *status;
+  SampleArgs smp;
   bool operator==(const GraphKey& o) const {
     return g == o.g && hidden == o.hidden && n_steps == o.n_steps && batch == o.batch && k == o.k &&
            max_steps == o.max_steps && head == o.head && toks == o.toks && logits == o.logits &&
-           lens == o.lens && status == o.status;
+           lens == o.lens && status == o.status && smp == o.smp;
   }
 };
 
@@ -348,6 +362,40 @@ tc_status check_decode_args(tc_ctx* c, const void* hidden, int32_t n_steps, int3
   return check_head(c, head, batch);
 }
 
+void apply_sampling(StepParams& p, const SampleArgs& a) {
+  p.smp = a.smp;
+  p.inv_temp = a.inv_temp;
+  p.top_k = a.top_k;
+  p.top_p = a.top_p;
+  p.u = a.u;
+}
+
+// Sampling runs in the one-CTA sparse step (grammars whose nodes have at most
+// 32 edges); temperature > 0 and finite, top_k >= 0, top_p in [0, 1].
+tc_status check_sampling(const tc_ctx* c, const DevGrammar* g, int head, const tc_sampling_t* sp, const float* u,
+                         SampleArgs* out) {
+  (void)c;
+  if (!sp || !u || misaligned(u, 4)) {
+    set_error_message("sampling: parameters and 4-byte aligned uniforms are required");
+    return TC_ERR_INVALID_ARG;
+  }
+  if (!(sp->temperature > 0.f) || !std::isfinite(sp->temperature) || sp->top_k < 0 || !(sp->top_p >= 0.f) ||
+      sp->top_p > 1.f) {
+    set_error_message("sampling: temperature must be positive and finite, top_k >= 0, 0 <= top_p <= 1");
+    return TC_ERR_INVALID_ARG;
+  }
+  if ((head & ~TC_FLAG_JUMP_FORWARD) != TC_HEAD_SPARSE || !g || !one_cta_sparse(g)) {
+    set_error_message("sampling: sparse head on grammars whose nodes have at most 32 edges");
+    return TC_ERR_UNSUPPORTED;
+  }
+  out->smp = 1;
+  out->inv_temp = 1.f / sp->temperature;
+  out->top_k = sp->top_k;
+  out->top_p = sp->top_p;
+  out->u = u;
+  return TC_OK;
+}
+
 void destroy_graph(tc_graph* gr) {
   if (!gr) return;
   if (gr->exec) cudaGraphExecDestroy(gr->exec);
@@ -435,6 +483,7 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
   p.device_form = 1;
   p.jump = (key.head & TC_FLAG_JUMP_FORWARD) ? 1 : 0;
   p.iv = r.iv;
+  apply_sampling(p, key.smp);
   const int head = key.head & ~TC_FLAG_JUMP_FORWARD;
   // The body runs kLoopUnroll steps; only the last sets the loop condition.
   // A sequence that has stopped makes the remaining steps of the body no-ops.
@@ -658,8 +707,10 @@ extern "C" tc_status tc_reset(tc_ctx* c, int32_t batch, int32_t k, void* stream)
   return TC_OK;
 }
 
-extern "C" tc_status tc_step(tc_ctx* c, const void* hidden, int32_t head, int32_t* tok_out, float* logit_out,
-                             int32_t* status_out, void* stream) {
+namespace {
+
+tc_status step_impl(tc_ctx* c, const void* hidden, int32_t head, const tc_sampling_t* sp, const float* u,
+                    int32_t* tok_out, float* logit_out, int32_t* status_out, void* stream) {
   if (!c || !hidden || !tok_out) return TC_ERR_INVALID_ARG;
   if (misaligned(hidden, 16) || misaligned(tok_out, 4) || misaligned(logit_out, 4) || misaligned(status_out, 4)) {
     set_error_message("tc_step: hidden states must be 16-byte aligned and outputs 4-byte aligned");
@@ -680,8 +731,28 @@ extern "C" tc_status tc_step(tc_ctx* c, const void* hidden, int32_t head, int32_
   p.logit_out = logit_out;
   p.status_out = status_out;
   p.out_stride = 1;
+  if (sp || u) {
+    SampleArgs smp;
+    rc = check_sampling(c, g, head, sp, u, &smp);
+    if (rc != TC_OK) return rc;
+    apply_sampling(p, smp);
+  }
   TC_CUDA(launch_any_step(c, g, p, head, s, false));
   return TC_OK;
+}
+
+}  // namespace
+
+extern "C" tc_status tc_step(tc_ctx* c, const void* hidden, int32_t head, int32_t* tok_out, float* logit_out,
+                             int32_t* status_out, void* stream) {
+  return step_impl(c, hidden, head, nullptr, nullptr, tok_out, logit_out, status_out, stream);
+}
+
+extern "C" tc_status tc_step_sample(tc_ctx* c, const void* hidden, int32_t head, const tc_sampling_t* sampling,
+                                    const float* uniforms, int32_t* tok_out, float* logit_out, int32_t* status_out,
+                                    void* stream) {
+  if (!sampling || !uniforms) return TC_ERR_INVALID_ARG;
+  return step_impl(c, hidden, head, sampling, uniforms, tok_out, logit_out, status_out, stream);
 }
 
 extern "C" tc_status tc_decode_graph_create(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch,
@@ -692,7 +763,7 @@ extern "C" tc_status tc_decode_graph_create(tc_ctx* c, const void* hidden, int32
   tc_status rc = check_decode_args(c, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status);
   if (rc != TC_OK) return rc;
   DeviceGuard dg(c->device);
-  GraphKey key{c->bound, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status};
+  GraphKey key{c->bound, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status, SampleArgs{}};
   tc_graph* gr = nullptr;
   rc = build_graph(c, c->bound, key, &gr);
   if (rc != TC_OK) return rc;
@@ -716,13 +787,20 @@ extern "C" void tc_graph_destroy(tc_graph* gr) {
   destroy_graph(gr);
 }
 
-extern "C" tc_status tc_decode(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch, int32_t k,
-                               int32_t max_steps, int32_t head, int32_t* toks, float* logits, int32_t* lens,
-                               int32_t* status, void* stream) {
+namespace {
+
+tc_status decode_impl(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch, int32_t k, int32_t max_steps,
+                      int32_t head, const tc_sampling_t* sp, const float* u, int32_t* toks, float* logits,
+                      int32_t* lens, int32_t* status, void* stream) {
   tc_status rc = check_decode_args(c, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status);
   if (rc != TC_OK) return rc;
+  SampleArgs smp;
+  if (sp || u) {
+    rc = check_sampling(c, c->bound, head, sp, u, &smp);
+    if (rc != TC_OK) return rc;
+  }
   DeviceGuard dg(c->device);
-  GraphKey key{c->bound, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status};
+  GraphKey key{c->bound, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status, smp};
   tc_graph* gr = nullptr;
   for (size_t i = 0; i < c->cache.size(); ++i) {
     if (c->cache[i]->key == key) {
@@ -745,6 +823,24 @@ extern "C" tc_status tc_decode(tc_ctx* c, const void* hidden, int32_t n_steps, i
     c->cache.push_back(gr);
   }
   return launch_graph(gr, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" tc_status tc_decode(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch, int32_t k,
+                               int32_t max_steps, int32_t head, int32_t* toks, float* logits, int32_t* lens,
+                               int32_t* status, void* stream) {
+  return decode_impl(c, hidden, n_steps, batch, k, max_steps, head, nullptr, nullptr, toks, logits, lens, status,
+                     stream);
+}
+
+extern "C" tc_status tc_decode_sample(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch, int32_t k,
+                                      int32_t max_steps, int32_t head, const tc_sampling_t* sampling,
+                                      const float* uniforms, int32_t* toks, float* logits, int32_t* lens,
+                                      int32_t* status, void* stream) {
+  if (!sampling || !uniforms) return TC_ERR_INVALID_ARG;
+  return decode_impl(c, hidden, n_steps, batch, k, max_steps, head, sampling, uniforms, toks, logits, lens, status,
+                     stream);
 }
 
 extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t batch, int32_t k,

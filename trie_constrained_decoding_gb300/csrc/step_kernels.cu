@@ -786,10 +786,69 @@ struct Step1Shared {
   Cand cand[kPreMax];                 // this step's candidates
   Cand spec[kPreMax][kPreMax];        // per candidate: its child's legal candidates
   int32_t spec_n[kPreMax];            // their number, -1 when not available
+  float lg[kPreMax];                  // candidate logits (sampling)
   float wl[kWarps];
   int32_t wt[kWarps], wslot[kWarps];
-  int32_t ncand, err, pid, done_after;
+  int32_t ncand, err, pid, done_after, smp_slot, smp_nan;
 };
+
+// Sampling over one sequence's candidates ("Understanding Inference for
+// Systems Engineers", section 3.8): softmax of logit / temperature, restricted
+// first to the top-k highest logits - a value threshold, so tied logits are
+// all kept - then by removing the ascending prefix, in (logit, token) order,
+// whose probability mass is at most 1 - top-p (the largest is never removed,
+// so among equal probabilities the highest id survives); the token is the
+// first kept candidate in ascending token order whose cumulative weight
+// exceeds u times the kept total.  One warp, n <= 32 candidates in ascending
+// token order, lane i holding candidate i; every sum runs in a fixed order.
+// Returns the chosen slot, or -1 with nan = 1 when a logit is NaN.
+__device__ __forceinline__ int warp_sample(const StepParams& p, const float* lg, const Cand* cand, int n, float u,
+                                           int lane, int& nan) {
+  const bool act = lane < n;
+  const float l = act ? lg[lane] : 0.f;
+  const int32_t tok = act ? cand[lane].a.x : INT_MAX;
+  nan = __any_sync(kFull, act && !(l == l)) ? 1 : 0;
+  if (nan) return -1;
+  int kept = act ? 1 : 0;
+  if (p.top_k > 0 && p.top_k < n) {
+    int greater = 0;
+    for (int j = 0; j < 32; ++j) {
+      const float lj = __shfl_sync(kFull, l, j);
+      greater += (j < n && lj > l) ? 1 : 0;
+    }
+    kept = (act && greater < p.top_k) ? 1 : 0;
+  }
+  float m = kept ? l : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  float wgt = kept ? expf((l - m) * p.inv_temp) : 0.f;
+  if (p.top_p < 1.f) {
+    float total = 0.f, run = 0.f;
+    int larger = 0;
+    for (int j = 0; j < 32; ++j) {
+      const float lj = __shfl_sync(kFull, l, j);
+      const int32_t tj = __shfl_sync(kFull, tok, j);
+      const float wj = __shfl_sync(kFull, wgt, j);
+      const int kj = __shfl_sync(kFull, kept, j);
+      total += wj;
+      if (kj && (lj < l || (lj == l && tj <= tok))) run += wj;
+      if (kj && (lj > l || (lj == l && tj > tok))) larger = 1;
+    }
+    if (kept && larger && run <= (1.f - p.top_p) * total) kept = 0;
+    if (!kept) wgt = 0.f;
+  }
+  float pre = wgt;  // inclusive prefix in lane (ascending token) order
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v = __shfl_up_sync(kFull, pre, o);
+    if (lane >= o) pre += v;
+  }
+  const float target = u * __shfl_sync(kFull, pre, 31);
+  const unsigned hit = __ballot_sync(kFull, kept && pre > target);
+  const unsigned any = __ballot_sync(kFull, kept);
+  if (hit) return __ffs(hit) - 1;
+  return any ? 31 - __clz(any) : -1;
+}
 
 template <bool kConst, int NCH>
 __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams p) {
@@ -869,8 +928,9 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
           for (int c = lane; c < nch; c += 32) acc = dot8(ld_row(r4 + c), xs[c], acc);
         }
         const float v = warp_sum(acc);
-        if (pre) {
-          if (lane == 0) sh.cand[l] = cd;  // the winner's edge data is read from here below
+        if (lane == 0) {
+          if (pre) sh.cand[l] = cd;  // the winner's edge data is read from here below
+          if (p.smp) sh.lg[l] = v;
         }
         if (better(v, cd.a.x, wl, wt)) {
           wl = v;
@@ -888,13 +948,37 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
   if (p.stats && tid == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
   __syncthreads();
 
+  if (mode == 1 && p.smp) {  // (uniform over the CTA: one sequence)
+    if (warp == 0) {
+      int nan = 0, slot = -1;
+      if (!sh.err && sh.ncand > 0) {
+        const float u = p.device_form ? p.u[(size_t)b * p.out_stride + s.len] : p.u[b];
+        slot = warp_sample(p, sh.lg, sh.cand, sh.ncand, u, lane, nan);
+      }
+      if (lane == 0) {
+        sh.smp_slot = slot;
+        sh.smp_nan = nan;
+      }
+    }
+    __syncthreads();
+  }
+
   if (mode == 1) {
-    // Every thread folds the eight warp bests (same order, same result).
+    // Every thread folds the eight warp bests (same order, same result), or
+    // takes the sampled slot.
     float bl = -INFINITY;
     int32_t bt = INT_MAX, bs = -1;
+    if (p.smp) {
+      bs = sh.smp_slot;
+      if (bs >= 0) {
+        bl = sh.smp_nan ? __int_as_float(0x7fc00000) : sh.lg[bs];
+        bt = sh.cand[bs].a.x;
+      }
+    } else {
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i)
-      if (better(sh.wl[i], sh.wt[i], bl, bt)) { bl = sh.wl[i]; bt = sh.wt[i]; bs = sh.wslot[i]; }
+      for (int i = 0; i < kWarps; ++i)
+        if (better(sh.wl[i], sh.wt[i], bl, bt)) { bl = sh.wl[i]; bt = sh.wt[i]; bs = sh.wslot[i]; }
+    }
     const int ncand = sh.ncand;
     int status = TC_OK;
     int32_t new_node = s.node, ptr_done = -1;

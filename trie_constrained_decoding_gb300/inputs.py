@@ -25,7 +25,7 @@ import numpy as np
 MASTER_SEED = 20261202
 
 # Sub-seed slots derived from the master seed with SeedSequence.spawn.
-_SLOT_CATALOG, _SLOT_EMBEDDING, _SLOT_HIDDEN, _SLOT_ORDER = range(4)
+_SLOT_CATALOG, _SLOT_EMBEDDING, _SLOT_HIDDEN, _SLOT_ORDER, _SLOT_UNIFORM = range(5)
 
 
 def sub_seed(slot: int, master: int = MASTER_SEED, extra: int = 0) -> np.random.SeedSequence:
@@ -266,6 +266,16 @@ class Workload:
                 out[:, i, :] = integer_bf16(rng, (steps, self.hidden))
             else:
                 out[:, i, :] = gaussian_bf16(rng, (steps, self.hidden), self.hid_std)
+        return out
+
+    def uniforms(self, query0: int, n_queries: int, steps: Optional[int] = None) -> np.ndarray:
+        """float32 [n_queries, steps] in [0, 1): the sampling draws of each
+        (query, position), seeded per query like the hidden states."""
+        steps = self.max_steps if steps is None else steps
+        out = np.empty((n_queries, steps), dtype=np.float32)
+        for i in range(n_queries):
+            rng = rng_for(_SLOT_UNIFORM, self.seed, extra=(query0 + i) * 16 + 3)
+            out[i] = rng.random(steps, dtype=np.float32)
         return out
 
     def order_rng(self, extra: int = 0) -> np.random.Generator:
