@@ -20,10 +20,13 @@ Modules:
   teacher-forcing comparison used for floating-point parity.
 * ``oracle.sample``   - sampling with temperature, top-k and top-p and their
   tie rules, the sampling decode loop and its teacher-forcing checker.
+* ``oracle.chars``    - the character-level constraint over a byte vocabulary
+  (every tokenization of a catalog string accepted), from its definition, and
+  brute-force enumeration of its language.
 
 Every function is pinned by a ``-m "not gpu"`` test against something other
 than itself (brute-force enumeration, exact integer arithmetic, constructed
 ties, hand-derived fixtures under ``tests/golden/``).
 """
 
-from . import language, grammar, head, decode, sample  # noqa: F401
+from . import language, grammar, head, decode, sample, chars  # noqa: F401

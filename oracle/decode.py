@@ -29,6 +29,15 @@ import numpy as np
 from .grammar import PrefixTrie, WalkState, advance, legal_tokens, walk
 from .head import abs_mass, argmax_lower_id, candidate_logits, dense_masked_argmax
 
+
+def walk_fns(grammar):
+    """(start, legal, advance) of a grammar: the token trie's walk, or the
+    grammar object's own (oracle.chars.CharGrammar)."""
+    if hasattr(grammar, "legal"):
+        return grammar.start, grammar.legal, grammar.advance
+    return (WalkState, lambda st, k: legal_tokens(grammar, st, k),
+            lambda st, tok, k: advance(grammar, st, tok, k))
+
 # Tolerances for Gaussian inputs: chosen logits within 1e-3 relative; a token
 # may differ from the oracle's argmax only when the oracle's own top-2 margin
 # is below 1e-5 relative.  Near zero, "relative" is taken against
@@ -49,17 +58,18 @@ def greedy_decode(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
     ``jump=True`` takes forced tokens without the head: from the second
     position on, a position whose legal set holds one token emits it with a
     NaN logit and computes nothing (the first token always comes from the head)."""
-    st = WalkState()
+    start, legal_of, step = walk_fns(trie)
+    st = start()
     toks: List[int] = []
     logits: List[float] = []
     for t in range(max_steps):
-        legal = legal_tokens(trie, st, k)
+        legal = legal_of(st, k)
         if not legal:
             return toks, logits, "empty_mask"
         if jump and t > 0 and len(legal) == 1:
             toks.append(legal[0])
             logits.append(float("nan"))
-            st = advance(trie, st, legal[0], k)
+            st = step(st, legal[0], k)
             if st.done:
                 return toks, logits, "ok"
             continue
@@ -69,7 +79,7 @@ def greedy_decode(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
             tok, lg = argmax_lower_id(legal, candidate_logits(emb_bits, hidden_bits[t], legal))
         toks.append(tok)
         logits.append(lg)
-        st = advance(trie, st, tok, k)
+        st = step(st, tok, k)
         if st.done:
             return toks, logits, "ok"
     return toks, logits, "max_steps"
@@ -78,19 +88,25 @@ def greedy_decode(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
 def forced_positions(trie: PrefixTrie, tokens: Sequence[int], k: int) -> List[int]:
     """Positions t >= 1 of a walkable output whose legal set holds exactly one
     token (where a forced-span decode emits without the head)."""
-    st = WalkState()
+    start, legal_of, step = walk_fns(trie)
+    st = start()
     out = []
     for t, tok in enumerate(tokens):
-        if t > 0 and len(legal_tokens(trie, st, k)) == 1:
+        if t > 0 and len(legal_of(st, k)) == 1:
             out.append(t)
-        st = advance(trie, st, int(tok), k)
+        st = step(st, int(tok), k)
     return out
 
 
 def replay_ok(trie: PrefixTrie, tokens: Sequence[int], k: int) -> bool:
     """Host replay: every token walkable and the string ends with the stop token."""
-    st = walk(trie, tokens, k)
-    return st is not None and st.done
+    start, legal_of, step = walk_fns(trie)
+    st = start()
+    for t in tokens:
+        if int(t) not in legal_of(st, k):
+            return False
+        st = step(st, int(t), k)
+    return st.done
 
 
 def parse_pointers(trie: PrefixTrie, tokens: Sequence[int]) -> List[int]:
@@ -133,10 +149,11 @@ def teacher_force(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
     token must carry a NaN logit (forced, no head read) and every other
     position a real one."""
     rep = ForcingReport()
-    st = WalkState()
+    start, legal_of, step = walk_fns(trie)
+    st = start()
     for t, (g_tok, g_log) in enumerate(zip(toks, logits)):
         rep.steps += 1
-        legal = legal_tokens(trie, st, k)
+        legal = legal_of(st, k)
         if g_tok not in legal:
             rep.fail(f"step {t}: token {g_tok} not legal (legal={legal[:8]}...)")
             return rep
@@ -146,7 +163,7 @@ def teacher_force(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
                 rep.fail(f"step {t}: forced={forced} but logit {float(g_log)!r}")
                 return rep
             if forced:
-                st = advance(trie, st, int(g_tok), k)
+                st = step(st, int(g_tok), k)
                 if st.done and t != len(toks) - 1:
                     rep.fail(f"step {t}: tokens continue after stop")
                     return rep
@@ -174,7 +191,7 @@ def teacher_force(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
                              f"(logit {best_l}); margin {best_l - r:g} above tolerance")
                 else:
                     rep.flips += 1
-        st = advance(trie, st, int(g_tok), k)
+        st = step(st, int(g_tok), k)
         if st.done and t != len(toks) - 1:
             rep.fail(f"step {t}: tokens continue after stop")
             return rep
@@ -186,7 +203,7 @@ def teacher_force(trie: PrefixTrie, k: int, emb_bits: np.ndarray, hidden_bits: n
         if st.done or n != max_steps:
             rep.fail(f"status max_steps but done={st.done}, len={n}, max_steps={max_steps}")
     elif status == "empty_mask":
-        if st.done or legal_tokens(trie, st, k):
+        if st.done or legal_of(st, k):
             rep.fail("status empty_mask but the oracle has legal tokens")
     else:
         rep.fail(f"unexpected status {status}")

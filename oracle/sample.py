@@ -107,13 +107,14 @@ def sample_decode(trie, k: int, emb_bits: np.ndarray, hidden_bits: np.ndarray, u
     """Constrained decoding with sampling: greedy_decode with the argmax
     replaced by sample_token using uniforms[t] at position t (forced positions
     with ``jump`` draw nothing and report a NaN logit)."""
-    from .grammar import WalkState, advance, legal_tokens
+    from .decode import walk_fns
     from .head import candidate_logits
-    st = WalkState()
+    start, legal_of, step = walk_fns(trie)
+    st = start()
     toks: List[int] = []
     logits: List[float] = []
     for t in range(max_steps):
-        legal = legal_tokens(trie, st, k)
+        legal = legal_of(st, k)
         if not legal:
             return toks, logits, "empty_mask"
         if jump and t > 0 and len(legal) == 1:
@@ -123,7 +124,7 @@ def sample_decode(trie, k: int, emb_bits: np.ndarray, hidden_bits: np.ndarray, u
             tok, lg = sample_token(legal, list(lg_all), temperature, top_k, top_p, float(uniforms[t]))
         toks.append(tok)
         logits.append(lg)
-        st = advance(trie, st, tok, k)
+        st = step(st, tok, k)
         if st.done:
             return toks, logits, "ok"
     return toks, logits, "max_steps"
@@ -170,14 +171,14 @@ def sample_teacher_force(trie, k: int, emb_bits: np.ndarray, hidden_bits: np.nda
     (draw_excused); its logit equals the exact dot product (``exact_logits``)
     or is within the greedy checker's relative tolerance; forced positions
     (``jump``) carry NaN.  Returns (ok, problems, excused_draws)."""
-    from .decode import FLOOR_SCALE, REL_TOL
-    from .grammar import WalkState, advance, legal_tokens
+    from .decode import FLOOR_SCALE, REL_TOL, walk_fns
     from .head import abs_mass, candidate_logits
-    st = WalkState()
+    start, legal_of, step = walk_fns(trie)
+    st = start()
     problems: List[str] = []
     excused = 0
     for t, (g_tok, g_log) in enumerate(zip(toks, logits)):
-        legal = legal_tokens(trie, st, k)
+        legal = legal_of(st, k)
         g_tok = int(g_tok)
         if g_tok not in legal:
             return False, [f"step {t}: token {g_tok} not legal"], excused
@@ -200,7 +201,7 @@ def sample_teacher_force(trie, k: int, emb_bits: np.ndarray, hidden_bits: np.nda
                 scale = max(abs(r), FLOOR_SCALE * float(abs_mass(emb_bits, hidden_bits[t], [g_tok])[0]))
                 if abs(float(g_log) - r) > REL_TOL * scale:
                     problems.append(f"step {t}: logit {float(g_log)} vs exact {r}")
-        st = advance(trie, st, g_tok, k)
+        st = step(st, g_tok, k)
         if st.done and t != len(toks) - 1:
             return False, problems + [f"step {t}: tokens continue after stop"], excused
     n = len(toks)

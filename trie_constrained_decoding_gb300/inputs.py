@@ -213,6 +213,84 @@ def hex_catalog(rng: np.random.Generator, hv: HexVocab, n_strings: int = 1000,
 
 
 # ----------------------------------------------------------------------------
+# Character-level catalogs and byte vocabularies
+# ----------------------------------------------------------------------------
+
+def hex_byte_vocab(hv: HexVocab) -> List[Tuple[int, bytes]]:
+    """The hex subset as (token id, bytes): 16 one-character and 256 two-character tokens."""
+    out = [(i, d.encode()) for d, i in hv.one.items()] + [(i, d.encode()) for d, i in hv.two.items()]
+    return sorted(out)
+
+
+def char_tool_names(rng: np.random.Generator, n_names: int, n_namespaces: int = 8, verbs: int = 4,
+                    objects: int = 3, max_suffix: int = 3) -> List[bytes]:
+    """ASCII tool names ``namespace.verb_object[suffix]`` over a-z, '.' and '_':
+    each level drawn from a small set under the level above (shared prefixes),
+    then 0..max_suffix random letters."""
+    letters = np.array(list("abcdefghijklmnopqrstuvwxyz"))
+
+    def word(lo, hi):
+        return "".join(letters[rng.integers(0, 26, size=int(rng.integers(lo, hi + 1)))])
+
+    tree = [(word(2, 5), [(word(3, 6), [word(2, 6) for _ in range(objects)]) for _ in range(verbs)])
+            for _ in range(n_namespaces)]
+    seen, out = set(), []
+    while len(out) < n_names:
+        ns, vs = tree[int(rng.integers(len(tree)))]
+        vb, obs = vs[int(rng.integers(len(vs)))]
+        name = f"{ns}.{vb}_{obs[int(rng.integers(len(obs)))]}" + word(0, max_suffix)
+        if name not in seen:
+            seen.add(name)
+            out.append(name.encode())
+    return out
+
+
+def char_bpe_vocab(rng: np.random.Generator, names: Sequence[bytes], vocab: int, n_pieces: int,
+                   reserved: Sequence[int] = ()) -> List[Tuple[int, bytes]]:
+    """A synthetic byte vocabulary for ``names``: every single character that
+    occurs, the words between separators (also with their separator attached)
+    and ``n_pieces`` random substrings of 2..4 characters, each given a distinct
+    seeded token id."""
+    pieces = set()
+    for n in names:
+        pieces.update(bytes([c]) for c in n)
+        txt = n.decode()
+        for part in txt.replace(".", " . ").replace("_", " _ ").split():
+            pieces.add(part.encode())
+        for sep in (".", "_"):
+            for i, seg in enumerate(txt.split(sep)[:-1]):
+                pieces.add((seg.split("." if sep == "_" else "_")[-1] + sep).encode())
+    names = list(names)
+    while len(pieces) < n_pieces + 40:
+        n = names[int(rng.integers(len(names)))]
+        L = int(rng.integers(2, 5))
+        if len(n) >= L:
+            i = int(rng.integers(0, len(n) - L + 1))
+            pieces.add(n[i:i + L])
+    banned = set(int(r) for r in reserved)
+    allowed = np.array([i for i in range(vocab) if i not in banned], dtype=np.int64)
+    ids = rng.choice(allowed, size=len(pieces), replace=False)
+    return sorted(zip((int(i) for i in ids), sorted(pieces)))
+
+
+def greedy_tokenize(s: bytes, vocab: Sequence[Tuple[int, bytes]]) -> Tuple[int, ...]:
+    """Canonical tokenization: longest vocabulary match at each position."""
+    by_bytes = {b: i for i, b in vocab}
+    longest = max(len(b) for _, b in vocab)
+    out, pos = [], 0
+    while pos < len(s):
+        for L in range(min(longest, len(s) - pos), 0, -1):
+            i = by_bytes.get(s[pos:pos + L])
+            if i is not None:
+                out.append(i)
+                pos += L
+                break
+        else:
+            raise ValueError(f"{s!r} cannot be tokenized at {pos}")
+    return tuple(out)
+
+
+# ----------------------------------------------------------------------------
 # Workloads
 # ----------------------------------------------------------------------------
 
@@ -236,9 +314,17 @@ class Workload:
     hid_std: float = 1.0
     seed: int = MASTER_SEED
     notes: dict = field(default_factory=dict)
+    # Character-level workloads: the catalog as byte strings and the byte
+    # vocabulary as (token id, bytes); ``catalog`` then holds each string's
+    # canonical (greedy longest-match) tokenization.
+    char_strings: Optional[List[bytes]] = None
+    char_vocab: Optional[List[Tuple[int, bytes]]] = None
 
     @property
     def max_depth(self) -> int:
+        """Most tokens one pointer can take (characters, for a character-level catalog)."""
+        if self.char_strings is not None:
+            return max(len(p) for p in self.char_strings)
         return max(len(p) for p in self.catalog)
 
     @property
@@ -328,12 +414,50 @@ def tensor_batch() -> Workload:
     return w
 
 
+def _char_workload(name, V, H, names, cv, **kw) -> Workload:
+    cat = [greedy_tokenize(n, cv) for n in names]
+    return Workload(name, V, H, cat, V - 2, V - 1, char_strings=list(names), char_vocab=list(cv), **kw)
+
+
+def char_tiny() -> Workload:
+    """Character-level tool names (42, ASCII) over a synthetic byte vocabulary in
+    vocab 8192, hidden 256, integer-valued bf16 (exact sums); k=3, B=1."""
+    V = 8192
+    names = char_tool_names(rng_for(_SLOT_CATALOG, extra=11), 42, n_namespaces=4, verbs=3, objects=3)
+    cv = char_bpe_vocab(rng_for(_SLOT_CATALOG, extra=12), names, V, 120, reserved=(V - 2, V - 1))
+    return _char_workload("char_tiny", V, 256, names, cv, k=3, batch=1, n_queries=64, max_fanout=256,
+                          cand_cap=256, residency="const", emb_kind="int")
+
+
+def char_tools() -> Workload:
+    """200 character-level tool names over a 1200-piece byte vocabulary in vocab
+    151936, hidden 2048 Gaussian (the large-head embedding); k=3, B=1."""
+    V = 151936
+    names = char_tool_names(rng_for(_SLOT_CATALOG, extra=13), 200)
+    cv = char_bpe_vocab(rng_for(_SLOT_CATALOG, extra=14), names, V, 1200, reserved=(V - 2, V - 1))
+    return _char_workload("char_tools", V, 2048, names, cv, k=3, batch=1, n_queries=1000, max_fanout=4096,
+                          cand_cap=4096, residency="auto", emb_kind="gauss")
+
+
+def char_hex() -> Workload:
+    """The 1000 random 32-character hex strings at character level: any
+    segmentation into the 272 hex tokens is legal; B=16, k=2."""
+    V = 151936
+    hv = hex_vocab(rng_for(_SLOT_CATALOG, extra=4), vocab=V, reserved=(V - 2, V - 1))
+    strings, _ = hex_catalog(rng_for(_SLOT_CATALOG, extra=5), hv)
+    return _char_workload("char_hex", V, 4096, [x.encode() for x in strings], hex_byte_vocab(hv), k=2, batch=16,
+                          n_queries=16, max_fanout=4096, cand_cap=4096, residency="global", emb_kind="gauss")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "large_head": large_head,
     "batched": batched,
     "unstructured": unstructured,
     "tensor_batch": tensor_batch,
+    "char_tiny": char_tiny,
+    "char_tools": char_tools,
+    "char_hex": char_hex,
 }
 
 
