@@ -197,9 +197,13 @@ def host_hidden(w, qids):
 def _oracle_batches(w, seconds: float, batches, hid_of, head: str):
     """Decode query batches in order with the oracle for about `seconds`;
     return (decode steps, tokens, batches decoded, seconds)."""
+    from oracle import chars as C
     from oracle import decode as D
     from oracle import grammar as G
-    trie = G.compile_catalog(w.catalog, w.sep_id, w.stop_id, w.vocab, max_fanout=w.max_fanout)
+    if w.char_strings is not None:
+        trie = C.CharGrammar(w.char_strings, w.char_vocab, w.sep_id, w.stop_id)
+    else:
+        trie = G.compile_catalog(w.catalog, w.sep_id, w.stop_id, w.vocab, max_fanout=w.max_fanout)
     emb = hid_of("emb")
     t0 = time.perf_counter()
     steps = tokens = done = 0
@@ -334,7 +338,10 @@ def run_ours(args):
     emb_bits = w.embedding()
     emb = torch.from_numpy(emb_bits.view(np.int16)).to(f"cuda:{dev}").view(torch.bfloat16)
     del emb_bits
-    trie = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
+    if w.char_strings is not None:
+        trie = tcd.Trie.compile_chars(w.char_strings, w.char_vocab, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
+    else:
+        trie = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
     tinfo = trie.info()
     ctx = tcd.Context(emb, max_batch=B, cand_cap=w.cand_cap)
     res = {"const": tcd.RES_CONST, "global": tcd.RES_GLOBAL, "auto": tcd.RES_AUTO}[args.residency or w.residency]

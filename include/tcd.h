@@ -175,6 +175,37 @@ tc_status tc_trie_export(const tc_trie* trie, int32_t* node_begin, int32_t* edge
                          int32_t* path_off, int32_t* path);
 
 /*
+ * tc_compile_char_trie - compile a character-level grammar: the catalog as
+ * byte strings and a byte vocabulary, so that every tokenization of a catalog
+ * string is accepted, not only one (the pith.science review of arXiv
+ * 2608.12574, key machinery: a character trie of the strings whose nodes carry
+ * the vocabulary tokens that can be walked from them without overshooting,
+ * found by Aho-Corasick matching of the vocabulary along the trie).
+ *
+ *  chars, offsets       string i is chars[offsets[i] .. offsets[i+1]) (bytes,
+ *                       non-empty, distinct), offsets int64[n_strings + 1]
+ *  tok_ids              int32[n_tokens] distinct ids in [0, vocab), none equal
+ *                       to sep_id / stop_id
+ *  tok_chars, tok_offsets  token j's bytes, non-empty, distinct
+ *  max_fanout           cap on any node's edges (token edges + 2 control edges)
+ *
+ * The result is a tc_trie like tc_compile_trie's: nodes are character-trie
+ * nodes numbered breadth-first, a node's edges are the tokens that walk from
+ * it (a token edge may skip several characters, and several edges may lead to
+ * one node) plus the separator and stop edges at a terminal, sorted by token
+ * id; static_cnt counts the strings below an edge's target.  It keeps no
+ * pointer paths (path_off all 0), so only the read-only no-repeat state
+ * applies: k <= 8 pointers, and TC_BIND_LIVE_COUNTS is TC_ERR_UNSUPPORTED.
+ * Errors: TC_ERR_INVALID_ARG, TC_ERR_EMPTY_STRING, TC_ERR_DUPLICATE (equal
+ * strings, equal token ids or token bytes), TC_ERR_CONTROL_COLLISION,
+ * TC_ERR_TOKEN_RANGE, TC_ERR_FANOUT.
+ */
+tc_status tc_compile_char_trie(const uint8_t* chars, const int64_t* offsets, int32_t n_strings,
+                               const int32_t* tok_ids, const uint8_t* tok_chars, const int64_t* tok_offsets,
+                               int32_t n_tokens, int32_t sep_id, int32_t stop_id, int32_t vocab,
+                               int32_t max_fanout, tc_trie** out);
+
+/*
  * tc_trie_export_ranks - the depth-first pointer numbering behind the
  * read-only no-repeat state ("Constraint made cheaper than no constraint",
  * section "The batched engine": batched sequences share one read-only trie and

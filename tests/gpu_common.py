@@ -8,6 +8,7 @@ import functools
 
 import numpy as np
 
+from oracle import chars as C
 from oracle import decode as D
 from oracle import grammar as G
 from trie_constrained_decoding_gb300 import inputs as I
@@ -45,15 +46,24 @@ def embedding(vocab: int, hidden: int, kind: str):
 
 @functools.lru_cache(maxsize=None)
 def oracle_trie(name: str):
+    """The oracle's grammar of a workload: the token trie, or the character-level grammar."""
     w = workload(name)
+    if w.char_strings is not None:
+        return C.CharGrammar(w.char_strings, w.char_vocab, w.sep_id, w.stop_id)
     return G.compile_catalog(w.catalog, w.sep_id, w.stop_id, w.vocab, max_fanout=w.max_fanout)
+
+
+def compile_trie(tcd, w):
+    if w.char_strings is not None:
+        return tcd.Trie.compile_chars(w.char_strings, w.char_vocab, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
+    return tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
 
 
 def make_ctx(tcd, name: str, max_batch: int = None, residency=None):
     w = workload(name)
     _, emb = embedding(w.vocab, w.hidden, w.emb_kind)
     ctx = tcd.Context(emb, max_batch=max_batch or w.batch, cand_cap=w.cand_cap)
-    trie = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
+    trie = compile_trie(tcd, w)
     res = {"const": tcd.RES_CONST, "global": tcd.RES_GLOBAL, "auto": tcd.RES_AUTO}[residency or w.residency]
     ctx.bind(trie, res)
     return ctx, trie

@@ -61,6 +61,9 @@ def _decl(name, restype, argtypes):
 
 _compile = _decl("tc_compile_trie", ctypes.c_int, [_i32p, _i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                    ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_vp)])
+_compile_chars = _decl("tc_compile_char_trie", ctypes.c_int,
+                       [_vp, _i64p, ctypes.c_int32, _i32p, _vp, _i64p, ctypes.c_int32, ctypes.c_int32,
+                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_vp)])
 _info = _decl("tc_trie_info", ctypes.c_int, [_vp, ctypes.POINTER(_TrieInfo)])
 _export = _decl("tc_trie_export", ctypes.c_int, [_vp] + [_i32p] * 7)
 _trie_free = _decl("tc_trie_free", None, [_vp])
@@ -140,6 +143,24 @@ class Trie:
         code = _compile(ids.ctypes.data_as(_i32p), offsets.ctypes.data_as(_i64p), len(catalog), sep_id, stop_id,
                         vocab, max_fanout, ctypes.byref(h))
         _check(code, "tc_compile_trie")
+        return cls(h)
+
+    @classmethod
+    def compile_chars(cls, strings: Sequence[bytes], vocab: Sequence[tuple], sep_id: int, stop_id: int,
+                      vocab_size: int, max_fanout: int = 4096) -> "Trie":
+        """tc_compile_char_trie: byte strings and a byte vocabulary [(token id, bytes)]."""
+        offs = np.zeros(len(strings) + 1, dtype=np.int64)
+        offs[1:] = np.cumsum([len(x) for x in strings])
+        chars = np.frombuffer(b"".join(strings), dtype=np.uint8).copy()
+        ids = np.array([i for i, _ in vocab], dtype=np.int32)
+        toff = np.zeros(len(vocab) + 1, dtype=np.int64)
+        toff[1:] = np.cumsum([len(b) for _, b in vocab])
+        tchars = np.frombuffer(b"".join(b for _, b in vocab), dtype=np.uint8).copy()
+        h = _vp()
+        code = _compile_chars(chars.ctypes.data, offs.ctypes.data_as(_i64p), len(strings),
+                              ids.ctypes.data_as(_i32p), tchars.ctypes.data, toff.ctypes.data_as(_i64p), len(vocab),
+                              sep_id, stop_id, vocab_size, max_fanout, ctypes.byref(h))
+        _check(code, "tc_compile_char_trie")
         return cls(h)
 
     def info(self) -> dict:

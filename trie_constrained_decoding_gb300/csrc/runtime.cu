@@ -88,6 +88,7 @@ struct DevGrammar {
   int32_t kw = 1;
   int32_t batch = 0, k = 0;  // of the last reset (0: none)
   bool force_counts = false;  // TC_BIND_LIVE_COUNTS: per-sequence count arrays for every k
+  bool no_counts = false;     // character-level grammar: no pointer paths, read-only state only
   int32_t iv = 0;             // state mode of the last reset (1: read-only no-repeat state)
   size_t cnt_batch = 0;       // sequences the count arrays (allocated on first use) hold
 
@@ -299,6 +300,11 @@ bool use_iv(const DevGrammar* g, int k) {
 
 // Count arrays of max_batch sequences, allocated the first time count mode runs.
 tc_status ensure_counts(const tc_ctx* c, DevGrammar* g) {
+  if (g->no_counts) {
+    set_error_message("a character-level grammar keeps no live-count arrays: k must be at most " +
+                      std::to_string(kBanMax));
+    return TC_ERR_UNSUPPORTED;
+  }
   if (g->d_cnt) return TC_OK;
   const size_t n = (size_t)c->max_batch * (size_t)std::max<int32_t>(1, g->n_edges);
   cudaError_t e = cudaMalloc(&g->d_cnt, sizeof(int32_t) * n);
@@ -588,6 +594,10 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
   if (!c || !t) return TC_ERR_INVALID_ARG;
   const bool force_counts = (residency & TC_BIND_LIVE_COUNTS) != 0;
   residency &= ~TC_BIND_LIVE_COUNTS;
+  if (force_counts && t->char_level) {
+    set_error_message("tc_bind_grammar: a character-level grammar has no live-count arrays");
+    return TC_ERR_UNSUPPORTED;
+  }
   if (residency != TC_RES_AUTO && residency != TC_RES_CONST && residency != TC_RES_GLOBAL) return TC_ERR_INVALID_ARG;
   if (t->vocab > c->V) {
     set_error_message("tc_bind_grammar: the trie's vocabulary is larger than the context's");
@@ -627,6 +637,7 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
     g->layout = L;
     g->kw = (t->n_strings + 31) / 32;
     g->force_counts = force_counts;
+    g->no_counts = t->char_level;
     g->root_beg = t->node_begin[0];
     g->root_end = t->node_begin[1];
     g->root_pid = t->node_ptr[0] >= 0 ? t->ptr_rank[t->node_ptr[0]] : -1;

@@ -787,6 +787,8 @@ struct Step1Shared {
   Cand spec[kPreMax][kPreMax];        // per candidate: its child's legal candidates
   int32_t spec_n[kPreMax];            // their number, -1 when not available
   float lg[kPreMax];                  // candidate logits (sampling)
+  float smp_w[kPreMax];               // sampling weights and kept flags, per candidate
+  int32_t smp_k[kPreMax];
   float wl[kWarps];
   int32_t wt[kWarps], wslot[kWarps];
   int32_t ncand, err, pid, done_after, smp_slot, smp_nan;
@@ -803,7 +805,7 @@ struct Step1Shared {
 // token order, lane i holding candidate i; every sum runs in a fixed order.
 // Returns the chosen slot, or -1 with nan = 1 when a logit is NaN.
 __device__ __forceinline__ int warp_sample(const StepParams& p, const float* lg, const Cand* cand, int n, float u,
-                                           int lane, int& nan) {
+                                           int lane, float* wsh, int* ksh, int& nan) {
   const bool act = lane < n;
   const float l = act ? lg[lane] : 0.f;
   const int32_t tok = act ? cand[lane].a.x : INT_MAX;
@@ -812,10 +814,7 @@ __device__ __forceinline__ int warp_sample(const StepParams& p, const float* lg,
   int kept = act ? 1 : 0;
   if (p.top_k > 0 && p.top_k < n) {
     int greater = 0;
-    for (int j = 0; j < 32; ++j) {
-      const float lj = __shfl_sync(kFull, l, j);
-      greater += (j < n && lj > l) ? 1 : 0;
-    }
+    for (int j = 0; j < n; ++j) greater += lg[j] > l ? 1 : 0;  // shared-memory broadcast reads
     kept = (act && greater < p.top_k) ? 1 : 0;
   }
   float m = kept ? l : -INFINITY;
@@ -823,13 +822,15 @@ __device__ __forceinline__ int warp_sample(const StepParams& p, const float* lg,
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
   float wgt = kept ? expf((l - m) * p.inv_temp) : 0.f;
   if (p.top_p < 1.f) {
+    wsh[lane] = wgt;
+    ksh[lane] = kept;
+    __syncwarp();
     float total = 0.f, run = 0.f;
     int larger = 0;
-    for (int j = 0; j < 32; ++j) {
-      const float lj = __shfl_sync(kFull, l, j);
-      const int32_t tj = __shfl_sync(kFull, tok, j);
-      const float wj = __shfl_sync(kFull, wgt, j);
-      const int kj = __shfl_sync(kFull, kept, j);
+    for (int j = 0; j < n; ++j) {  // candidates in token order, a fixed summation order
+      const float lj = lg[j], wj = wsh[j];
+      const int32_t tj = cand[j].a.x;
+      const int kj = ksh[j];
       total += wj;
       if (kj && (lj < l || (lj == l && tj <= tok))) run += wj;
       if (kj && (lj > l || (lj == l && tj > tok))) larger = 1;
@@ -953,7 +954,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
       int nan = 0, slot = -1;
       if (!sh.err && sh.ncand > 0) {
         const float u = p.device_form ? p.u[(size_t)b * p.out_stride + s.len] : p.u[b];
-        slot = warp_sample(p, sh.lg, sh.cand, sh.ncand, u, lane, nan);
+        slot = warp_sample(p, sh.lg, sh.cand, sh.ncand, u, lane, sh.smp_w, sh.smp_k, nan);
       }
       if (lane == 0) {
         sh.smp_slot = slot;

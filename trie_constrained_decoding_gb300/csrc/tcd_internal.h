@@ -19,6 +19,11 @@ struct tc_trie {
   // of ranks.  edge_lo[e] is the first rank below a token edge's child (the
   // range has static_cnt[e] ranks), or the terminal's own rank for a control edge.
   std::vector<int32_t> ptr_rank, edge_lo;
+  // Character-level grammar (tc_compile_char_trie): nodes are characters and a
+  // token edge may span several of them, so several edges can lead to one
+  // node; pointer paths are not kept and only the read-only no-repeat state
+  // (rank ranges) applies.
+  bool char_level = false;
   uint64_t content_hash = 0;
 
   int32_t n_nodes() const { return (int32_t)node_ptr.size(); }
