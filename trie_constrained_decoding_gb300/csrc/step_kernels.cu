@@ -868,6 +868,19 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
 
   float wl = -INFINITY;
   int32_t wt = INT_MAX, ws = -1;
+  const bool pre = s.pre_n > 0;
+  // With a precomputed list every warp knows its candidates from the state
+  // alone: the first one's row loads start at once, before the hidden state is
+  // read, and no barrier precedes the candidate loop.
+  uint4 e[NCH > 0 ? NCH : 1];  // the row of the candidate in flight
+  if constexpr (NCH > 0) {
+    if (mode == 1 && pre && warp < s.pre_n - 1) {
+      const uint4* r0 = reinterpret_cast<const uint4*>(p.emb + (size_t)pre0.a.x * p.H);
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) e[i] = ld_row(r0 + i * 32 + lane);
+    }
+  }
+  int n = 0, err = 0;
   if (mode == 1) {
     const uint16_t* x = hidden_row(p, s, b);
     if (p.device_form && tid == 32 && s.len + 1 < p.max_steps)
@@ -878,13 +891,12 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
     } else {
       for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
     }
-    const bool pre = s.pre_n > 0;
     if (!pre) {
       // Filter the node (fan-out <= 32: one warp).
       if (warp == 0) {
-        const int n = s.node;
-        const bool n_ok = n >= 0 && n < p.g.n_nodes;
-        const int nn = n_ok ? n : 0;
+        const int nd = s.node;
+        const bool n_ok = nd >= 0 && nd < p.g.n_nodes;
+        const int nn = n_ok ? nd : 0;
         const int beg = w.begin(nn), end = w.begin(nn + 1), pid = w.ptr(nn);
         const int cnt = n_ok ? warp_legal_set<kConst>(p, w, s, b, beg, end, pid, lane, sh.cand) : -1;
         if (lane == 0) {
@@ -893,14 +905,19 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
           sh.pid = pid;
         }
       }
-    } else if (tid == 0) {
-      sh.ncand = s.pre_n - 1;
-      sh.err = 0;
-      sh.pid = s.pre_pid;
+      __syncthreads();  // (pre is the same for the whole CTA)
+      n = sh.ncand;
+      err = sh.err;
+    } else {
+      n = s.pre_n - 1;
+      if (tid == 0) {
+        sh.ncand = n;
+        sh.err = 0;
+        sh.pid = s.pre_pid;
+      }
+      if constexpr (NCH == 0) __syncthreads();  // x staged in shared memory by all threads
     }
-    __syncthreads();
-    const int n = sh.ncand;
-    if (!sh.err) {
+    if (!err) {
       for (int l = warp; l < n; l += kWarps) {
         const Cand cd = pre ? (l == warp ? pre0 : p.pre[(size_t)b * kPreMax + l]) : sh.cand[l];
         // The row, then the child's edges: the candidate carries the child's
@@ -910,9 +927,10 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
         const uint4* r4 = reinterpret_cast<const uint4*>(p.emb + (size_t)cd.a.x * p.H);
         float acc = 0.f;
         if constexpr (NCH > 0) {
-          uint4 e[NCH];
+          if (!pre || l != warp) {  // (the first precomputed candidate's row is already in flight)
 #pragma unroll
-          for (int i = 0; i < NCH; ++i) e[i] = ld_row(r4 + i * 32 + lane);
+            for (int i = 0; i < NCH; ++i) e[i] = ld_row(r4 + i * 32 + lane);
+          }
           const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
           if (lane == 0) sh.spec_n[l] = sn;
           __syncwarp();
@@ -949,43 +967,50 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
   if (p.stats && tid == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
   __syncthreads();
 
-  if (mode == 1 && p.smp) {  // (uniform over the CTA: one sequence)
-    if (warp == 0) {
-      int nan = 0, slot = -1;
-      if (!sh.err && sh.ncand > 0) {
-        const float u = p.device_form ? p.u[(size_t)b * p.out_stride + s.len] : p.u[b];
-        slot = warp_sample(p, sh.lg, sh.cand, sh.ncand, u, lane, sh.smp_w, sh.smp_k, nan);
-      }
-      if (lane == 0) {
-        sh.smp_slot = slot;
-        sh.smp_nan = nan;
-      }
-    }
-    __syncthreads();
-  }
-
-  if (mode == 1) {
-    // Every thread folds the eight warp bests (same order, same result), or
-    // takes the sampled slot.
+  // The rest of the step is warp 0's: the fold, the transition, the next list.
+  if (mode == 1 && warp == 0) {
     float bl = -INFINITY;
     int32_t bt = INT_MAX, bs = -1;
     if (p.smp) {
-      bs = sh.smp_slot;
+      int nan = 0, slot = -1;
+      if (!err && n > 0) {
+        const float u = p.device_form ? p.u[(size_t)b * p.out_stride + s.len] : p.u[b];
+        slot = warp_sample(p, sh.lg, sh.cand, n, u, lane, sh.smp_w, sh.smp_k, nan);
+      }
+      bs = slot;
       if (bs >= 0) {
-        bl = sh.smp_nan ? __int_as_float(0x7fc00000) : sh.lg[bs];
+        bl = nan ? __int_as_float(0x7fc00000) : sh.lg[bs];
         bt = sh.cand[bs].a.x;
       }
     } else {
+      // Eight warp bests, folded by a fixed butterfly over lanes 0-7 (a strict
+      // total order, so every lane ends with the same winner).
+      if (lane < kWarps) {
+        bl = sh.wl[lane];
+        bt = sh.wt[lane];
+        bs = sh.wslot[lane];
+      }
 #pragma unroll
-      for (int i = 0; i < kWarps; ++i)
-        if (better(sh.wl[i], sh.wt[i], bl, bt)) { bl = sh.wl[i]; bt = sh.wt[i]; bs = sh.wslot[i]; }
+      for (int o = kWarps / 2; o > 0; o >>= 1) {
+        const float ol = __shfl_xor_sync(kFull, bl, o);
+        const int32_t ot = __shfl_xor_sync(kFull, bt, o);
+        const int32_t os = __shfl_xor_sync(kFull, bs, o);
+        if (better(ol, ot, bl, bt)) {
+          bl = ol;
+          bt = ot;
+          bs = os;
+        }
+      }
+      bl = __shfl_sync(kFull, bl, 0);
+      bt = __shfl_sync(kFull, bt, 0);
+      bs = __shfl_sync(kFull, bs, 0);
     }
-    const int ncand = sh.ncand;
+    const int ncand = n;
     int status = TC_OK;
     int32_t new_node = s.node, ptr_done = -1;
     bool stop = false;
     Cand win{make_int4(0, -1, 0, 0), make_int4(0, 0, -1, 0)};
-    if (sh.err) {
+    if (err) {
       status = TC_ERR_BOUNDS;
     } else if (ncand == 0) {
       status = TC_ERR_EMPTY_MASK;
@@ -997,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
         if (win.a.w <= 0) status = TC_ERR_NO_LIVE_EDGE;  // live count read this step
         else new_node = win.a.z;
       } else {
-        const int32_t pid = sh.pid;
+        const int32_t pid = pre ? s.pre_pid : sh.pid;
         if (!ptr_free(p, seq_live(p, s, b), pid)) {
           status = TC_ERR_NO_LIVE_EDGE;
         } else {
@@ -1012,69 +1037,65 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
     // Forced continuations follow when that set is a single token, or after a
     // separator (the root's set is not precomputed).
     const bool chain = p.jump && status == TC_OK && !stop && (next_n == 1 || ptr_done >= 0);
-    if (!chain && next_n > 0)
-      for (int i = tid; i < next_n; i += kThreads) p.pre[(size_t)b * kPreMax + i] = sh.spec[bs][i];
-    if (ptr_done >= 0 && !p.iv) decrement_path(p, b, ptr_done, tid, kThreads);
-    if (chain) __syncthreads();  // the decrements above are seen by the chain's legal sets
-    if (warp == 0) {
-      SeqState ns = s;
-      int pre_n = next_n, pre_pid = next_n >= 0 ? win.h.z : -2;  // the child's pointer rank
-      if (status != TC_OK) {
-        ns.status = status;
-        ns.done = 1;
+    if (!chain && lane < next_n) p.pre[(size_t)b * kPreMax + lane] = sh.spec[bs][lane];
+    if (ptr_done >= 0 && !p.iv) decrement_path(p, b, ptr_done, lane, 32);
+    SeqState ns = s;
+    int pre_n = next_n, pre_pid = next_n >= 0 ? win.h.z : -2;  // the child's pointer rank
+    if (status != TC_OK) {
+      ns.status = status;
+      ns.done = 1;
+    } else {
+      ns.node = new_node;
+      ns.len = s.len + 1;
+      if (ptr_done >= 0) {
+        if (p.iv) ban_add(ns, ptr_done);
+        else if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
+        ns.emitted = s.emitted + 1;
+      }
+      if (stop) ns.done = 1;
+    }
+    if (lane == 0) {
+      if (p.stats) {
+        atomicAdd(&p.stats[kStatSeqSteps], 1ull);
+        atomicAdd(&p.stats[kStatCandRows], (unsigned long long)ncand);
+      }
+      if (p.device_form) {
+        if (status == TC_OK && s.len < p.out_stride) {
+          p.tok_out[(size_t)b * p.out_stride + s.len] = bt;
+          p.logit_out[(size_t)b * p.out_stride + s.len] = bl;
+        }
       } else {
-        ns.node = new_node;
-        ns.len = s.len + 1;
-        if (ptr_done >= 0) {
-          if (p.iv) ban_add(ns, ptr_done);
-          else if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
-          ns.emitted = s.emitted + 1;
-        }
-        if (stop) ns.done = 1;
-      }
-      if (lane == 0) {
-        if (p.stats) {
-          atomicAdd(&p.stats[kStatSeqSteps], 1ull);
-          atomicAdd(&p.stats[kStatCandRows], (unsigned long long)ncand);
-        }
-        if (p.device_form) {
-          if (status == TC_OK && s.len < p.out_stride) {
-            p.tok_out[(size_t)b * p.out_stride + s.len] = bt;
-            p.logit_out[(size_t)b * p.out_stride + s.len] = bl;
-          }
-        } else {
-          p.tok_out[(size_t)b * p.out_stride] = status == TC_OK ? bt : -1;
-          if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = status == TC_OK ? bl : 0.f;
-        }
-      }
-      if (chain) {
-        __syncwarp();  // the spent flag set above
-        // The winner's own (precomputed) list slot serves as the chain's scratch.
-        Cand* list = sh.spec[bs];
-        const int4 hdr = ptr_done >= 0 ? root_hdr(p) : win.h;
-        forced_chain<kConst>(p, w, b, ns, lane, hdr, list, next_n == 1, pre_n, pre_pid);
-        if (pre_n > 0 && lane < pre_n) {
-          p.pre[(size_t)b * kPreMax + lane] = list[lane];
-          prefetch_l2(p.emb + (size_t)list[lane].a.x * p.H, (uint32_t)p.H * 2u);
-        }
-        if (lane == 0 && !ns.done && ns.len < p.max_steps)
-          prefetch_l2(p.hidden + ((size_t)ns.len * p.B + b) * p.H, (uint32_t)p.H * 2u);
-      }
-      if (ns.status == TC_OK) {
-        ns.pre_n = pre_n >= 0 ? pre_n + 1 : 0;
-        ns.pre_pid = pre_n >= 0 ? pre_pid : -2;
-      } else {
-        ns.pre_n = 0;
-      }
-      if (lane == 0) {
-        p.st[b] = ns;
-        if (p.status_out) p.status_out[b] = ns.status;
-        if (p.lens_out) p.lens_out[b] = ns.len;
-        if (ns.done) atomicSub(&p.ctrl->live, 1);
-        sh.done_after = ns.done;
+        p.tok_out[(size_t)b * p.out_stride] = status == TC_OK ? bt : -1;
+        if (p.logit_out) p.logit_out[(size_t)b * p.out_stride] = status == TC_OK ? bl : 0.f;
       }
     }
-  } else if (tid == 0) {
+    if (chain) {
+      __syncwarp();  // the decrements and the spent flag above are seen by the chain
+      // The winner's own (precomputed) list slot serves as the chain's scratch.
+      Cand* list = sh.spec[bs];
+      const int4 hdr = ptr_done >= 0 ? root_hdr(p) : win.h;
+      forced_chain<kConst>(p, w, b, ns, lane, hdr, list, next_n == 1, pre_n, pre_pid);
+      if (pre_n > 0 && lane < pre_n) {
+        p.pre[(size_t)b * kPreMax + lane] = list[lane];
+        prefetch_l2(p.emb + (size_t)list[lane].a.x * p.H, (uint32_t)p.H * 2u);
+      }
+      if (lane == 0 && !ns.done && ns.len < p.max_steps)
+        prefetch_l2(p.hidden + ((size_t)ns.len * p.B + b) * p.H, (uint32_t)p.H * 2u);
+    }
+    if (ns.status == TC_OK) {
+      ns.pre_n = pre_n >= 0 ? pre_n + 1 : 0;
+      ns.pre_pid = pre_n >= 0 ? pre_pid : -2;
+    } else {
+      ns.pre_n = 0;
+    }
+    if (lane == 0) {
+      p.st[b] = ns;
+      if (p.status_out) p.status_out[b] = ns.status;
+      if (p.lens_out) p.lens_out[b] = ns.len;
+      if (ns.done) atomicSub(&p.ctrl->live, 1);
+      sh.done_after = ns.done;
+    }
+  } else if (mode != 1 && tid == 0) {
     if (mode == 2) {
       stop_out_of_steps(p, s, b);
     } else if (!p.device_form) {
