@@ -167,9 +167,10 @@ struct ResetParams {
 
 enum Head { kHeadSparse = 0, kHeadDense = 1, kHeadUnionGemm = 2, kHeadDenseGemm = 3 };
 
-// Number of CTAs per sequence the sparse step uses for a grammar of the given
-// largest fan-out at batch B, and the dense step's CTAs per sequence.
-int sparse_tiles(int max_fanout, int B, int num_sms);
+// Number of CTAs per sequence the multi-CTA sparse step uses for a grammar of
+// the given largest fan-out at batch B (at most one wave of resident CTAs),
+// and the dense step's CTAs per sequence.
+int sparse_tiles(int max_fanout, int B, int num_sms, int H, int cand_cap, bool const_resident);
 int dense_tiles(int B, int num_sms);
 
 // Opt the step kernels in to kMaxDynamicSmem bytes of dynamic shared memory

@@ -182,7 +182,9 @@ bool one_cta_sparse(const DevGrammar* g) { return g->max_fanout <= 32; }
 
 int tiles_for(const tc_ctx* c, const DevGrammar* g, int head, int B) {
   if (head == TC_HEAD_SPARSE && one_cta_sparse(g)) return 1;
-  return head == TC_HEAD_SPARSE ? sparse_tiles(g->max_fanout, B, c->num_sms) : dense_tiles(B, c->num_sms);
+  return head == TC_HEAD_SPARSE ? sparse_tiles(g->max_fanout, B, c->num_sms, c->H, c->cand_cap,
+                                              g->residency == TC_RES_CONST)
+                                 : dense_tiles(B, c->num_sms);
 }
 
 bool is_gemm_head(int head) { return head == TC_HEAD_UNION_GEMM || head == TC_HEAD_DENSE_GEMM; }

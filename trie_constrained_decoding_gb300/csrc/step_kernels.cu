@@ -1515,9 +1515,39 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
 
 // ---------------------------------------------------------------- launchers
 
-int sparse_tiles(int max_fanout, int B, int num_sms) {
+namespace {
+
+// Resident CTAs per SM of the multi-CTA sparse step for this hidden size and
+// dynamic shared memory (registers usually allow one).
+template <bool kConst>
+int sparse_occupancy(int H, size_t smem) {
+  int occ = 0;
+  cudaError_t e;
+  switch (H) {
+    case 256: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 1>, kThreads, smem); break;
+    case 2048: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 8>, kThreads, smem); break;
+    case 4096: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 16>, kThreads, smem); break;
+    default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 0>, kThreads, smem); break;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return occ < 1 ? 1 : occ;
+}
+
+}  // namespace
+
+int sparse_tiles(int max_fanout, int B, int num_sms, int H, int cand_cap, bool const_resident) {
+  // One warp per candidate, but no more CTAs than the GPU holds at once: a
+  // second wave would add a whole kernel's latency to every step.
   int by_fan = (max_fanout + kWarps - 1) / kWarps;
-  int by_grid = (4 * num_sms + B - 1) / B;
+  const int b = B > 0 ? B : 1;
+  const size_t xbytes = (H == 256 || H == 2048 || H == 4096) ? 0 : (size_t)H * 2;  // x staged for other sizes
+  const size_t smem = xbytes + 2 * (size_t)((cand_cap + by_fan - 1) / (by_fan > 0 ? by_fan : 1)) * sizeof(int32_t);
+  const int occ = const_resident ? sparse_occupancy<true>(H, smem) : sparse_occupancy<false>(H, smem);
+  int by_grid = (num_sms * occ) / b;
+  if (by_grid < 1) by_grid = 1;
   int t = by_fan < by_grid ? by_fan : by_grid;
   if (t < 1) t = 1;
   if (t > kMaxTiles) t = kMaxTiles;
