@@ -44,6 +44,14 @@ __constant__ int32_t c_walk[TC_CONST_CAPACITY_BYTES / 4];
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+
+// Candidate slots per CTA of the multi-CTA sparse step with T CTAs per
+// sequence: a node using A <= T of them gives each at most
+// max(ceil(C / T), kWarps) candidates (A is ceil(fan-out / kWarps) unless T caps it).
+__host__ __device__ __forceinline__ int sparse_local_cap(int cand_cap, int T) {
+  const int c = (cand_cap + T - 1) / T;
+  return c > kWarps ? c : kWarps;
+}
 constexpr int gemm_tile_cols_dev = 128;  // columns per GEMM tile (gemm_tc.cu)
 
 template <bool kConst>
@@ -621,13 +629,16 @@ __device__ __forceinline__ void stop_out_of_steps(const StepParams& p, const Seq
 // apply the transition; then, in a loop-control launch, set the loop condition.
 template <bool kConst>
 __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int mode,
-                          float wl, int32_t wt, int32_t we, StepShared& sh) {
-  // mode: 0 = idle (stopped or failed before this step), 1 = active, 2 = out of steps now
+                          float wl, int32_t wt, int32_t we, StepShared& sh, int active) {
+  // mode: 0 = idle (stopped or failed before this step), 1 = active, 2 = out of steps now.
+  // active: the sequence's CTAs taking part in this step (blockIdx.x < active).
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tiles = gridDim.x, t = blockIdx.x;
+  const int tiles = active, t = blockIdx.x;
   if (p.stats && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
   if (tid == 0) sh.done_after = 1;
-  if (mode == 1) {
+  if (mode == 1 && t >= tiles) {
+    // not needed for this node: nothing to fold
+  } else if (mode == 1) {
     if (lane == 0) {
       sh.wl[warp] = wl;
       sh.wt[warp] = wt;
@@ -641,7 +652,7 @@ __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kCon
         if (better(sh.wl[i], sh.wt[i], bl, bt)) { bl = sh.wl[i]; bt = sh.wt[i]; be = sh.we[i]; }
       int last = 1;
       if (tiles > 1) {
-        Partial* slot = p.part + (size_t)b * tiles;
+        Partial* slot = p.part + (size_t)b * gridDim.x;
         slot[t] = Partial{bl, bt, be, 0};
         __threadfence();
         const uint32_t ticket = atomicAdd(&p.seq_ticket[b], 1u);
@@ -740,14 +751,25 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   const SeqState s = p.st[b];
   const int mode = seq_mode(p, s);
   const int nch = p.H >> 3;
-  const int local_cap = (p.cand_cap + T - 1) / T;
+  const int local_cap = sparse_local_cap(p.cand_cap, T);
   uint4* xs = reinterpret_cast<uint4*>(smem_raw);
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
   int32_t* s_edge = s_tok + local_cap;
+  // A node needs one CTA per kWarps of its edges: the others leave at once
+  // (deep nodes of a wide catalog have a few edges, its root hundreds).
+  int A = T;
+  if (mode == 1) {
+    const int nd = s.node;
+    if (nd >= 0 && nd < p.g.n_nodes) {
+      const int fan = w.begin(nd + 1) - w.begin(nd);
+      const int need = (fan + kWarps - 1) / kWarps;
+      A = need < 1 ? 1 : (need < T ? need : T);
+    }
+  }
 
   float wl = -INFINITY;
   int32_t wt = INT_MAX, we = -1;
-  if (mode == 1) {
+  if (mode == 1 && t < A) {
     const uint16_t* x = hidden_row(p, s, b);
     XFrag<NCH> xf;
     if constexpr (NCH > 0) {
@@ -755,10 +777,10 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
     } else {
       for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
     }
-    filter_node<kConst>(p, w, s, b, T, t, s_tok, s_edge, sh);
+    filter_node<kConst>(p, w, s, b, A, t, s_tok, s_edge, sh);
     if (!sh.err) {
       const int nc = sh.ncand;
-      const int nlocal = nc > t ? (nc - t + T - 1) / T : 0;
+      const int nlocal = nc > t ? (nc - t + A - 1) / A : 0;
       for (int l = warp; l < nlocal; l += kWarps) {
         const int32_t tok = s_tok[l];
         const float v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
@@ -766,7 +788,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
       }
     }
   }
-  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh);
+  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh, A);
 }
 
 // ---------------------------------------------------------------- one-CTA sparse step
@@ -1269,7 +1291,7 @@ __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p
     }
   }
   pdl_trigger();
-  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh);
+  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh, gridDim.x);
 }
 
 __global__ void __launch_bounds__(kThreads) reset_kernel(const ResetParams r) {
@@ -1510,7 +1532,7 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
     }
     __syncthreads();
   }
-  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh);
+  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh, gridDim.x);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -1544,7 +1566,7 @@ int sparse_tiles(int max_fanout, int B, int num_sms, int H, int cand_cap, bool c
   int by_fan = (max_fanout + kWarps - 1) / kWarps;
   const int b = B > 0 ? B : 1;
   const size_t xbytes = (H == 256 || H == 2048 || H == 4096) ? 0 : (size_t)H * 2;  // x staged for other sizes
-  const size_t smem = xbytes + 2 * (size_t)((cand_cap + by_fan - 1) / (by_fan > 0 ? by_fan : 1)) * sizeof(int32_t);
+  const size_t smem = xbytes + 2 * (size_t)sparse_local_cap(cand_cap, by_fan > 0 ? by_fan : 1) * sizeof(int32_t);
   const int occ = const_resident ? sparse_occupancy<true>(H, smem) : sparse_occupancy<false>(H, smem);
   int by_grid = (num_sms * occ) / b;
   if (by_grid < 1) by_grid = 1;
@@ -1567,7 +1589,7 @@ template <bool kConst, int NCH>
 cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaStream_t s) {
   const int nch = p.H >> 3;
   const size_t xbytes = NCH == 0 ? (size_t)nch * 16 : 0;
-  const int cap = head == kHeadSparse ? (p.cand_cap + tiles - 1) / tiles : p.cand_cap;
+  const int cap = head == kHeadSparse ? sparse_local_cap(p.cand_cap, tiles) : p.cand_cap;
   size_t smem = xbytes + 2 * (size_t)cap * sizeof(int32_t);
   if (head != kHeadSparse) {
     int R, S;
