@@ -616,7 +616,7 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
                                                         "forced span after it")
 
     # --- sampling (temperature 1, top-p 0.9) against the greedy argmax, same queries
-    if head == tcd.HEAD_SPARSE and max_fanout <= 32:
+    if head == tcd.HEAD_SPARSE:
         n_s = min(len(qids), 500 if B == 1 else 16)
         uq = {q: torch.from_numpy(w.uniforms(q * B, B)).to(f"cuda:{dev}") for q in sorted(set(qids[:n_s]))}
         rates = {}

@@ -339,8 +339,10 @@ typedef struct tc_sampling_t {
  * tc_decode_sample - tc_decode with sampling.  uniforms (device) float[batch,
  * max_steps]: the uniform of sequence b at output position t is
  * uniforms[b * max_steps + t] (positions filled by forced continuations use
- * none).  Sparse head only (TC_FLAG_JUMP_FORWARD may be or-ed in), on grammars
- * whose nodes have at most 32 edges: TC_ERR_UNSUPPORTED otherwise.  The
+ * none).  Sparse head only (TC_FLAG_JUMP_FORWARD may be or-ed in):
+ * TC_ERR_UNSUPPORTED otherwise.  On grammars with a node of more than 32 edges
+ * the first call allocates per-context scratch of 12 bytes per candidate slot
+ * (max_batch x cand_cap) for the multi-CTA step's candidate logits.  The
  * random numbers are the caller's: the library generates none.
  */
 tc_status tc_decode_sample(tc_ctx* ctx, const void* hidden_steps_bf16, int32_t n_steps, int32_t batch,

@@ -1,4 +1,5 @@
-"""GPU parity of sampling (tc_decode_sample / tc_step_sample) against the oracle.
+"""GPU parity of sampling (tc_decode_sample / tc_step_sample) against the oracle,
+on the one-CTA step (nodes of at most 32 edges) and the multi-CTA step.
 
 "Understanding Inference for Systems Engineers", section 3.8: softmax of
 logit / temperature over the legal candidates, restricted to the top-k highest
@@ -176,10 +177,48 @@ def test_sampling_rejected_where_unsupported(tcd):
             bufs.run(ctx, hid, u, w.k, **kw)
         assert e.value.name == name
     ctx.close()
-    uw = workload("unstructured")
-    ctx, _ = make_ctx(tcd, "unstructured", max_batch=2)
-    b2 = _Bufs(uw.max_steps, 2, uw.hidden, uw.max_steps)
-    with pytest.raises(tcd.TcError) as e:       # fan-out above 32
-        b2.run(ctx, uw.hidden_states(0, 2), uw.uniforms(0, 2), uw.k)
-    assert e.value.name == "TC_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("name,T,top_k,top_p", [("unstructured", 1.0, 0, 0.9), ("unstructured", 0.7, 20, 1.0),
+                                                ("char_tools", 1.0, 0, 0.8), ("char_hex", 1.2, 50, 0.95)])
+def test_multi_cta_sampling_matches_oracle(tcd, name, T, top_k, top_p):
+    """Grammars with nodes of more than 32 edges: the multi-CTA step leaves every
+    candidate's logit to the sequence's last CTA, which sorts and draws."""
+    w = workload(name)
+    B = 8
+    hid = w.hidden_states(0, B)
+    u = w.uniforms(0, B)
+    ctx, _ = make_ctx(tcd, name, max_batch=B)
+    out = _Bufs(w.max_steps, B, w.hidden, w.max_steps).run(ctx, hid, u, w.k, temperature=T, top_k=top_k,
+                                                           top_p=top_p)
     ctx.close()
+    assert np.all(out[3] == 0)
+    _check(name, hid, u, out, w.k, w.max_steps, T, top_k, top_p)
+
+
+def test_multi_cta_grid_of_uniforms(tcd):
+    """The hex catalog's root (267 candidates), 2048 sequences with one hidden
+    state and uniforms (i + 1/2) / 2048: the first tokens follow the oracle's
+    interval lengths."""
+    w = workload("unstructured")
+    N = 2048
+    one = w.hidden_states(3, 1)
+    hid = np.repeat(one, N, axis=1)
+    u = np.zeros((N, w.max_steps), dtype=np.float32)
+    u[:, 0] = (np.arange(N, dtype=np.float64) + 0.5) / N
+    u[:, 1:] = 0.5
+    ctx, _ = make_ctx(tcd, "unstructured", max_batch=N)
+    T, top_k, top_p = 0.5, 0, 0.9
+    out = _Bufs(w.max_steps, N, w.hidden, w.max_steps).run(ctx, hid, u, w.k, temperature=T, top_k=top_k,
+                                                           top_p=top_p)
+    ctx.close()
+    trie = oracle_trie("unstructured")
+    emb_bits, _ = embedding(w.vocab, w.hidden, w.emb_kind)
+    legal = G.legal_tokens(trie, G.WalkState(), w.k)
+    lg = list(candidate_logits(emb_bits, one[0, 0], legal))
+    iv = S.token_intervals(legal, lg, T, top_k, top_p)
+    first = out[0][:, 0]
+    assert set(np.unique(first).tolist()) <= set(iv)
+    assert len(iv) >= 4
+    for t, (lo, hi) in iv.items():
+        assert abs(int((first == t).sum()) - N * (hi - lo)) <= 2.0

@@ -18,8 +18,10 @@ constexpr int kMaxCandCap = 4096;
 constexpr int kLoopUnroll = 8;
 // Dynamic shared memory a step kernel may request: x staged for the generic
 // hidden size, two int32 candidate lists of up to kMaxCandCap entries, and
-// (dense head) 128 KiB of row stages.
+// (dense head) 128 KiB of row stages or (multi-CTA sampling) 64 KiB of sort
+// keys and weights.
 constexpr int kMaxDynamicSmem = kMaxHidden * 2 + 2 * kMaxCandCap * 4 + 128 + 128 * 1024;
+constexpr int kSampleSmem = kMaxCandCap * 8 + 2 * kMaxCandCap * 4 + 256 * 4 + 64;
 
 // Largest k of the read-only no-repeat state: the banned set is up to kBanMax
 // 16-bit pointer ranks, 16 bytes per sequence.
@@ -135,6 +137,11 @@ struct StepParams {
   int32_t top_k;            // <= 0: off
   float top_p;              // >= 1: off
   const float* u;           // uniforms: device form [b * out_stride + position], host form [b]
+  // Multi-CTA sampling: each CTA leaves its candidates' logits, tokens and
+  // edges here by candidate rank, for the sequence's last CTA ([B, cand_cap] each)
+  float* smp_lg;
+  int32_t* smp_tok;
+  int32_t* smp_edge;
 };
 
 // Cumulative counters kept by the kernels (one atomic per launch / per sequence step).

@@ -165,6 +165,9 @@ struct tc_ctx {
   uint32_t* d_seq_ticket = nullptr;
   Ctrl* d_ctrl = nullptr;
   unsigned long long* d_stats = nullptr;
+  float* d_smp_lg = nullptr;       // multi-CTA sampling scratch [max_batch, cand_cap], on first use
+  int32_t* d_smp_tok = nullptr;
+  int32_t* d_smp_edge = nullptr;
   HeadScratch hs{};           // GEMM-head scratch, allocated on first use
   EmbMaps emb_maps{};         // tensor maps of the embedding for the GEMM heads
   bool hs_ready = false;
@@ -291,6 +294,9 @@ StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
   p.max_steps = INT32_MAX;
   p.pre = one_cta_sparse(g) ? g->d_pre : nullptr;
   p.iv = g->iv;
+  p.smp_lg = c->d_smp_lg;
+  p.smp_tok = c->d_smp_tok;
+  p.smp_edge = c->d_smp_edge;
   return p;
 }
 
@@ -380,9 +386,8 @@ void apply_sampling(StepParams& p, const SampleArgs& a) {
 
 // Sampling runs in the one-CTA sparse step (grammars whose nodes have at most
 // 32 edges); temperature > 0 and finite, top_k >= 0, top_p in [0, 1].
-tc_status check_sampling(const tc_ctx* c, const DevGrammar* g, int head, const tc_sampling_t* sp, const float* u,
+tc_status check_sampling(tc_ctx* c, const DevGrammar* g, int head, const tc_sampling_t* sp, const float* u,
                          SampleArgs* out) {
-  (void)c;
   if (!sp || !u || misaligned(u, 4)) {
     set_error_message("sampling: parameters and 4-byte aligned uniforms are required");
     return TC_ERR_INVALID_ARG;
@@ -392,9 +397,26 @@ tc_status check_sampling(const tc_ctx* c, const DevGrammar* g, int head, const t
     set_error_message("sampling: temperature must be positive and finite, top_k >= 0, 0 <= top_p <= 1");
     return TC_ERR_INVALID_ARG;
   }
-  if ((head & ~TC_FLAG_JUMP_FORWARD) != TC_HEAD_SPARSE || !g || !one_cta_sparse(g)) {
-    set_error_message("sampling: sparse head on grammars whose nodes have at most 32 edges");
+  if ((head & ~TC_FLAG_JUMP_FORWARD) != TC_HEAD_SPARSE || !g) {
+    set_error_message("sampling: sparse head only");
     return TC_ERR_UNSUPPORTED;
+  }
+  if (!one_cta_sparse(g) && !c->d_smp_lg) {
+    // The multi-CTA step hands every candidate's logit to the sequence's last CTA.
+    const size_t n = (size_t)c->max_batch * (size_t)c->cand_cap;
+    cudaError_t e = cudaMalloc(&c->d_smp_lg, n * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&c->d_smp_tok, n * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMalloc(&c->d_smp_edge, n * sizeof(int32_t));
+    if (e != cudaSuccess) {
+      cudaFree(c->d_smp_lg);
+      cudaFree(c->d_smp_tok);
+      cudaFree(c->d_smp_edge);
+      c->d_smp_lg = nullptr;
+      c->d_smp_tok = c->d_smp_edge = nullptr;
+      cudaGetLastError();
+      set_error_message("sampling scratch: " + std::string(cudaGetErrorString(e)));
+      return TC_ERR_OOM;
+    }
   }
   out->smp = 1;
   out->inv_temp = 1.f / sp->temperature;
@@ -587,6 +609,9 @@ extern "C" void tc_ctx_destroy(tc_ctx* c) {
   cudaFree(c->d_seq_ticket);
   cudaFree(c->d_ctrl);
   cudaFree(c->d_stats);
+  cudaFree(c->d_smp_lg);
+  cudaFree(c->d_smp_tok);
+  cudaFree(c->d_smp_edge);
   if (c->h_live) cudaFreeHost(c->h_live);
   if (c->capture_stream) cudaStreamDestroy(c->capture_stream);
   delete c;
@@ -749,6 +774,9 @@ tc_status step_impl(tc_ctx* c, const void* hidden, int32_t head, const tc_sampli
     rc = check_sampling(c, g, head, sp, u, &smp);
     if (rc != TC_OK) return rc;
     apply_sampling(p, smp);
+    p.smp_lg = c->d_smp_lg;  // (allocated by check_sampling on first use)
+    p.smp_tok = c->d_smp_tok;
+    p.smp_edge = c->d_smp_edge;
   }
   TC_CUDA(launch_any_step(c, g, p, head, s, false));
   return TC_OK;
@@ -807,12 +835,12 @@ tc_status decode_impl(tc_ctx* c, const void* hidden, int32_t n_steps, int32_t ba
                       int32_t* lens, int32_t* status, void* stream) {
   tc_status rc = check_decode_args(c, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status);
   if (rc != TC_OK) return rc;
+  DeviceGuard dg(c->device);
   SampleArgs smp;
   if (sp || u) {
     rc = check_sampling(c, c->bound, head, sp, u, &smp);
     if (rc != TC_OK) return rc;
   }
-  DeviceGuard dg(c->device);
   GraphKey key{c->bound, hidden, n_steps, batch, k, max_steps, head, toks, logits, lens, status, smp};
   tc_graph* gr = nullptr;
   for (size_t i = 0; i < c->cache.size(); ++i) {

@@ -41,6 +41,10 @@ namespace tcd {
 
 __constant__ int32_t c_walk[TC_CONST_CAPACITY_BYTES / 4];
 
+// Sampling over one sequence's candidates by a whole CTA (defined below).
+__device__ int block_sample(const StepParams& p, const float* lg, const int32_t* tk, int n, float u,
+                            unsigned char* smem, int& nan);
+
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
@@ -625,6 +629,15 @@ __device__ __forceinline__ void stop_out_of_steps(const StepParams& p, const Seq
   atomicSub(&p.ctrl->live, 1);
 }
 
+// Byte offset of the multi-CTA step's sampling buffers in its dynamic shared
+// memory: after the staged hidden state (generic sizes) and the candidate lists.
+__host__ __device__ __forceinline__ size_t sample_smem_offset(const StepParams& p, int tiles) {
+  const bool staged = !(p.H == 256 || p.H == 2048 || p.H == 4096);
+  const size_t x = staged ? (size_t)(p.H >> 3) * 16 : 0;
+  const size_t lists = 2 * (size_t)sparse_local_cap(p.cand_cap, tiles) * sizeof(int32_t);
+  return (x + lists + 127) & ~(size_t)127;
+}
+
 // Fold the per-warp bests, combine the CTAs of sequence b, let the last CTA
 // apply the transition; then, in a loop-control launch, set the loop condition.
 template <bool kConst>
@@ -678,6 +691,28 @@ __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kCon
     }
     __syncthreads();
     if (sh.last) {
+      if (p.smp && !sh.err && sh.ncand > 0) {
+        // Sampling: the draw replaces the fold's argmax (all candidates' logits
+        // were left in the sequence's scratch rows by their CTAs).
+        extern __shared__ __align__(128) unsigned char smem_raw[];
+        const size_t row = (size_t)b * p.cand_cap;
+        const float u = p.device_form ? p.u[(size_t)b * p.out_stride + s.len] : p.u[b];
+        int nan = 0;
+        const int slot = block_sample(p, p.smp_lg + row, p.smp_tok + row, sh.ncand, u,
+                                      smem_raw + sample_smem_offset(p, gridDim.x), nan);
+        if (tid == 0) {
+          if (slot >= 0) {
+            sh.bl = __ldcg(p.smp_lg + row + slot);
+            sh.bt = __ldcg(p.smp_tok + row + slot);
+            sh.be = __ldcg(p.smp_edge + row + slot);
+          } else {
+            sh.bl = -INFINITY;
+            sh.bt = INT_MAX;
+            sh.be = -1;
+          }
+        }
+        __syncthreads();
+      }
       const int d = finish_sequence<kConst>(p, w, s, b, sh.bl, sh.bt, sh.be, sh.ncand, sh.err);
       if (tid == 0) sh.done_after = d;
     }
@@ -785,6 +820,13 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
         const int32_t tok = s_tok[l];
         const float v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
         if (better(v, tok, wl, wt)) { wl = v; wt = tok; we = s_edge[l]; }
+        if (p.smp && lane == 0) {  // by candidate rank, for the sequence's last CTA
+          const size_t r = (size_t)b * p.cand_cap + (size_t)l * A + t;
+          p.smp_lg[r] = v;
+          p.smp_tok[r] = tok;
+          p.smp_edge[r] = s_edge[l];
+          __threadfence();
+        }
       }
     }
   }
@@ -871,6 +913,150 @@ __device__ __forceinline__ int warp_sample(const StepParams& p, const float* lg,
   const unsigned any = __ballot_sync(kFull, kept);
   if (hit) return __ffs(hit) - 1;
   return any ? 31 - __clz(any) : -1;
+}
+
+// Inclusive prefix sums of v[0, n) in place, in a fixed order for any n:
+// thread t sums its contiguous chunk sequentially, warp 0 scans the 256 chunk
+// totals (8 per lane, then a shuffle scan), and each chunk adds its offset.
+// tot: 256 floats of scratch.  All threads of the CTA call it.
+__device__ __forceinline__ void block_scan_inclusive(float* v, int n, float* tot) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int c = (n + kThreads - 1) / kThreads;
+  const int i0 = tid * c, i1 = min(n, i0 + c);
+  float run = 0.f;
+  for (int i = i0; i < i1; ++i) {
+    run += v[i];
+    v[i] = run;
+  }
+  tot[tid] = run;
+  __syncthreads();
+  if (tid < 32) {
+    float mine[kThreads / 32];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < kThreads / 32; ++j) {
+      mine[j] = tot[lane * (kThreads / 32) + j];
+      s += mine[j];
+    }
+    float pre = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float x = __shfl_up_sync(kFull, pre, o);
+      if (lane >= o) pre += x;
+    }
+    float off = pre - s;  // exclusive offset of this lane's first chunk
+#pragma unroll
+    for (int j = 0; j < kThreads / 32; ++j) {
+      tot[lane * (kThreads / 32) + j] = off;
+      off += mine[j];
+    }
+  }
+  __syncthreads();
+  const float off = tot[tid];
+  for (int i = i0; i < i1; ++i) v[i] += off;
+  __syncthreads();
+}
+
+// Sampling over n <= kMaxCandCap candidates by one CTA, with warp_sample's
+// rules ("Understanding Inference for Systems Engineers", section 3.8):
+// candidates come in ascending token order (lg, tk: logits and tokens in
+// global memory).  The (logit, token) keys are sorted ascending by a bitonic
+// network; the top-k threshold is the logit k places from the top; weights
+// exp((logit - max) / temperature) are prefix-summed in that order and the
+// prefix with mass <= 1 - top_p is removed (never the last); the kept weights
+// are then prefix-summed in token order and the draw is the first candidate
+// whose sum exceeds u times the total.  Every sum has a fixed order.
+// Returns the chosen candidate index (all threads), or -1 with nan = 1.
+__device__ int block_sample(const StepParams& p, const float* lg, const int32_t* tk, int n, float u,
+                            unsigned char* smem, int& nan) {
+  const int tid = threadIdx.x;
+  int npad = 1;
+  while (npad < n) npad <<= 1;
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
+  float* wsort = reinterpret_cast<float*>(smem + (size_t)kMaxCandCap * 8);
+  float* wtok = wsort + kMaxCandCap;
+  float* tot = wtok + kMaxCandCap;
+  int* pick = reinterpret_cast<int*>(tot + kThreads);
+  int bad = 0;
+  for (int i = tid; i < npad; i += kThreads) {
+    unsigned long long key = ~0ull;
+    if (i < n) {
+      float l = __ldcg(lg + i);
+      if (!(l == l)) bad = 1;
+      if (l == 0.f) l = 0.f;  // -0 ties with +0
+      uint32_t bits = __float_as_uint(l);
+      bits = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);  // ascending float order
+      key = ((unsigned long long)bits << 32) | (uint32_t)__ldcg(tk + i);
+    }
+    keys[i] = key;
+  }
+  nan = __syncthreads_or(bad);
+  if (nan) return -1;
+  for (int k = 2; k <= npad; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < npad; i += kThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = keys[i], c = keys[ixj];
+          if ((a > c) == ((i & k) == 0)) {
+            keys[i] = c;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  auto logit_of = [&](unsigned long long key) {
+    uint32_t bits = (uint32_t)(key >> 32);
+    bits = (bits & 0x80000000u) ? (bits & 0x7fffffffu) : ~bits;
+    return __uint_as_float(bits);
+  };
+  const float m = logit_of(keys[n - 1]);
+  const float tau = (p.top_k > 0 && p.top_k < n) ? logit_of(keys[n - p.top_k]) : -INFINITY;
+  for (int i = tid; i < n; i += kThreads) {
+    const float l = logit_of(keys[i]);
+    wsort[i] = l >= tau ? expf((l - m) * p.inv_temp) : 0.f;
+  }
+  __syncthreads();
+  if (p.top_p < 1.f) {
+    for (int i = tid; i < n; i += kThreads) wtok[i] = wsort[i];
+    __syncthreads();
+    block_scan_inclusive(wtok, n, tot);  // ascending (logit, token) order
+    const float cut = (1.f - p.top_p) * wtok[n - 1];
+    for (int i = tid; i < n - 1; i += kThreads)
+      if (wsort[i] > 0.f && wtok[i] <= cut) wsort[i] = 0.f;
+    __syncthreads();
+  }
+  // back to token order: a candidate's index is its token's rank among the candidates
+  for (int i = tid; i < n; i += kThreads) {
+    const int32_t t = (int32_t)(uint32_t)keys[i];
+    int lo = 0, hi = n;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldcg(tk + mid) < t) lo = mid + 1; else hi = mid;
+    }
+    wtok[lo] = wsort[i];
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) wsort[i] = wtok[i];  // keep the weights; scan a copy
+  if (tid == 0) {
+    pick[0] = INT_MAX;
+    pick[1] = -1;
+  }
+  __syncthreads();
+  block_scan_inclusive(wtok, n, tot);
+  const float target = u * wtok[n - 1];
+  for (int i = tid; i < n; i += kThreads) {
+    if (wsort[i] > 0.f) {
+      atomicMax(&pick[1], i);
+      if (wtok[i] > target) atomicMin(&pick[0], i);
+    }
+  }
+  __syncthreads();
+  const int slot = pick[0] != INT_MAX ? pick[0] : pick[1];
+  __syncthreads();
+  return slot;
 }
 
 template <bool kConst, int NCH>
@@ -1611,6 +1797,7 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
     cfg.dynamicSmemBytes = xbytes;
     return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH>, p);
   }
+  if (head == kHeadSparse && p.smp) cfg.dynamicSmemBytes = sample_smem_offset(p, tiles) + kSampleSmem;
   if (head == kHeadSparse) return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH>, p);
   return cudaLaunchKernelEx(&cfg, dense_step_kernel<kConst, NCH>, p);
 }
