@@ -222,3 +222,24 @@ def test_union_gemm_host_equals_graph(tcd):
     (_, h), = _run_head(tcd, "batched", tcd.HEAD_UNION_GEMM, mode="host")
     for x, y in zip(g, h):
         assert np.array_equal(x, y)
+
+
+def test_wide_batch_equals_two_narrow_batches(tcd):
+    """Above the SM count the one-CTA step stages the hidden state in shared
+    memory (two CTAs per SM); its results equal those of two smaller batches
+    decoded with the register-resident variant, bit for bit."""
+    w = workload("tensor_batch")
+    B = 256
+    hid = w.hidden_states(0, B)
+    ctx, _ = make_ctx(tcd, "tensor_batch", max_batch=B)
+    buf = DecodeBuffers(w.max_steps, B, w.hidden, w.max_steps)
+    buf.load(hid)
+    wide = buf.run(ctx, w.k)
+    half = DecodeBuffers(w.max_steps, B // 2, w.hidden, w.max_steps)
+    for h in range(2):
+        half.load(hid[:, h * (B // 2):(h + 1) * (B // 2)])
+        out = half.run(ctx, w.k)
+        for i in range(4):
+            assert np.array_equal(out[i], wide[i][h * (B // 2):(h + 1) * (B // 2)])
+    ctx.close()
+    assert np.all(wide[3] == 0)

@@ -142,6 +142,7 @@ struct StepParams {
   float* smp_lg;
   int32_t* smp_tok;
   int32_t* smp_edge;
+  int32_t wide;             // batch above the SM count: the one-CTA step stages x in shared memory
 };
 
 // Cumulative counters kept by the kernels (one atomic per launch / per sequence step).

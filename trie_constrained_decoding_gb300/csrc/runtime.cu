@@ -297,6 +297,7 @@ StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
   p.smp_lg = c->d_smp_lg;
   p.smp_tok = c->d_smp_tok;
   p.smp_edge = c->d_smp_edge;
+  p.wide = B > c->num_sms ? 1 : 0;
   return p;
 }
 

@@ -1059,8 +1059,10 @@ __device__ int block_sample(const StepParams& p, const float* lg, const int32_t*
   return slot;
 }
 
-template <bool kConst, int NCH>
-__global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams p) {
+// kXs: the hidden state staged in shared memory instead of registers, so two
+// CTAs fit an SM (for batches larger than the SM count: one wave, not two).
+template <bool kConst, int NCH, bool kXs = false>
+__global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ Step1Shared sh;
   pdl_enter();
@@ -1093,8 +1095,8 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
     const uint16_t* x = hidden_row(p, s, b);
     if (p.device_form && tid == 32 && s.len + 1 < p.max_steps)
       prefetch_l2(x + (size_t)p.B * p.H, (uint32_t)p.H * 2u);  // the next step's hidden state
-    XFrag<NCH> xf;
-    if constexpr (NCH > 0) {
+    XFrag<kXs ? 0 : NCH> xf;
+    if constexpr (NCH > 0 && !kXs) {
       xf.load(x, lane);
     } else {
       for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
@@ -1123,7 +1125,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
         sh.err = 0;
         sh.pid = s.pre_pid;
       }
-      if constexpr (NCH == 0) __syncthreads();  // x staged in shared memory by all threads
+      if constexpr (NCH == 0 || kXs) __syncthreads();  // x staged in shared memory by all threads
     }
     if (!err) {
       for (int l = warp; l < n; l += kWarps) {
@@ -1144,8 +1146,13 @@ __global__ void __launch_bounds__(kThreads) sparse_step1_kernel(const StepParams
           __syncwarp();
           // If this candidate wins, its child's rows are the next step's reads: start them towards L2 now.
           if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].a.x * p.H, (uint32_t)p.H * 2u);
+          if constexpr (kXs) {
 #pragma unroll
-          for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xf.v[i], acc);
+            for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xs[i * 32 + lane], acc);
+          } else {
+#pragma unroll
+            for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xf.v[i], acc);
+          }
         } else {
           const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
           if (lane == 0) sh.spec_n[l] = sn;
@@ -1794,6 +1801,12 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
   cfg.numAttrs = pdl ? 1 : 0;
   if (head == kHeadSparse && p.pre) {
     cfg.gridDim = dim3(1, p.B);
+    if constexpr (NCH >= 8) {
+      if (p.wide) {
+        cfg.dynamicSmemBytes = (size_t)nch * 16;
+        return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, true>, p);
+      }
+    }
     cfg.dynamicSmemBytes = xbytes;
     return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH>, p);
   }
