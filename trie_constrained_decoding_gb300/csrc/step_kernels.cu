@@ -42,8 +42,8 @@ namespace tcd {
 __constant__ int32_t c_walk[TC_CONST_CAPACITY_BYTES / 4];
 
 // Sampling over one sequence's candidates by a whole CTA (defined below).
-__device__ int block_sample(const StepParams& p, const float* lg, const int32_t* tk, int n, float u,
-                            unsigned char* smem, int& nan);
+__device__ __noinline__ int block_sample(const StepParams& p, const float* lg, const int32_t* tk, int n, float u,
+                                         unsigned char* smem, int& nan);
 
 namespace {
 
@@ -634,13 +634,13 @@ __device__ __forceinline__ void stop_out_of_steps(const StepParams& p, const Seq
 __host__ __device__ __forceinline__ size_t sample_smem_offset(const StepParams& p, int tiles) {
   const bool staged = !(p.H == 256 || p.H == 2048 || p.H == 4096);
   const size_t x = staged ? (size_t)(p.H >> 3) * 16 : 0;
-  const size_t lists = 2 * (size_t)sparse_local_cap(p.cand_cap, tiles) * sizeof(int32_t);
+  const size_t lists = 3 * (size_t)sparse_local_cap(p.cand_cap, tiles) * sizeof(int32_t);
   return (x + lists + 127) & ~(size_t)127;
 }
 
 // Fold the per-warp bests, combine the CTAs of sequence b, let the last CTA
 // apply the transition; then, in a loop-control launch, set the loop condition.
-template <bool kConst>
+template <bool kConst, bool kSmp = false>
 __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int mode,
                           float wl, int32_t wt, int32_t we, StepShared& sh, int active) {
   // mode: 0 = idle (stopped or failed before this step), 1 = active, 2 = out of steps now.
@@ -691,7 +691,7 @@ __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kCon
     }
     __syncthreads();
     if (sh.last) {
-      if (p.smp && !sh.err && sh.ncand > 0) {
+      if (kSmp && !sh.err && sh.ncand > 0) {
         // Sampling: the draw replaces the fold's argmax (all candidates' logits
         // were left in the sequence's scratch rows by their CTAs).
         extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -775,7 +775,9 @@ __device__ __forceinline__ void pdl_enter() {
   pdl_trigger();
 }
 
-template <bool kConst, int NCH>
+// kSmp: sampling instead of the argmax (a separate instantiation, so the greedy
+// kernel carries none of it).
+template <bool kConst, int NCH, bool kSmp = false>
 __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ StepShared sh;
@@ -790,6 +792,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   uint4* xs = reinterpret_cast<uint4*>(smem_raw);
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
   int32_t* s_edge = s_tok + local_cap;
+  float* s_lg = reinterpret_cast<float*>(s_edge + local_cap);  // sampling only
   // A node needs one CTA per kWarps of its edges: the others leave at once
   // (deep nodes of a wide catalog have a few edges, its root hundreds).
   int A = T;
@@ -820,17 +823,23 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
         const int32_t tok = s_tok[l];
         const float v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
         if (better(v, tok, wl, wt)) { wl = v; wt = tok; we = s_edge[l]; }
-        if (p.smp && lane == 0) {  // by candidate rank, for the sequence's last CTA
-          const size_t r = (size_t)b * p.cand_cap + (size_t)l * A + t;
-          p.smp_lg[r] = v;
-          p.smp_tok[r] = tok;
-          p.smp_edge[r] = s_edge[l];
-          __threadfence();
+        if (kSmp && lane == 0) s_lg[l] = v;
+      }
+      if constexpr (kSmp) {
+        // Every candidate's logit, token and edge go to the sequence's scratch
+        // rows by candidate rank, for its last CTA (kept out of the loop above).
+        __syncthreads();
+        for (int i = tid; i < nlocal; i += kThreads) {
+          const size_t r = (size_t)b * p.cand_cap + (size_t)i * A + t;
+          p.smp_lg[r] = s_lg[i];
+          p.smp_tok[r] = s_tok[i];
+          p.smp_edge[r] = s_edge[i];
         }
+        __threadfence();
       }
     }
   }
-  step_tail<kConst>(p, w, s, b, mode, wl, wt, we, sh, A);
+  step_tail<kConst, kSmp>(p, w, s, b, mode, wl, wt, we, sh, A);
 }
 
 // ---------------------------------------------------------------- one-CTA sparse step
@@ -957,6 +966,8 @@ __device__ __forceinline__ void block_scan_inclusive(float* v, int n, float* tot
   __syncthreads();
 }
 
+// (Not inlined: a call kept out of line leaves the greedy path's register
+// allocation as it was.)
 // Sampling over n <= kMaxCandCap candidates by one CTA, with warp_sample's
 // rules ("Understanding Inference for Systems Engineers", section 3.8):
 // candidates come in ascending token order (lg, tk: logits and tokens in
@@ -967,8 +978,8 @@ __device__ __forceinline__ void block_scan_inclusive(float* v, int n, float* tot
 // are then prefix-summed in token order and the draw is the first candidate
 // whose sum exceeds u times the total.  Every sum has a fixed order.
 // Returns the chosen candidate index (all threads), or -1 with nan = 1.
-__device__ int block_sample(const StepParams& p, const float* lg, const int32_t* tk, int n, float u,
-                            unsigned char* smem, int& nan) {
+__device__ __noinline__ int block_sample(const StepParams& p, const float* lg, const int32_t* tk, int n, float u,
+                                         unsigned char* smem, int& nan) {
   const int tid = threadIdx.x;
   int npad = 1;
   while (npad < n) npad <<= 1;
@@ -1810,7 +1821,10 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
     cfg.dynamicSmemBytes = xbytes;
     return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH>, p);
   }
-  if (head == kHeadSparse && p.smp) cfg.dynamicSmemBytes = sample_smem_offset(p, tiles) + kSampleSmem;
+  if (head == kHeadSparse && p.smp) {
+    cfg.dynamicSmemBytes = sample_smem_offset(p, tiles) + kSampleSmem;
+    return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH, true>, p);
+  }
   if (head == kHeadSparse) return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH>, p);
   return cudaLaunchKernelEx(&cfg, dense_step_kernel<kConst, NCH>, p);
 }
@@ -1819,6 +1833,8 @@ template <bool kConst, int NCH>
 cudaError_t prepare_one() {
   constexpr int kSmem = kMaxDynamicSmem;
   cudaError_t e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(dense_step_kernel<kConst, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
 }
