@@ -236,6 +236,31 @@ def oracle_baseline(w, seconds: float, head: str = "sparse"):
                       f"fp64 oracle ({head} head), single process"}
 
 
+def oracle_dense_steps(w, seconds: float):
+    """The oracle's literal dense pipeline (every vocabulary logit, then the
+    mask, then the argmax): first decode steps of successive queries, one
+    process, for about `seconds` (at least one step)."""
+    from oracle import chars as C
+    from oracle import decode as D
+    from oracle import grammar as G
+    if w.char_strings is not None:
+        trie = C.CharGrammar(w.char_strings, w.char_vocab, w.sep_id, w.stop_id)
+    else:
+        trie = G.compile_catalog(w.catalog, w.sep_id, w.stop_id, w.vocab, max_fanout=w.max_fanout)
+    emb = w.embedding()
+    hid = w.hidden_states(0, 8, steps=1)
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        D.greedy_decode(trie, w.k, emb, hid[:, steps % 8], 1, head="dense")
+        steps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": steps / dt, "unit": "steps/s", "cores": 1,
+            "sample": f"first decode step of {steps} '{w.name}' queries, fp64 oracle, dense head"}
+
+
 def _oracle_worker(name, shm_name, emb_shape, seconds, worker, n_workers, n_batches, head, ready, start, results):
     from multiprocessing import shared_memory
     shm = shared_memory.SharedMemory(name=shm_name)
@@ -450,6 +475,8 @@ def run_ours(args):
         cpu = {k: one[k] for k in ("value", "unit", "cores", "kind", "sample")}
         cpu["tokens_per_s"] = one["tokens_per_s"]
         cpu["all_cores_pool"] = {k: pool[k] for k in ("value", "unit", "cores", "tokens_per_s", "sample")}
+        if B == 1:   # the dense-logits-then-mask oracle, on a small subset (every vocabulary row per step)
+            cpu["dense_head"] = oracle_dense_steps(w, min(6.0, args.cpu_seconds / 2))
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": dev_ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
