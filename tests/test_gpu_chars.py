@@ -119,3 +119,22 @@ def test_char_grammar_refusals(tcd):
         ctx.reset(2, 9)
     assert e.value.name == "TC_ERR_UNSUPPORTED"
     ctx.close()
+
+
+@pytest.mark.parametrize("head", ["union", "dense_gemm"])
+def test_char_tiny_gemm_heads_bitexact(tcd, head):
+    """The GEMM heads walk the same compiled CSR: bit-exact on integer inputs."""
+    w = workload("char_tiny")
+    B = 32
+    hid = w.hidden_states(100, B)
+    ctx, _ = make_ctx(tcd, "char_tiny", max_batch=B)
+    buf = DecodeBuffers(w.max_steps, B, w.hidden, w.max_steps)
+    buf.load(hid)
+    h = tcd.HEAD_UNION_GEMM if head == "union" else tcd.HEAD_DENSE_GEMM
+    out = buf.run(ctx, w.k, head=h)
+    sparse = buf.run(ctx, w.k)
+    ctx.close()
+    assert np.all(out[3] == 0)
+    check_against_oracle("char_tiny", hid, out, w.k, w.max_steps, exact=True)
+    for a, b in zip(out, sparse):
+        assert np.array_equal(a, b)
