@@ -613,7 +613,9 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     if head in (tcd.HEAD_SPARSE, tcd.HEAD_DENSE):
         n_j = min(len(qids), 500 if B == 1 else 16)
         rates = {}
-        for name, fl in (("plain", 0), ("jump_forward", tcd.FLAG_JUMP_FORWARD)):
+        per_query = {}       # decode steps of each query under forced continuations (same with logits)
+        for name, fl in (("plain", 0), ("jump_forward", tcd.FLAG_JUMP_FORWARD),
+                         ("jump_forward_with_logits", tcd.FLAG_JUMP_FORWARD | tcd.FLAG_FORCED_LOGITS)):
             steps = toks_n = 0
             for q in sorted(set(qids[:n_j])):      # untimed: the exact step counts of each variant
                 hid_buf.copy_(dev_hidden[q])
@@ -631,7 +633,10 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
                 n = lens.cpu().numpy()
                 lg = logits.cpu().numpy()
                 forced = np.array([int(np.isnan(lg[b, :n[b]]).sum()) for b in range(B)])
-                steps += int((n - forced).max())
+                if name == "jump_forward":
+                    per_query[q] = int((n - forced).max())
+                # with logits the forced positions are not NaN: same decisions as jump_forward
+                steps += per_query[q] if name == "jump_forward_with_logits" else int((n - forced).max())
                 toks_n += int(n.sum())
             torch.cuda.synchronize()
             ms = sum(x.elapsed_time(y) for x, y in evs)

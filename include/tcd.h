@@ -108,6 +108,16 @@ enum {
  */
 #define TC_FLAG_JUMP_FORWARD 0x100
 
+/*
+ * Or-ed in together with TC_FLAG_JUMP_FORWARD: forced tokens keep their
+ * logits.  Each forced position still takes no head decision, but its token's
+ * embedding row is dotted with that position's hidden state (the head's lane
+ * map and reduction, so the logit equals the plain decode's bit for bit):
+ * tokens and logits are those of the decode without either flag, at one row
+ * read per forced token.  Alone: TC_ERR_INVALID_ARG.
+ */
+#define TC_FLAG_FORCED_LOGITS 0x200
+
 /* Bytes of __constant__ memory reserved for the header part of one walk image. */
 #define TC_CONST_CAPACITY_BYTES (63 * 1024)
 

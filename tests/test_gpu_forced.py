@@ -149,3 +149,26 @@ def test_jump_rejected_where_unsupported(tcd):
         ctx.step(buf.hid[0], tok, head=tcd.HEAD_SPARSE | tcd.FLAG_JUMP_FORWARD)
     assert e.value.name == "TC_ERR_INVALID_ARG"
     ctx.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "large_head", "unstructured", "char_tools"])
+def test_forced_logits_equal_the_plain_decode(tcd, name):
+    """With TC_FLAG_FORCED_LOGITS forced positions still take no head decision
+    but carry their logit: tokens and logits equal the plain decode's bit for
+    bit (one-CTA and multi-CTA steps)."""
+    w = workload(name)
+    B = 8 if w.batch <= 8 else w.batch
+    hid = w.hidden_states(0, B)
+    flags = tcd.HEAD_SPARSE | tcd.FLAG_JUMP_FORWARD | tcd.FLAG_FORCED_LOGITS
+    out, st = _run(tcd, name, hid, B, flags)
+    plain, _ = _run(tcd, name, hid, B, tcd.HEAD_SPARSE)
+    for a, b in zip(out, plain):
+        assert np.array_equal(a, b)
+    assert st["forced"] > 0 and not np.isnan(out[1]).any()
+
+
+def test_forced_logits_needs_jump(tcd):
+    w = workload("tiny")
+    with pytest.raises(tcd.TcError) as e:
+        _run(tcd, "tiny", w.hidden_states(0, 2), 2, tcd.HEAD_SPARSE | tcd.FLAG_FORCED_LOGITS)
+    assert e.value.name == "TC_ERR_INVALID_ARG"

@@ -30,6 +30,7 @@ RES_AUTO, RES_CONST, RES_GLOBAL = 0, 1, 2
 BIND_LIVE_COUNTS = 0x10        # or-ed into bind's residency: per-sequence live-count arrays for every k
 HEAD_SPARSE, HEAD_DENSE, HEAD_UNION_GEMM, HEAD_DENSE_GEMM = 0, 1, 2, 3
 FLAG_JUMP_FORWARD = 0x100      # or-ed into `head` of decode / decode_graph: forced tokens skip the head
+FLAG_FORCED_LOGITS = 0x200     # with FLAG_JUMP_FORWARD: forced tokens still get their logits
 STAT_SLOTS = 5
 TC_ERR_EMPTY_MASK, TC_ERR_NO_LIVE_EDGE, TC_ERR_MAX_STEPS, TC_ERR_BOUNDS = 16, 17, 18, 19
 CONST_CAPACITY_BYTES = 63 * 1024

@@ -130,6 +130,7 @@ struct StepParams {
   HeadScratch hs;           // GEMM heads only
   Cand* pre;                // [B, 32] precomputed candidate lists (one-CTA sparse step), or null
   int32_t jump;             // 1: emit forced tokens without the head after each decision (device form only)
+  int32_t forced_logits;    // 1: still compute a forced token's logit (one row dot)
   int32_t iv;               // 1: read-only no-repeat state (rank ranges + banned ranks); 0: cnt/spent arrays
   // Sampling instead of the argmax (one-CTA sparse step only)
   int32_t smp;              // 1: sample

@@ -367,6 +367,11 @@ tc_status check_decode_args(tc_ctx* c, const void* hidden, int32_t n_steps, int3
   if (batch < 1 || batch > c->max_batch) return TC_ERR_CAPACITY;
   if (k < 1 || k > c->bound->n_strings) return TC_ERR_K_RANGE;
   if (max_steps < 1 || max_steps > n_steps) return TC_ERR_INVALID_ARG;
+  if ((head & TC_FLAG_FORCED_LOGITS) && !(head & TC_FLAG_JUMP_FORWARD)) {
+    set_error_message("TC_FLAG_FORCED_LOGITS needs TC_FLAG_JUMP_FORWARD");
+    return TC_ERR_INVALID_ARG;
+  }
+  head &= ~TC_FLAG_FORCED_LOGITS;
   if (head & TC_FLAG_JUMP_FORWARD) {
     head &= ~TC_FLAG_JUMP_FORWARD;
     if (head != TC_HEAD_SPARSE && head != TC_HEAD_DENSE) {
@@ -398,7 +403,7 @@ tc_status check_sampling(tc_ctx* c, const DevGrammar* g, int head, const tc_samp
     set_error_message("sampling: temperature must be positive and finite, top_k >= 0, 0 <= top_p <= 1");
     return TC_ERR_INVALID_ARG;
   }
-  if ((head & ~TC_FLAG_JUMP_FORWARD) != TC_HEAD_SPARSE || !g) {
+  if ((head & ~(TC_FLAG_JUMP_FORWARD | TC_FLAG_FORCED_LOGITS)) != TC_HEAD_SPARSE || !g) {
     set_error_message("sampling: sparse head only");
     return TC_ERR_UNSUPPORTED;
   }
@@ -513,9 +518,10 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
   p.cond = (unsigned long long)cond;
   p.device_form = 1;
   p.jump = (key.head & TC_FLAG_JUMP_FORWARD) ? 1 : 0;
+  p.forced_logits = (key.head & TC_FLAG_FORCED_LOGITS) ? 1 : 0;
   p.iv = r.iv;
   apply_sampling(p, key.smp);
-  const int head = key.head & ~TC_FLAG_JUMP_FORWARD;
+  const int head = key.head & ~(TC_FLAG_JUMP_FORWARD | TC_FLAG_FORCED_LOGITS);
   // The body runs kLoopUnroll steps; only the last sets the loop condition.
   // A sequence that has stopped makes the remaining steps of the body no-ops.
   for (int u = 0; u < kLoopUnroll; ++u) {

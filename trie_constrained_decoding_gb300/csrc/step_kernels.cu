@@ -501,9 +501,19 @@ __device__ __forceinline__ void forced_chain(const StepParams& p, const WalkRd<k
       }
       break;
     }
+    float v = __int_as_float(0x7fc00000);  // no head read: NaN
+    if (p.forced_logits) {
+      // Requested anyway: the forced token's own row against this position's
+      // hidden state, with the head's lane map (the same value bit for bit).
+      const uint4* r4 = reinterpret_cast<const uint4*>(p.emb + (size_t)only.a.x * p.H);
+      const uint4* x4 = reinterpret_cast<const uint4*>(p.hidden + ((size_t)ns.len * p.B + b) * p.H);
+      float acc = 0.f;
+      for (int c = lane; c < (p.H >> 3); c += 32) acc = dot8(ld_row(r4 + c), __ldg(x4 + c), acc);
+      v = warp_sum(acc);
+    }
     if (lane == 0) {
       p.tok_out[(size_t)b * p.out_stride + ns.len] = only.a.x;
-      p.logit_out[(size_t)b * p.out_stride + ns.len] = __int_as_float(0x7fc00000);
+      p.logit_out[(size_t)b * p.out_stride + ns.len] = v;
     }
     ns.len += 1;
     ++forced;
