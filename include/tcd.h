@@ -48,7 +48,7 @@ typedef enum tc_status {
   TC_ERR_TOKEN_RANGE = 5,        /* a token id outside [0, vocab) */
   TC_ERR_EMPTY_STRING = 6,       /* a catalog string has no tokens */
   TC_ERR_K_RANGE = 7,            /* k < 1 or k > number of catalog strings */
-  TC_ERR_CONST_CAPACITY = 8,     /* constant residency requested but the walk image does not fit */
+  TC_ERR_CONST_CAPACITY = 8,     /* constant residency requested but the walk image's header part does not fit */
   TC_ERR_NOT_BOUND = 9,          /* no grammar bound, or no tc_reset since binding */
   TC_ERR_CAPACITY = 10,          /* batch > max_batch or max fan-out > the candidate buffer */
   TC_ERR_UNSUPPORTED = 11,       /* shape the kernels do not handle (e.g. hidden % 8 != 0) */
@@ -62,9 +62,10 @@ typedef enum tc_status {
 
 /* Grammar residency (tc_bind_grammar). */
 enum {
-  TC_RES_AUTO = 0,    /* constant memory when the walk image fits, else global memory */
-  TC_RES_CONST = 1,   /* walk image in __constant__ memory (at most TC_CONST_CAPACITY_BYTES) */
-  TC_RES_GLOBAL = 2   /* walk image in global memory, read through the read-only cache */
+  TC_RES_AUTO = 0,    /* constant memory when the walk image's header part fits, else global memory */
+  TC_RES_CONST = 1,   /* header part (node ranges, pointer ranks) in __constant__ memory, at most
+                         TC_CONST_CAPACITY_BYTES; edge records always in global memory */
+  TC_RES_GLOBAL = 2   /* the whole walk image in global memory, read through the read-only cache */
 };
 
 /*
@@ -260,9 +261,10 @@ void tc_ctx_destroy(tc_ctx* ctx);
  * Uploads the trie's image to device memory owned by the context (once per
  * distinct trie content; the trie may be freed afterwards) and allocates its
  * per-sequence state for max_batch sequences.  residency is TC_RES_AUTO,
- * TC_RES_CONST or TC_RES_GLOBAL; AUTO picks CONST when the walk image is at
- * most TC_CONST_CAPACITY_BYTES.  With CONST the image is copied into the
- * device's __constant__ bank on `stream` now, before any later tc_step, and
+ * TC_RES_CONST or TC_RES_GLOBAL (optionally or-ed with TC_BIND_LIVE_COUNTS);
+ * AUTO picks CONST when the walk image's header part (tc_trie_info's
+ * header_bytes) is at most TC_CONST_CAPACITY_BYTES.  With CONST that part is
+ * copied into the device's __constant__ bank on `stream` now, before any later tc_step, and
  * as the first node of any graph captured for it.  There is one constant
  * image per device: contexts that use different CONST grammars on
  * concurrently running streams race; use GLOBAL for that.

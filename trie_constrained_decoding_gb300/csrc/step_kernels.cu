@@ -7,15 +7,20 @@
 // tie-break, advance; section "The sparse output layer": one tied-embedding
 // dot product per legal candidate over a fixed grid).
 //
-// Grid: (tiles, B) CTAs of 256 threads.  Every CTA of sequence b filters the
-// node's edges itself (a few hundred bytes of cached reads), so no second
-// launch is needed to publish the candidate list.  Candidate rank r belongs
-// to CTA r % tiles; its warps gather embedding rows with 16-byte loads and
-// reduce each dot product with a fixed shuffle tree.  With several CTAs per
-// sequence each leaves its best (logit, token) in a fixed slot and the last
-// CTA to arrive (atomic ticket after a fence, no waiting) folds the slots in
-// slot order and applies the transition.
-//
+// Two step kernels serve the sparse head.  For grammars whose nodes have at
+// most 32 edges, sparse_step1_kernel gives each sequence one CTA: the
+// candidates come from a list the previous step computed, each warp gathers a
+// candidate's embedding row and meanwhile computes that candidate's child
+// legal set, and the winner's set becomes the next step's list.  Otherwise
+// sparse_step_kernel gives each sequence up to `tiles` CTAs (one wave): every
+// CTA the node needs filters the node's edges itself (a few hundred bytes of
+// cached reads), so no second launch publishes the candidate list; candidate
+// rank r belongs to CTA r % active; each CTA leaves its best (logit, token) in
+// a fixed slot and the last to arrive (atomic ticket after a fence, no
+// waiting) folds the slots in slot order and applies the transition.  Rows
+// are gathered with 16-byte loads and each dot product is reduced by a fixed
+// shuffle tree.
+
 // Device form (the graph loop body): sequence b at its own step t = len_b
 // reads hidden[t, b] and writes toks[b, t]; a live sequence's length equals
 // the loop iteration, so no shared step counter is read.  The launch flagged
