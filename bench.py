@@ -135,19 +135,29 @@ def sparse_kernel_name(max_fanout: int) -> str:
     return "sparse_step1_kernel" if max_fanout <= 32 else "sparse_step_kernel"
 
 
+def source_code_sha256(path: str) -> str:
+    """sha256 of a source file's code: `//` comments, surrounding blanks and
+    empty lines removed, so that comment edits keep a capture valid."""
+    import hashlib
+    lines = []
+    for line in open(path, encoding="utf-8").read().splitlines():
+        code = line.split("//", 1)[0].strip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def recorded_traffic(source: str, profile: str):
     """DRAM bytes per launch recorded by the last ncu capture of a kernel, or
-    None when the kernel's source file has changed since that capture."""
-    import hashlib
+    None when the kernel's source code has changed since that capture."""
     try:
         text = open(os.path.join(ROOT, "profiles", profile)).read()
-        src = open(os.path.join(ROOT, "trie_constrained_decoding_gb300", "csrc", source), "rb").read()
+        want = source_code_sha256(os.path.join(ROOT, "trie_constrained_decoding_gb300", "csrc", source))
     except OSError:
         return None
-    want = hashlib.sha256(src).hexdigest()
     sha = traffic = None
     for line in text.splitlines():
-        if line.startswith(f"source-sha256 {source}:"):
+        if line.startswith(f"source-code-sha256 {source}:"):
             sha = line.split(":", 1)[1].strip()
         if line.startswith("dram-bytes-per-launch:"):
             traffic = float(line.split(":", 1)[1])
