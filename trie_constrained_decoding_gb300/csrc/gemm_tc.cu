@@ -35,20 +35,29 @@
 namespace tcd {
 namespace {
 
-constexpr int kThreadsG = 192;
 constexpr int kTileN = 128;
+static_assert(sizeof(TileCands) == 32 && kTileN == 32 * 4, "a TileCands record covers one 128-column tile");
 constexpr int kTileK = 64;  // bf16 elements = one 128-byte swizzle row
 constexpr uint32_t kRowBytes = 128;
 constexpr uint32_t kATileBytes = 128 * kRowBytes;     // 16 KiB per 128-row M tile
 constexpr uint32_t kBTileBytes = kTileN * kRowBytes;  // 16 KiB
 constexpr long long kWaitLimit = 1ll << 22;           // try_wait polls before giving up
 
+constexpr int kTbStride = 33;  // floats per row of an epilogue warp's 32 x 32 transpose buffer
+// Per epilogue warp: the transpose buffer, then each lane's (candidate bits, first index) pair.
+constexpr uint32_t kTbWarpBytes = 32 * kTbStride * 4 + 32 * 8;
+
+// MT: 128-row M tiles (sequences) per CTA.  Warps: TMA producer, MMA issuer,
+// then 4 * MT epilogue warps, one thread per sequence.
 template <int MT>
 struct Cfg {
-  static constexpr int kStages = MT == 2 ? 4 : 6;
+  static constexpr int kStages = MT == 2 ? 3 : 6;
   static constexpr uint32_t kStageBytes = MT * kATileBytes + kBTileBytes;
   static constexpr int kAccCols = MT * kTileN;  // TMEM columns of one accumulator
   static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr int kEpiWarps = 4 * MT;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr size_t kTbBytes = (size_t)kEpiWarps * kTbWarpBytes;
 };
 
 struct GemmHdr {
@@ -60,9 +69,7 @@ struct GemmHdr {
   int32_t abort;
   int32_t row0;
   int32_t pad;
-  int32_t active[256];               // sequence takes this step
-  uint32_t cbits[256][kTileN / 32];  // per sequence: its candidate columns in the current tile
-  int32_t cpos[256];                 // per sequence: index of its first candidate in the current tile
+  int32_t active[256];  // sequence takes this step
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -155,12 +162,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Shared-memory accesses by 32-bit shared address (explicitly in the shared
+// state space, so that they are never taken for global accesses).
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ bool gbetter(float l, int32_t c, float bl, int32_t bc) {
   return l > bl || (l == bl && c < bc);
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThreadsG, 1)
+__global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     union_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmG) {
   using C = Cfg<MT>;
@@ -170,12 +196,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   GemmHdr* hdr = reinterpret_cast<GemmHdr*>(tiles + S * C::kStageBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tiles_s = smem_u32(tiles);
-  // Launched as a programmatic dependent of the step's previous kernel: wait
-  // for its results before reading any of them, and let the next kernel start
-  // launching now.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&hdr->full[s]), 1);
@@ -183,19 +203,28 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&hdr->tfull[a]), 1);
-      mbar_init(smem_u32(&hdr->tempty[a]), 128);
+      mbar_init(smem_u32(&hdr->tempty[a]), 32 * C::kEpiWarps);
     }
     hdr->abort = 0;
-    hdr->row0 = p.row0_ptr ? *p.row0_ptr : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmG)) : "memory");
   }
-  for (int r = tid; r < MT * 128; r += kThreadsG) hdr->active[r] = (r < p.B && p.xrow[r] >= 0) ? 1 : 0;
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&hdr->tmem_base)),
                  "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // Launched as a programmatic dependent of the step's previous kernel: the
+  // setup above touches only shared memory, TMEM and the kernel's own
+  // parameters, so it overlaps that kernel's tail; its results are read only
+  // from here on.  The next kernel may start launching now.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) hdr->row0 = p.row0_ptr ? *p.row0_ptr : 0;
+  for (int r = tid; r < MT * 128; r += C::kThreads) hdr->active[r] = (r < p.B && p.xrow[r] >= 0) ? 1 : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -215,14 +244,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
       const int tile = task / KS, split = task % KS;
       const int n0 = tile * kTileN;
-      int rr0 = 0, rr1 = 0, rr2 = 0, rr3 = 0;  // this lane's four gathered rows
-      if (gather) {
-        const int c = n0 + 4 * lane;
-        rr0 = c + 0 < n_cols ? p.row_list[c + 0] : 0;
-        rr1 = c + 1 < n_cols ? p.row_list[c + 1] : 0;
-        rr2 = c + 2 < n_cols ? p.row_list[c + 2] : 0;
-        rr3 = c + 3 < n_cols ? p.row_list[c + 3] : 0;
-      }
       bool stop = false;
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const int stage = (int)(it % S);
@@ -237,12 +258,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         const uint32_t fb = smem_u32(&hdr->full[stage]);
         const int k0 = (split * KT + kt) * kTileK;
         if (lane == 0) {
+          // The stage's bytes: the activation tiles issued here, and the
+          // embedding tile (tiled here, or gathered by the epilogue warps).
           mbar_expect_tx(fb, C::kStageBytes);
           for (int m = 0; m < MT; ++m) tma_tile_2d(a_base + m * kATileBytes, &tmA, k0, row0 + m * 128, fb);
           if (!gather) tma_tile_2d(b_base, &tmB, k0, n0, fb);
         }
         __syncwarp();
-        if (gather) tma_gather4(b_base + lane * 4 * kRowBytes, &tmG, k0, rr0, rr1, rr2, rr3, fb);
       }
       if (stop || hdr->abort) break;
     }
@@ -288,71 +310,155 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int q = warp & 3;        // TMEM lane quarter this warp may read
-    const int et = q * 32 + lane;  // accumulator row = sequence within an M tile
+    // Warp w may read only TMEM lane quarter w % 4; warps 2..4MT+1 cover each
+    // quarter of each M tile once, so every thread owns one sequence.
+    const int q = warp & 3;
+    const int m = (warp - 2) >> 2;
+    const int s0 = m * 128 + q * 32;  // this warp's first sequence
+    const int b = s0 + lane;
+    const bool has = hdr->active[b] != 0;
+    const uint32_t tb = smem_u32(hdr + 1) + (uint32_t)(warp - 2) * kTbWarpBytes;  // this warp's transpose buffer
+    const uint32_t tbp = tb + 32 * kTbStride * 4;                                    // and its (bits, index) pairs
+    // Gathered embedding rows: each four-row gather is one TMA instruction
+    // per lane, and one warp's lanes issue theirs one after another, so the
+    // 32 gathers of a stage are spread over the epilogue warps (idle until the
+    // accumulator is ready): groups of four rows, kGroups per warp.
+    constexpr int kGroups = 32 / C::kEpiWarps;
+    const int g = (warp - 2) * kGroups + lane;  // this lane's group (lane < kGroups)
+    long long it = 0;
     int tl = 0;
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x, ++tl) {
       const int tile = task / KS, split = task % KS;
       const int n0 = tile * kTileN;
       const int acc = tl & 1;
-      // Which columns of this tile are this thread's sequences' candidates
-      // (computed while the MMAs of this task run).
-      for (int m = 0; m < MT; ++m) {
-        const int b = m * 128 + et;
-#pragma unroll
-        for (int w = 0; w < kTileN / 32; ++w) hdr->cbits[b][w] = 0u;
-        int lo = 0;
-        if (hdr->active[b]) {
-          const int nc = p.ncand[b];
-          const int32_t* cand = p.cand_col + (size_t)b * p.C;
-          int hi = nc;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (cand[mid] < n0) lo = mid + 1; else hi = mid;
-          }
-          for (int i = lo; i < nc; ++i) {
-            const int c = cand[i] - n0;
-            if (c >= kTileN) break;
-            hdr->cbits[b][c >> 5] |= 1u << (c & 31);
-          }
+      if (gather) {
+        int rr0 = 0, rr1 = 0, rr2 = 0, rr3 = 0;
+        if (lane < kGroups) {
+          const int c = n0 + 4 * g;
+          rr0 = c + 0 < n_cols ? p.row_list[c + 0] : 0;
+          rr1 = c + 1 < n_cols ? p.row_list[c + 1] : 0;
+          rr2 = c + 2 < n_cols ? p.row_list[c + 2] : 0;
+          rr3 = c + 3 < n_cols ? p.row_list[c + 3] : 0;
         }
-        hdr->cpos[b] = lo;
+        bool stop = false;
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int stage = (int)(it % S);
+          if (!mbar_wait(smem_u32(&hdr->empty[stage]), (uint32_t)((it / S) & 1) ^ 1u)) {
+            hdr->abort = 1;
+            stop = true;
+            break;
+          }
+          const uint32_t b_base = tiles_s + stage * C::kStageBytes + MT * kATileBytes;
+          if (lane < kGroups)
+            tma_gather4(b_base + g * 4 * kRowBytes, &tmG, (split * KT + kt) * kTileK, rr0, rr1, rr2, rr3,
+                        smem_u32(&hdr->full[stage]));
+        }
+        if (stop) break;
+      }
+      // Which columns of this tile are this sequence's candidates, and the
+      // index of the first one (found while the MMAs of this task run).
+      uint32_t cb[kTileN / 32] = {0u, 0u, 0u, 0u};
+      int cpos = 0;
+      if (p.tile_cands) {
+        if (has) {
+          const int4* r = reinterpret_cast<const int4*>(p.tile_cands + (size_t)b * p.max_tiles + tile);
+          const int4 bits = __ldg(r);
+          cpos = __ldg(reinterpret_cast<const int*>(r + 1));
+          cb[0] = (uint32_t)bits.x;
+          cb[1] = (uint32_t)bits.y;
+          cb[2] = (uint32_t)bits.z;
+          cb[3] = (uint32_t)bits.w;
+        }
+      } else if (has) {
+        const int nc = p.ncand[b];
+        const int32_t* cand = p.cand_col + (size_t)b * p.C;
+        int lo = 0, hi = nc;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (cand[mid] < n0) lo = mid + 1; else hi = mid;
+        }
+        cpos = lo;
+        for (int i = lo; i < nc; ++i) {
+          const int c = cand[i] - n0;
+          if (c >= kTileN) break;
+          const uint32_t bit = 1u << (c & 31);  // cb kept in registers: no dynamic index
+          cb[0] |= (c >> 5) == 0 ? bit : 0u;
+          cb[1] |= (c >> 5) == 1 ? bit : 0u;
+          cb[2] |= (c >> 5) == 2 ? bit : 0u;
+          cb[3] |= (c >> 5) == 3 ? bit : 0u;
+        }
       }
       if (!mbar_wait(smem_u32(&hdr->tfull[acc]), (uint32_t)((tl >> 1) & 1))) {
         hdr->abort = 1;
         break;
       }
       tc_fence_after();
-      for (int m = 0; m < MT; ++m) {
-        const int b = m * 128 + et;
-        const bool has = hdr->active[b] != 0;
-        float bl = -INFINITY;
-        int32_t bc = INT32_MAX;
-        float* sp = KS > 1 && has ? p.split_part + ((size_t)split * p.B + b) * p.C : nullptr;
-        int pos = hdr->cpos[b];
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols + m * kTileN);
+      if (KS > 1) {
+        // This split's partial sum of every candidate, at the candidate's
+        // index.  Through a 32 x 32 transpose in shared memory, one store
+        // instruction writes consecutive candidates of one sequence.
+        int pos = cpos;
 #pragma unroll 1
         for (int ch = 0; ch < kTileN / 32; ++ch) {
           uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols + m * kTileN + ch * 32), v);
-          const int c0 = n0 + ch * 32;
-          const uint32_t bits = hdr->cbits[b][ch];
+          tmem_ld32(tacc + ch * 32, v);
+          if (ch == kTileN / 32 - 1) {
+            // The sums are in registers: hand the accumulator back to the MMA warp.
+            tc_fence_before();
+            mbar_arrive(smem_u32(&hdr->tempty[acc]));
+          }
+          const uint32_t bits = (ch == 0) ? cb[0] : (ch == 1) ? cb[1] : (ch == 2) ? cb[2] : cb[3];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sts32(tb + (uint32_t)(lane * kTbStride + j) * 4u, v[j]);
+          sts64(tbp + lane * 8u, bits, (uint32_t)pos);
+          __syncwarp();
+          // Sequence s0 + s's column `lane` and its (bits, index) pair, read as
+          // shared-memory broadcasts (warp shuffles here cost far more).
+          // In two halves of 16 sequences, every load of a half before any of
+          // its stores, so that no store waits on a load.
+          float* row = p.split_part + ((size_t)split * p.B + s0) * p.C;
+#pragma unroll
+          for (int h = 0; h < 32; h += 16) {
+            uint32_t tv[16];
+            int off[16];
+            uint32_t take = 0u;
+#pragma unroll
+            for (int s = 0; s < 16; ++s) tv[s] = lds32(tb + (uint32_t)((h + s) * kTbStride + lane) * 4u);
+#pragma unroll
+            for (int s = 0; s < 16; ++s) {
+              const uint2 bp = lds64(tbp + (h + s) * 8u);
+              take |= ((bp.x >> lane) & 1u) << s;
+              off[s] = (int)bp.y + __popc(bp.x & ((1u << lane) - 1u));
+            }
+#pragma unroll
+            for (int s = 0; s < 16; ++s)
+              if ((take >> s) & 1u) row[(size_t)(h + s) * p.C + off[s]] = __uint_as_float(tv[s]);
+          }
+          __syncwarp();
+          pos += __popc(bits);
+        }
+      } else {
+        float bl = -INFINITY;
+        int32_t bc = INT32_MAX;
+#pragma unroll 1
+        for (int ch = 0; ch < kTileN / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tacc + ch * 32, v);
+          const uint32_t bits = (ch == 0) ? cb[0] : (ch == 1) ? cb[1] : (ch == 2) ? cb[2] : cb[3];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if ((bits >> j) & 1u) {
-              const float x = __uint_as_float(v[j]);
-              if (sp) {
-                sp[pos++] = x;  // this split's partial sum of candidate pos
-              } else if (gbetter(x, c0 + j, bl, bc)) {
-                bl = x;
-                bc = c0 + j;
-              }
+            const float x = __uint_as_float(v[j]);
+            if (((bits >> j) & 1u) && gbetter(x, n0 + ch * 32 + j, bl, bc)) {
+              bl = x;
+              bc = n0 + ch * 32 + j;
             }
           }
         }
-        if (has && KS == 1) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
+        tc_fence_before();
+        mbar_arrive(smem_u32(&hdr->tempty[acc]));
+        if (has) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&hdr->tempty[acc]));
     }
   }
 
@@ -394,8 +500,8 @@ cudaError_t encode_2d(CUtensorMap* m, const void* base, int64_t rows, int H, int
 }  // namespace
 
 size_t gemm_smem_bytes(int mt) {
-  return mt == 2 ? 1024 + (size_t)Cfg<2>::kStages * Cfg<2>::kStageBytes + sizeof(GemmHdr)
-                 : 1024 + (size_t)Cfg<1>::kStages * Cfg<1>::kStageBytes + sizeof(GemmHdr);
+  return mt == 2 ? 1024 + (size_t)Cfg<2>::kStages * Cfg<2>::kStageBytes + sizeof(GemmHdr) + Cfg<2>::kTbBytes
+                 : 1024 + (size_t)Cfg<1>::kStages * Cfg<1>::kStageBytes + sizeof(GemmHdr) + Cfg<1>::kTbBytes;
 }
 
 cudaError_t prepare_gemm() {
@@ -424,7 +530,7 @@ cudaError_t launch_union_gemm(const GemmParams& p, const void* hidden, int64_t r
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(num_ctas);
-  cfg.blockDim = dim3(kThreadsG);
+  cfg.blockDim = dim3(p.B > 128 ? Cfg<2>::kThreads : Cfg<1>::kThreads);
   cfg.dynamicSmemBytes = gemm_smem_bytes(p.B > 128 ? 2 : 1);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

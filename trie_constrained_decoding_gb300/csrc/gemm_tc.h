@@ -13,6 +13,14 @@ struct GemmPartial {
   int32_t col;  // INT32_MAX when the sequence has no candidate in the tile
 };
 
+// One sequence's candidates within one 128-column tile of the union GEMM,
+// written before the GEMM so that its epilogue reads them with one load.
+struct alignas(16) TileCands {
+  uint32_t bits[4];  // bit c set: column tile * 128 + c is one of the sequence's candidates
+  int32_t start;     // the sequence's candidates in earlier tiles (index of the first one in this tile)
+  int32_t pad[3];
+};
+
 struct GemmParams {
   const int64_t* xrow;       // [B] >= 0 for sequences that take this step, -1 otherwise
   const int32_t* row0_ptr;   // device: first activation row of the step in the activation map (null: 0)
@@ -23,6 +31,7 @@ struct GemmParams {
   int32_t n_cols_fixed;      // column count when n_cols_ptr is null
   const int32_t* cand_col;   // [B, C] ascending columns of each sequence's legal candidates
   const int32_t* ncand;      // [B]
+  const TileCands* tile_cands;  // [B, max_tiles] per-tile candidate records, or null (search cand_col)
   int32_t C;
   GemmPartial* part;         // [B, max_tiles] (ksplit == 1)
   int32_t max_tiles;

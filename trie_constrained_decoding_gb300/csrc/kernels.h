@@ -78,6 +78,7 @@ struct GrammarView {
 
 struct GemmPartial;  // gemm_tc.h
 struct EmbMaps;      // gemm_tc.h
+struct TileCands;    // gemm_tc.h
 
 // Scratch of the GEMM heads (candidate lists in global memory, the union of
 // legal rows, per-(sequence, column tile) partial results).
@@ -92,6 +93,7 @@ struct HeadScratch {
   int32_t* ulist;           // [V] union of legal tokens, ascending
   int32_t* umap;            // [V] token -> union index (valid for members only)
   int32_t* n_union;         // [1]
+  TileCands* tile_cands;    // [B, max_tiles] each sequence's candidates per union tile
   GemmPartial* part;        // [B, max_tiles]
   int32_t max_tiles;
   int32_t ksplit;           // K splits of the union GEMM (fixed by the hidden size)

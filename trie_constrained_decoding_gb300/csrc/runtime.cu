@@ -216,6 +216,7 @@ tc_status ensure_gemm_scratch(tc_ctx* c) {
   if (e == cudaSuccess) e = cudaMalloc(&h.n_union, 4);
   if (e == cudaSuccess) e = cudaMemset(h.n_union, 0, 4);
   if (e == cudaSuccess) e = cudaMalloc(&h.part, (size_t)c->max_batch * h.max_tiles * sizeof(GemmPartial));
+  if (e == cudaSuccess) e = cudaMalloc(&h.tile_cands, (size_t)c->max_batch * h.max_tiles * sizeof(TileCands));
   // The union GEMM splits K into tasks of 4 k-steps (256 elements) when the
   // hidden size allows; the split count depends only on the hidden size, so a
   // sequence's sums never depend on its batch-mates.
@@ -245,6 +246,7 @@ void free_gemm_scratch(tc_ctx* c) {
   cudaFree(h.umap);
   cudaFree(h.n_union);
   cudaFree(h.part);
+  cudaFree(h.tile_cands);
   cudaFree(h.split_part);
   cudaFree(h.gemm_err);
   cudaFree(h.row0);

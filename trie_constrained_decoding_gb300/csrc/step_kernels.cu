@@ -1659,15 +1659,45 @@ __global__ void __launch_bounds__(kCompactThreads) union_compact_kernel(const St
   if (tid == 0) *hs.n_union = s_warp[kCompactThreads / 32 - 1];
 }
 
-// Grid (1, B): the GEMM column of each of sequence b's candidates.
+// Grid (1, B): the GEMM column of each of sequence b's candidates, and for
+// every 128-column tile of the union the record of sequence b's candidates in
+// it (a bitmask of the columns and the index of the first one), so that the
+// GEMM's epilogue finds them with one load instead of a search.
 __global__ void __launch_bounds__(kThreads) cand_column_kernel(const StepParams p) {
+  extern __shared__ __align__(16) int32_t s_col[];  // [cand_cap]
   pdl_enter();
   const HeadScratch& hs = p.hs;
   const int b = blockIdx.y;
   const int n = hs.ncand[b];
   const int32_t* ct = hs.cand_tok + (size_t)b * p.cand_cap;
   int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
-  for (int i = threadIdx.x; i < n; i += kThreads) cc[i] = hs.umap[ct[i]];
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const int32_t col = hs.umap[ct[i]];
+    s_col[i] = col;
+    cc[i] = col;
+  }
+  __syncthreads();
+  // Columns ascend with the candidates (both follow the token order), so the
+  // candidates of tile t are the run that starts at the first column >= 128 t.
+  const int n_tiles = min((*hs.n_union + gemm_tile_cols_dev - 1) / gemm_tile_cols_dev, hs.max_tiles);
+  TileCands* rec = hs.tile_cands + (size_t)b * hs.max_tiles;
+  for (int t = threadIdx.x; t < n_tiles; t += kThreads) {
+    const int c0 = t * gemm_tile_cols_dev;
+    int lo = 0, hi = n;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_col[mid] < c0) lo = mid + 1; else hi = mid;
+    }
+    uint32_t bits[4] = {0u, 0u, 0u, 0u};
+    for (int i = lo; i < n; ++i) {
+      const int c = s_col[i] - c0;
+      if (c >= gemm_tile_cols_dev) break;
+      bits[c >> 5] |= 1u << (c & 31);
+    }
+    int4* r = reinterpret_cast<int4*>(rec + t);
+    r[0] = make_int4((int)bits[0], (int)bits[1], (int)bits[2], (int)bits[3]);
+    r[1] = make_int4(lo, 0, 0, 0);
+  }
 }
 
 // Grid (1, B): fold sequence b's column-tile partials, map the winning column
@@ -1920,7 +1950,9 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
   if (e != cudaSuccess) return e;
   if (q.hs.union_mode) {
     if ((e = launch_pdl(union_compact_kernel, dim3(1), dim3(kCompactThreads), 0, s, no_ctrl)) != cudaSuccess) return e;
-    if ((e = launch_pdl(cand_column_kernel, dim3(1, p.B), dim3(kThreads), 0, s, no_ctrl)) != cudaSuccess) return e;
+    if ((e = launch_pdl(cand_column_kernel, dim3(1, p.B), dim3(kThreads), (size_t)p.cand_cap * sizeof(int32_t), s,
+                        no_ctrl)) != cudaSuccess)
+      return e;
   }
   GemmParams gp{};
   gp.xrow = q.hs.xrow;
@@ -1932,6 +1964,7 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
   gp.n_cols_fixed = p.V;
   gp.cand_col = q.hs.cand_col;
   gp.ncand = q.hs.ncand;
+  gp.tile_cands = q.hs.union_mode ? q.hs.tile_cands : nullptr;
   gp.C = p.cand_cap;
   gp.part = q.hs.part;
   gp.max_tiles = q.hs.max_tiles;
