@@ -48,14 +48,16 @@ constexpr int kTbStride = 33;  // floats per row of an epilogue warp's 32 x 32 t
 constexpr uint32_t kTbWarpBytes = 32 * kTbStride * 4 + 32 * 8;
 
 // MT: 128-row M tiles (sequences) per CTA.  Warps: TMA producer, MMA issuer,
-// then 4 * MT epilogue warps, one thread per sequence.
+// then 8 epilogue warps: with two M tiles each takes one lane quarter of one
+// tile, with one M tile each takes one lane quarter and half of the columns.
 template <int MT>
 struct Cfg {
-  static constexpr int kStages = MT == 2 ? 3 : 6;
+  static constexpr int kStages = MT == 2 ? 3 : 5;
   static constexpr uint32_t kStageBytes = MT * kATileBytes + kBTileBytes;
   static constexpr int kAccCols = MT * kTileN;  // TMEM columns of one accumulator
   static constexpr int kTmemCols = 2 * kAccCols;
-  static constexpr int kEpiWarps = 4 * MT;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kChunks = 2 * MT;  // 32-column chunks of a tile per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr size_t kTbBytes = (size_t)kEpiWarps * kTbWarpBytes;
 };
@@ -68,9 +70,13 @@ struct GemmHdr {
   uint32_t tmem_base;
   int32_t abort;
   int32_t row0;
-  int32_t pad;
+  int32_t n_cols;
   int32_t active[256];  // sequence takes this step
 };
+// Dynamic shared memory of each configuration (1024 bytes of alignment slack)
+// within the 227 KiB a CTA may use.
+static_assert(1024 + Cfg<1>::kStages * Cfg<1>::kStageBytes + sizeof(GemmHdr) + Cfg<1>::kTbBytes <= 232448, "smem");
+static_assert(1024 + Cfg<2>::kStages * Cfg<2>::kStageBytes + sizeof(GemmHdr) + Cfg<2>::kTbBytes <= 232448, "smem");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -223,26 +229,46 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   // from here on.  The next kernel may start launching now.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (tid == 0) hdr->row0 = p.row0_ptr ? *p.row0_ptr : 0;
-  for (int r = tid; r < MT * 128; r += C::kThreads) hdr->active[r] = (r < p.B && p.xrow[r] >= 0) ? 1 : 0;
+  const int KS = p.ksplit;           // K splits per column tile (divides H / 64)
+  const int KT = p.H / kTileK / KS;  // k-steps per task
+  // Tasks: (column tile, K split, M tile); the M tiles of one (tile, split)
+  // are adjacent, so their shared embedding rows are read while still in L2.
+  const int MS = MT == 1 ? p.msplit : 1;
+  const bool gather = p.row_list != nullptr;
+  // Gathered embedding rows: each four-row gather is one TMA instruction per
+  // lane, and one warp's lanes issue theirs one after another, so the 32
+  // gathers of a stage are spread over the epilogue warps (idle until the
+  // accumulator is ready): groups of four rows, kGroups per warp.
+  constexpr int kGroups = 32 / C::kEpiWarps;
+  const int g = (warp - 2) * kGroups + lane;  // this lane's group (warp >= 2, lane < kGroups)
+  // The first task's gathered rows, read together with the step's scalars
+  // (the list holds the whole vocabulary, so the read is in bounds; entries
+  // past the union are replaced below).
+  int pre[4] = {0, 0, 0, 0};
+  if (gather && warp >= 2 && lane < kGroups) {
+    const int c = (int)(blockIdx.x / MS / KS) * kTileN + 4 * g;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pre[i] = c + i < p.n_cols_fixed ? p.row_list[c + i] : 0;
+  }
+  if (tid == 0) {
+    hdr->row0 = p.row0_ptr ? *p.row0_ptr : 0;
+    hdr->n_cols = p.n_cols_ptr ? *p.n_cols_ptr : p.n_cols_fixed;
+  }
+  for (int r = tid; r < 256; r += C::kThreads) hdr->active[r] = (r < p.B && p.xrow[r] >= 0) ? 1 : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
   const int row0 = hdr->row0;
-
-  const int n_cols = p.n_cols_ptr ? *p.n_cols_ptr : p.n_cols_fixed;
+  const int n_cols = hdr->n_cols;
   const int n_tiles = (n_cols + kTileN - 1) / kTileN;
-  const int KS = p.ksplit;           // K splits per column tile (divides H / 64)
-  const int KT = p.H / kTileK / KS;  // k-steps per task
-  const int n_tasks = n_tiles * KS;
-  const bool gather = p.row_list != nullptr;
+  const int n_tasks = n_tiles * KS * MS;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     long long it = 0;
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
-      const int tile = task / KS, split = task % KS;
+      const int mt = task % MS, tile = task / MS / KS, split = task / MS % KS;
       const int n0 = tile * kTileN;
       bool stop = false;
       for (int kt = 0; kt < KT; ++kt, ++it) {
@@ -261,7 +287,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           // The stage's bytes: the activation tiles issued here, and the
           // embedding tile (tiled here, or gathered by the epilogue warps).
           mbar_expect_tx(fb, C::kStageBytes);
-          for (int m = 0; m < MT; ++m) tma_tile_2d(a_base + m * kATileBytes, &tmA, k0, row0 + m * 128, fb);
+          for (int m = 0; m < MT; ++m) tma_tile_2d(a_base + m * kATileBytes, &tmA, k0, row0 + (mt + m) * 128, fb);
           if (!gather) tma_tile_2d(b_base, &tmB, k0, n0, fb);
         }
         __syncwarp();
@@ -313,32 +339,34 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     // Warp w may read only TMEM lane quarter w % 4; warps 2..4MT+1 cover each
     // quarter of each M tile once, so every thread owns one sequence.
     const int q = warp & 3;
-    const int m = (warp - 2) >> 2;
-    const int s0 = m * 128 + q * 32;  // this warp's first sequence
-    const int b = s0 + lane;
-    const bool has = hdr->active[b] != 0;
+    const int m = MT == 2 ? (warp - 2) >> 2 : 0;             // M tile of this warp
+    const int ch_lo = MT == 2 ? 0 : ((warp - 2) >> 2) * 2;   // its first 32-column chunk
     const uint32_t tb = smem_u32(hdr + 1) + (uint32_t)(warp - 2) * kTbWarpBytes;  // this warp's transpose buffer
     const uint32_t tbp = tb + 32 * kTbStride * 4;                                    // and its (bits, index) pairs
-    // Gathered embedding rows: each four-row gather is one TMA instruction
-    // per lane, and one warp's lanes issue theirs one after another, so the
-    // 32 gathers of a stage are spread over the epilogue warps (idle until the
-    // accumulator is ready): groups of four rows, kGroups per warp.
-    constexpr int kGroups = 32 / C::kEpiWarps;
-    const int g = (warp - 2) * kGroups + lane;  // this lane's group (lane < kGroups)
     long long it = 0;
     int tl = 0;
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x, ++tl) {
-      const int tile = task / KS, split = task % KS;
+      const int mt = task % MS, tile = task / MS / KS, split = task / MS % KS;
       const int n0 = tile * kTileN;
       const int acc = tl & 1;
+      const int s0 = (mt + m) * 128 + q * 32;  // this warp's first sequence
+      const int b = s0 + lane;
+      const bool has = hdr->active[b] != 0;
       if (gather) {
         int rr0 = 0, rr1 = 0, rr2 = 0, rr3 = 0;
         if (lane < kGroups) {
           const int c = n0 + 4 * g;
-          rr0 = c + 0 < n_cols ? p.row_list[c + 0] : 0;
-          rr1 = c + 1 < n_cols ? p.row_list[c + 1] : 0;
-          rr2 = c + 2 < n_cols ? p.row_list[c + 2] : 0;
-          rr3 = c + 3 < n_cols ? p.row_list[c + 3] : 0;
+          if (tl == 0) {
+            rr0 = c + 0 < n_cols ? pre[0] : 0;
+            rr1 = c + 1 < n_cols ? pre[1] : 0;
+            rr2 = c + 2 < n_cols ? pre[2] : 0;
+            rr3 = c + 3 < n_cols ? pre[3] : 0;
+          } else {
+            rr0 = c + 0 < n_cols ? p.row_list[c + 0] : 0;
+            rr1 = c + 1 < n_cols ? p.row_list[c + 1] : 0;
+            rr2 = c + 2 < n_cols ? p.row_list[c + 2] : 0;
+            rr3 = c + 3 < n_cols ? p.row_list[c + 3] : 0;
+          }
         }
         bool stop = false;
         for (int kt = 0; kt < KT; ++kt, ++it) {
@@ -398,12 +426,14 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         // This split's partial sum of every candidate, at the candidate's
         // index.  Through a 32 x 32 transpose in shared memory, one store
         // instruction writes consecutive candidates of one sequence.
-        int pos = cpos;
+        // This warp's chunks: [ch_lo, ch_lo + kChunks); the candidates of
+        // earlier chunks come first.
+        int pos = cpos + (ch_lo > 0 ? __popc(cb[0]) : 0) + (ch_lo > 1 ? __popc(cb[1]) : 0);
 #pragma unroll 1
-        for (int ch = 0; ch < kTileN / 32; ++ch) {
+        for (int ch = ch_lo; ch < ch_lo + C::kChunks; ++ch) {
           uint32_t v[32];
           tmem_ld32(tacc + ch * 32, v);
-          if (ch == kTileN / 32 - 1) {
+          if (ch == ch_lo + C::kChunks - 1) {
             // The sums are in registers: hand the accumulator back to the MMA warp.
             tc_fence_before();
             mbar_arrive(smem_u32(&hdr->tempty[acc]));
@@ -439,10 +469,12 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           pos += __popc(bits);
         }
       } else {
+        // Masked argmax of the tile: the warps with the first chunk take all
+        // of the tile's columns, the others only hand the accumulator back.
         float bl = -INFINITY;
         int32_t bc = INT32_MAX;
 #pragma unroll 1
-        for (int ch = 0; ch < kTileN / 32; ++ch) {
+        for (int ch = 0; ch < (ch_lo == 0 ? kTileN / 32 : 0); ++ch) {
           uint32_t v[32];
           tmem_ld32(tacc + ch * 32, v);
           const uint32_t bits = (ch == 0) ? cb[0] : (ch == 1) ? cb[1] : (ch == 2) ? cb[2] : cb[3];
@@ -457,7 +489,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&hdr->tempty[acc]));
-        if (has) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
+        if (has && ch_lo == 0) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
       }
     }
   }
@@ -529,17 +561,23 @@ cudaError_t launch_union_gemm(const GemmParams& p, const void* hidden, int64_t r
   cudaError_t e = encode_2d(&a, hidden, rows, p.H, 128);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
+  // Above 128 sequences the union GEMM takes each M tile as a task of its own
+  // (more, shorter tasks for its few column tiles); the full-vocabulary GEMM
+  // keeps both M tiles in one CTA so that every embedding tile is read once.
+  GemmParams q = p;
+  const bool two_m = p.B > 128 && p.row_list == nullptr;
+  q.msplit = p.B > 128 && !two_m ? 2 : 1;
   cfg.gridDim = dim3(num_ctas);
-  cfg.blockDim = dim3(p.B > 128 ? Cfg<2>::kThreads : Cfg<1>::kThreads);
-  cfg.dynamicSmemBytes = gemm_smem_bytes(p.B > 128 ? 2 : 1);
+  cfg.blockDim = dim3(two_m ? Cfg<2>::kThreads : Cfg<1>::kThreads);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(two_m ? 2 : 1);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.B > 128) return cudaLaunchKernelEx(&cfg, union_gemm_kernel<2>, p, a, emb.tiled, emb.gather);
-  return cudaLaunchKernelEx(&cfg, union_gemm_kernel<1>, p, a, emb.tiled, emb.gather);
+  if (two_m) return cudaLaunchKernelEx(&cfg, union_gemm_kernel<2>, q, a, emb.tiled, emb.gather);
+  return cudaLaunchKernelEx(&cfg, union_gemm_kernel<1>, q, a, emb.tiled, emb.gather);
 }
 
 }  // namespace tcd

@@ -36,6 +36,7 @@ struct GemmParams {
   GemmPartial* part;         // [B, max_tiles] (ksplit == 1)
   int32_t max_tiles;
   int32_t ksplit;            // K splits per column tile; H / 64 must be a multiple
+  int32_t msplit;            // set by the launcher: 128-sequence M tiles taken by separate tasks
   float* split_part;         // [ksplit, B, C] candidate partial sums (ksplit > 1)
   int32_t* err;              // set to 1 when a wait timed out
 };
