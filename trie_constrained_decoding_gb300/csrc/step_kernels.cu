@@ -1708,15 +1708,16 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
   pdl_enter();
   const int b = blockIdx.y, tid = threadIdx.x;
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
-  const SeqState s = p.st[b];
-  const int mode = seq_mode(p, s);
   const HeadScratch& hs = p.hs;
+  // The step's scalars are read together with the state (one round trip).
+  const SeqState s = p.st[b];
+  const int n = hs.ncand[b];
+  const int err = hs.errf[b] | *hs.gemm_err;  // a GEMM wait that timed out fails the step
+  const int n_cols = hs.union_mode ? *hs.n_union : p.V;
+  const int mode = seq_mode(p, s);
   float wl = -INFINITY;
   int32_t wt = INT_MAX, we = -1;
   if (mode == 1) {
-    const int n = hs.ncand[b];
-    const int err = hs.errf[b] | *hs.gemm_err;  // a GEMM wait that timed out fails the step
-    const int n_cols = hs.union_mode ? *hs.n_union : p.V;
     const int n_tiles = (n_cols + gemm_tile_cols_dev - 1) / gemm_tile_cols_dev;
     int32_t bc = INT_MAX;  // winning column (tile partials)
     int32_t bi = INT_MAX;  // winning candidate index (split sums)
@@ -1725,10 +1726,19 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
       // Split-K: each candidate's logit is the sum of its per-split partial
       // sums, added in split order (a fixed order, independent of the batch).
       // Candidates ascend by token, so the candidate index orders ties like the token.
+      const size_t split_stride = (size_t)p.B * p.cand_cap;
       for (int i = tid; i < n; i += kThreads) {
+        const float* sp = hs.split_part + (size_t)b * p.cand_cap + i;
         float v = 0.f;
-        for (int sidx = 0; sidx < hs.ksplit; ++sidx)
-          v += hs.split_part[((size_t)sidx * p.B + b) * p.cand_cap + i];
+        // Eight loads in flight, then added in split order.
+        for (int s0 = 0; s0 < hs.ksplit; s0 += 8) {
+          float x[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) x[j] = s0 + j < hs.ksplit ? __ldcg(sp + (size_t)(s0 + j) * split_stride) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (s0 + j < hs.ksplit) v += x[j];
+        }
         if (better(v, i, wl, bi)) {
           wl = v;
           bi = i;
