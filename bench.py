@@ -460,6 +460,8 @@ def run_ours(args):
         roof, extras = extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids[W:], head, flush,
                                     hid_buf, toks, logits, lens, status, tinfo["max_fanout"], work)
         e2e = extras.pop("e2e")
+        if world == 1 and args.workload == "large_head" and head == tcd.HEAD_SPARSE:
+            extras["sparse_head_by_batch"] = batch_size_passes(tcd, torch, dev, stream, flush)
 
     if rank != 0:
         return 0
@@ -517,6 +519,75 @@ def run_ours(args):
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def batch_size_passes(tcd, torch, dev, stream, flush):
+    """The sparse head at B=64 and B=256: the batched and tensor_batch
+    workloads (1000-tool catalog, one H=4096 embedding), decoded by the graph
+    loop with the same exact step counting and L2 flushes as the main pass, and
+    the algorithmic bytes of those steps (candidate rows and hidden states)
+    over their device time."""
+    out = {}
+    embs = {}
+    for name, n_q in (("batched", 24), ("tensor_batch", 8)):
+        w = I.WORKLOADS[name]()
+        B, S, H = w.batch, w.max_steps, w.hidden
+        key = (w.vocab, H, w.emb_kind)
+        if key not in embs:
+            bits = w.embedding()
+            embs[key] = torch.from_numpy(bits.view(np.int16)).to(f"cuda:{dev}").view(torch.bfloat16)
+            del bits
+        trie = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
+        ctx = tcd.Context(embs[key], max_batch=B, cand_cap=w.cand_cap)
+        ctx.bind(trie, {"const": tcd.RES_CONST, "global": tcd.RES_GLOBAL, "auto": tcd.RES_AUTO}[w.residency])
+        qids = list(range(n_q))
+        hh = host_hidden(w, qids)
+        hid = {q: torch.from_numpy(h.view(np.int16)).to(f"cuda:{dev}").view(torch.bfloat16) for q, h in hh.items()}
+        del hh
+        # one input buffer, as in the main pass: the captured decode graph is
+        # keyed by its arguments and reused
+        buf = torch.empty((S, B, H), dtype=torch.bfloat16, device=f"cuda:{dev}")
+        toks = torch.empty((B, S), dtype=torch.int32, device=f"cuda:{dev}")
+        logits = torch.empty((B, S), dtype=torch.float32, device=f"cuda:{dev}")
+        lens = torch.empty(B, dtype=torch.int32, device=f"cuda:{dev}")
+        status = torch.empty(B, dtype=torch.int32, device=f"cuda:{dev}")
+        steps = {}
+        for q in qids:        # untimed: the decode steps of each query batch
+            buf.copy_(hid[q])
+            ctx.decode(buf, w.k, S, toks, logits, lens, status)
+            n = lens.cpu().numpy()
+            steps[q] = (int((n + (status.cpu().numpy() != 0)).max()), int(n.sum()))
+        for q in qids[:3]:
+            buf.copy_(hid[q])
+            ctx.decode(buf, w.k, S, toks, logits, lens, status)
+        torch.cuda.synchronize()
+        ctx.raise_on_error()
+        ctx.stats(reset=True)
+        evs = []
+        for q in qids:
+            buf.copy_(hid[q])
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ctx.decode(buf, w.k, S, toks, logits, lens, status)
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        ctx.raise_on_error()
+        st = ctx.stats(reset=True)
+        sec = sum(a.elapsed_time(b) for a, b in evs) / 1000.0
+        n_steps = sum(steps[q][0] for q in qids)
+        n_tok = sum(steps[q][1] for q in qids)
+        algo = (st["cand_rows"] + st["seq_steps"]) * 2.0 * H
+        out[str(B)] = {"workload": name, "steps_per_s": n_steps / sec, "tokens_per_s": n_tok / sec,
+                       "us_per_step": sec * 1e6 / n_steps, "query_batches": n_q,
+                       "timed_work_matches_count": st["seq_steps"] == n_tok,
+                       "algorithmic_gbs": algo / sec / 1e9,
+                       "candidates_per_sequence_step": st["cand_rows"] / max(1, st["seq_steps"])}
+        ctx.close()
+        trie.close()
+        del hid, buf
+    return out
 
 
 def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, head, flush, hid_buf, toks, logits,
