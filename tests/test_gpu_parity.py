@@ -217,6 +217,41 @@ def test_union_gemm_batch_invariant(tcd):
     ctx.close()
 
 
+def test_union_gemm_ragged_m_split_equals_narrow_batches(tcd):
+    """Above 128 sequences the union GEMM runs each 128-sequence M tile as a
+    task of its own (here a full tile and a ragged one of 72); every sequence's
+    result equals the one it gets in batches of at most 128 (one M tile),
+    bit for bit, and stays within the oracle's tolerance."""
+    w = workload("batched")
+    B = 200
+    hid = w.hidden_states(0, B)
+    ctx, _ = make_ctx(tcd, "batched", max_batch=B)
+    buf = DecodeBuffers(w.max_steps, B, w.hidden, w.max_steps)
+    buf.load(hid)
+    wide = buf.run(ctx, w.k, head=tcd.HEAD_UNION_GEMM)
+    assert np.all(wide[3] == 0)
+    for lo, hi in ((0, 128), (128, 200)):
+        part = DecodeBuffers(w.max_steps, hi - lo, w.hidden, w.max_steps)
+        part.load(hid[:, lo:hi])
+        out = part.run(ctx, w.k, head=tcd.HEAD_UNION_GEMM)
+        for i in range(4):
+            assert np.array_equal(out[i], wide[i][lo:hi])
+    ctx.close()
+    check_against_oracle("batched", hid, wide, w.k, w.max_steps, exact=False, seqs=range(0, B, 8))
+
+
+def test_tiny_union_gemm_m_split_bitexact(tcd):
+    """Integer-valued inputs at B=200 (M-split union GEMM without a K split,
+    the masked-argmax epilogue): tokens and logits equal the sparse head's."""
+    w = workload("tiny")
+    (_, sp), = _run_head(tcd, "tiny", tcd.HEAD_SPARSE, batch=200)
+    (hid, un), = _run_head(tcd, "tiny", tcd.HEAD_UNION_GEMM, batch=200)
+    assert np.all(un[3] == 0)
+    for x, y in zip(sp, un):
+        assert np.array_equal(x, y)
+    check_against_oracle("tiny", hid, un, w.k, w.max_steps, exact=True, seqs=range(0, 200, 10))
+
+
 def test_union_gemm_host_equals_graph(tcd):
     (_, g), = _run_head(tcd, "batched", tcd.HEAD_UNION_GEMM, mode="graph")
     (_, h), = _run_head(tcd, "batched", tcd.HEAD_UNION_GEMM, mode="host")
