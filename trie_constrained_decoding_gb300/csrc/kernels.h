@@ -130,7 +130,8 @@ struct StepParams {
   int32_t loop_ctrl;        // 1: this launch sets the loop's condition (last step of a loop body)
   unsigned long long* stats;  // optional counters, see StatSlot
   HeadScratch hs;           // GEMM heads only
-  Cand* pre;                // [B, 32] precomputed candidate lists (one-CTA sparse step), or null
+  Cand* pre;                // [B, 32] precomputed candidate lists (sparse head), or null
+  int32_t one_cta;          // every node has at most 32 edges: the one-CTA sparse step kernel
   int32_t jump;             // 1: emit forced tokens without the head after each decision (device form only)
   int32_t forced_logits;    // 1: still compute a forced token's logit (one row dot)
   int32_t iv;               // 1: read-only no-repeat state (rank ranges + banned ranks); 0: cnt/spent arrays

@@ -294,7 +294,8 @@ StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
   p.ctrl = c->d_ctrl;
   p.stats = c->d_stats;
   p.max_steps = INT32_MAX;
-  p.pre = one_cta_sparse(g) ? g->d_pre : nullptr;
+  p.pre = g->d_pre;
+  p.one_cta = one_cta_sparse(g) ? 1 : 0;
   p.iv = g->iv;
   p.smp_lg = c->d_smp_lg;
   p.smp_tok = c->d_smp_tok;

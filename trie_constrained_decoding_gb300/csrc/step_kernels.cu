@@ -655,6 +655,30 @@ __host__ __device__ __forceinline__ size_t sample_smem_offset(const StepParams& 
 
 // Fold the per-warp bests, combine the CTAs of sequence b, let the last CTA
 // apply the transition; then, in a loop-control launch, set the loop condition.
+// In a loop-control launch (the last step of a graph loop body), set the
+// loop condition: every CTA takes a ticket and the last one reads the live
+// count; a grid of one CTA decides from its own sequence (`done_after`, read
+// by thread 0).  All threads of every CTA call it.
+__device__ __forceinline__ void loop_control(const StepParams& p, const int& done_after) {
+  if (!p.loop_ctrl) return;
+  if (gridDim.x * gridDim.y == 1) {
+    if (threadIdx.x == 0) cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, done_after ? 0u : 1u);
+    return;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t total = gridDim.x * gridDim.y;
+    const uint32_t g = atomicAdd(&p.ctrl->ticket, 1u);
+    if (g == total - 1) {
+      __threadfence();
+      const int32_t live = atomicAdd(&p.ctrl->live, 0);
+      p.ctrl->ticket = 0u;
+      cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, live > 0 ? 1u : 0u);
+    }
+  }
+}
+
 template <bool kConst, bool kSmp = false>
 __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s, int b, int mode,
                           float wl, int32_t wt, int32_t we, StepShared& sh, int active) {
@@ -743,25 +767,7 @@ __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kCon
     }
   }
 
-  if (p.loop_ctrl) {
-    if (gridDim.x * gridDim.y == 1) {
-      // The only CTA has finished its only sequence: its state decides.
-      if (tid == 0) cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, sh.done_after ? 0u : 1u);
-    } else {
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        const uint32_t total = gridDim.x * gridDim.y;
-        const uint32_t g = atomicAdd(&p.ctrl->ticket, 1u);
-        if (g == total - 1) {
-          __threadfence();
-          const int32_t live = atomicAdd(&p.ctrl->live, 0);
-          p.ctrl->ticket = 0u;
-          cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, live > 0 ? 1u : 0u);
-        }
-      }
-    }
-  }
+  loop_control(p, sh.done_after);
 }
 
 // 0: idle, 1: active, 2: live but out of steps.
@@ -792,71 +798,6 @@ __device__ __forceinline__ void pdl_enter() {
 
 // kSmp: sampling instead of the argmax (a separate instantiation, so the greedy
 // kernel carries none of it).
-template <bool kConst, int NCH, bool kSmp = false>
-__global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ StepShared sh;
-  pdl_enter();
-  const int b = blockIdx.y, t = blockIdx.x, T = gridDim.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
-  const SeqState s = p.st[b];
-  const int mode = seq_mode(p, s);
-  const int nch = p.H >> 3;
-  const int local_cap = sparse_local_cap(p.cand_cap, T);
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
-  int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
-  int32_t* s_edge = s_tok + local_cap;
-  float* s_lg = reinterpret_cast<float*>(s_edge + local_cap);  // sampling only
-  // A node needs one CTA per kWarps of its edges: the others leave at once
-  // (deep nodes of a wide catalog have a few edges, its root hundreds).
-  int A = T;
-  if (mode == 1) {
-    const int nd = s.node;
-    if (nd >= 0 && nd < p.g.n_nodes) {
-      const int fan = w.begin(nd + 1) - w.begin(nd);
-      const int need = (fan + kWarps - 1) / kWarps;
-      A = need < 1 ? 1 : (need < T ? need : T);
-    }
-  }
-
-  float wl = -INFINITY;
-  int32_t wt = INT_MAX, we = -1;
-  if (mode == 1 && t < A) {
-    const uint16_t* x = hidden_row(p, s, b);
-    XFrag<NCH> xf;
-    if constexpr (NCH > 0) {
-      xf.load(x, lane);
-    } else {
-      for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
-    }
-    filter_node<kConst>(p, w, s, b, A, t, s_tok, s_edge, sh);
-    if (!sh.err) {
-      const int nc = sh.ncand;
-      const int nlocal = nc > t ? (nc - t + A - 1) / A : 0;
-      for (int l = warp; l < nlocal; l += kWarps) {
-        const int32_t tok = s_tok[l];
-        const float v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
-        if (better(v, tok, wl, wt)) { wl = v; wt = tok; we = s_edge[l]; }
-        if (kSmp && lane == 0) s_lg[l] = v;
-      }
-      if constexpr (kSmp) {
-        // Every candidate's logit, token and edge go to the sequence's scratch
-        // rows by candidate rank, for its last CTA (kept out of the loop above).
-        __syncthreads();
-        for (int i = tid; i < nlocal; i += kThreads) {
-          const size_t r = (size_t)b * p.cand_cap + (size_t)i * A + t;
-          p.smp_lg[r] = s_lg[i];
-          p.smp_tok[r] = s_tok[i];
-          p.smp_edge[r] = s_edge[i];
-        }
-        __threadfence();
-      }
-    }
-  }
-  step_tail<kConst, kSmp>(p, w, s, b, mode, wl, wt, we, sh, A);
-}
-
 // ---------------------------------------------------------------- one-CTA sparse step
 //
 // For grammars whose nodes have at most 32 edges each sequence is served by
@@ -1087,17 +1028,16 @@ __device__ __noinline__ int block_sample(const StepParams& p, const float* lg, c
 
 // kXs: the hidden state staged in shared memory instead of registers, so two
 // CTAs fit an SM (for batches larger than the SM count: one wave, not two).
-template <bool kConst, int NCH, bool kXs = false>
-__global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(const StepParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ Step1Shared sh;
-  pdl_enter();
-  const int b = blockIdx.y;
+// One sequence's whole step by one CTA (fan-out of its node at most kPreMax):
+// `s` is its state and `pre0` this warp's entry of its precomputed list, both
+// read by the caller right after the programmatic-dependency wait; the caller
+// does the launch count and the loop control.  Leaves sh.done_after for
+// thread 0.
+template <bool kConst, int NCH, bool kXs>
+__device__ __forceinline__ void step1_body(const StepParams& p, int b, const SeqState& s, const Cand& pre0,
+                                           Step1Shared& sh, unsigned char* smem_raw) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
-  // The state and this warp's first precomputed candidate are read together.
-  const SeqState s = p.st[b];
-  const Cand pre0 = p.pre[(size_t)b * kPreMax + warp];
   const int mode = seq_mode(p, s);
   const int nch = p.H >> 3;
   uint4* xs = reinterpret_cast<uint4*>(smem_raw);
@@ -1205,7 +1145,6 @@ __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(con
       sh.wslot[warp] = ws;
     }
   }
-  if (p.stats && tid == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
   __syncthreads();
 
   // The rest of the step is warp 0's: the fold, the transition, the next list.
@@ -1347,24 +1286,110 @@ __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(con
     }
     sh.done_after = 1;
   }
+}
 
-  if (p.loop_ctrl) {
-    if (gridDim.y == 1) {
-      if (tid == 0) cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, sh.done_after ? 0u : 1u);
+template <bool kConst, int NCH, bool kXs = false>
+__global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(const StepParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ Step1Shared sh;
+  pdl_enter();
+  const int b = blockIdx.y;
+  // The state and this warp's first precomputed candidate are read together.
+  const SeqState s = p.st[b];
+  const Cand pre0 = p.pre[(size_t)b * kPreMax + (threadIdx.x >> 5)];
+  if (p.stats && threadIdx.x == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
+  step1_body<kConst, NCH, kXs>(p, b, s, pre0, sh, smem_raw);
+  loop_control(p, sh.done_after);
+}
+
+// ---------------------------------------------------------------- multi-CTA sparse step
+
+template <bool kConst, int NCH, bool kSmp = false>
+__global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // A narrow node's step uses the one-CTA step's shared state instead.
+  constexpr size_t kShBytes = kSmp || sizeof(Step1Shared) < sizeof(StepShared) ? sizeof(StepShared)
+                                                                                : sizeof(Step1Shared);
+  __shared__ __align__(16) unsigned char sh_raw[kShBytes];
+  StepShared& sh = *reinterpret_cast<StepShared*>(sh_raw);
+  pdl_enter();
+  const int b = blockIdx.y, t = blockIdx.x, T = gridDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
+  const SeqState s = p.st[b];
+  // (The first CTA's warps read their precomputed candidates with the state.)
+  Cand pre0{make_int4(0, -1, 0, 0), make_int4(0, 0, -1, 0)};
+  if (!kSmp && t == 0 && p.pre) pre0 = p.pre[(size_t)b * kPreMax + warp];
+  const int mode = seq_mode(p, s);
+  const int nch = p.H >> 3;
+  const int local_cap = sparse_local_cap(p.cand_cap, T);
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
+  int32_t* s_edge = s_tok + local_cap;
+  float* s_lg = reinterpret_cast<float*>(s_edge + local_cap);  // sampling only
+  // A node needs one CTA per kWarps of its edges: the others leave at once
+  // (deep nodes of a wide catalog have a few edges, its root hundreds).
+  int A = T;
+  bool narrow = false;
+  if (mode == 1) {
+    // A node with a precomputed list, or with at most kPreMax edges, takes the
+    // one-CTA step (greedy steps without forced continuations): the list is
+    // read with the state, the next node's list is computed while the rows
+    // are in flight, and the first CTA alone works.
+    narrow = !kSmp && p.pre && !p.jump && s.pre_n > 0;
+    const int nd = s.node;
+    if (!narrow && nd >= 0 && nd < p.g.n_nodes) {
+      const int fan = w.begin(nd + 1) - w.begin(nd);
+      narrow = !kSmp && p.pre && !p.jump && fan <= kPreMax;
+      const int need = (fan + kWarps - 1) / kWarps;
+      A = need < 1 ? 1 : (need < T ? need : T);
+    }
+  }
+  if constexpr (!kSmp) {
+    if (narrow) {
+      Step1Shared& sh1 = *reinterpret_cast<Step1Shared*>(sh_raw);
+      if (p.stats && tid == 0 && t == 0 && b == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
+      if (t == 0) step1_body<kConst, NCH, false>(p, b, s, pre0, sh1, smem_raw);
+      loop_control(p, sh1.done_after);
+      return;
+    }
+  }
+
+  float wl = -INFINITY;
+  int32_t wt = INT_MAX, we = -1;
+  if (mode == 1 && t < A) {
+    const uint16_t* x = hidden_row(p, s, b);
+    XFrag<NCH> xf;
+    if constexpr (NCH > 0) {
+      xf.load(x, lane);
     } else {
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        const uint32_t g = atomicAdd(&p.ctrl->ticket, 1u);
-        if (g == gridDim.y - 1) {
-          __threadfence();
-          const int32_t live = atomicAdd(&p.ctrl->live, 0);
-          p.ctrl->ticket = 0u;
-          cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond, live > 0 ? 1u : 0u);
+      for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
+    }
+    filter_node<kConst>(p, w, s, b, A, t, s_tok, s_edge, sh);
+    if (!sh.err) {
+      const int nc = sh.ncand;
+      const int nlocal = nc > t ? (nc - t + A - 1) / A : 0;
+      for (int l = warp; l < nlocal; l += kWarps) {
+        const int32_t tok = s_tok[l];
+        const float v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
+        if (better(v, tok, wl, wt)) { wl = v; wt = tok; we = s_edge[l]; }
+        if (kSmp && lane == 0) s_lg[l] = v;
+      }
+      if constexpr (kSmp) {
+        // Every candidate's logit, token and edge go to the sequence's scratch
+        // rows by candidate rank, for its last CTA (kept out of the loop above).
+        __syncthreads();
+        for (int i = tid; i < nlocal; i += kThreads) {
+          const size_t r = (size_t)b * p.cand_cap + (size_t)i * A + t;
+          p.smp_lg[r] = s_lg[i];
+          p.smp_tok[r] = s_tok[i];
+          p.smp_edge[r] = s_edge[i];
         }
+        __threadfence();
       }
     }
   }
+  step_tail<kConst, kSmp>(p, w, s, b, mode, wl, wt, we, sh, A);
 }
 
 // Dense head: every vocabulary row, then the legal mask, then the argmax.
@@ -1865,7 +1890,7 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (head == kHeadSparse && p.pre) {
+  if (head == kHeadSparse && p.one_cta) {
     cfg.gridDim = dim3(1, p.B);
     if constexpr (NCH >= 8) {
       if (p.wide) {
