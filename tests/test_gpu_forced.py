@@ -109,6 +109,23 @@ def test_unstructured_jump_teacher_forced(tcd):
     assert st["forced"] > 0.5 * int(lens.sum())
 
 
+@pytest.mark.parametrize("name", ["char_tools", "char_hex"])
+def test_char_jump_teacher_forced(tcd, name):
+    """Multi-CTA grammars whose narrow nodes take the one-CTA step: forced spans
+    that start at a narrow node and cross into a wide one (a node wider than a
+    precomputed list is counted by the chain itself)."""
+    w = workload(name)
+    B = 16
+    hid = w.hidden_states(0, B)
+    out, st = _run(tcd, name, hid, B, tcd.HEAD_SPARSE | tcd.FLAG_JUMP_FORWARD)
+    plain, _ = _run(tcd, name, hid, B, tcd.HEAD_SPARSE)
+    assert np.all(out[3] == 0)
+    check_against_oracle(name, hid, out, w.k, w.max_steps, exact=False, jump=True)
+    assert np.array_equal(out[0], plain[0]) and np.array_equal(out[2], plain[2])
+    assert st["forced"] == int(sum(np.isnan(out[1][b, :out[2][b]]).sum() for b in range(B)))
+    assert st["forced"] > 0
+
+
 def test_batched_jump_teacher_forced(tcd):
     w = workload("batched")
     hid = w.hidden_states(0, w.batch)

@@ -492,15 +492,16 @@ __device__ __forceinline__ void forced_chain(const StepParams& p, const WalkRd<k
       count = 1;
       only = list[0];
       known = false;
-    } else if (list) {
+    } else if (list && hdr.y - hdr.x <= kPreMax) {
       count = warp_legal_set<kConst>(p, w, ns, b, hdr.x, hdr.y, pid, lane, list);
       __syncwarp();
       if (count == 1) only = list[0];
     } else {
+      // (a node wider than a list: counted, and no list is left for it)
       count = warp_count_legal<kConst>(p, w, ns, b, hdr.x, hdr.y, pid, lane, only);
     }
     if (count != 1) {  // (-1: an index out of range, which the next step reports)
-      if (list) {
+      if (list && hdr.y - hdr.x <= kPreMax) {
         list_n = count;
         list_pid = pid;
       }
@@ -1214,9 +1215,10 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
     }
     // The winner's child legal set becomes the next step's candidate list.
     const int next_n = (status == TC_OK && ptr_done < 0) ? sh.spec_n[bs] : -1;
-    // Forced continuations follow when that set is a single token, or after a
-    // separator (the root's set is not precomputed).
-    const bool chain = p.jump && status == TC_OK && !stop && (next_n == 1 || ptr_done >= 0);
+    // Forced continuations follow when that set is a single token, after a
+    // separator (the root's set is not precomputed), or when no set was kept
+    // (a child wider than a list, counted by the chain itself).
+    const bool chain = p.jump && status == TC_OK && !stop && (next_n == 1 || next_n < 0 || ptr_done >= 0);
     if (!chain && lane < next_n) p.pre[(size_t)b * kPreMax + lane] = sh.spec[bs][lane];
     if (ptr_done >= 0 && !p.iv) decrement_path(p, b, ptr_done, lane, 32);
     SeqState ns = s;
@@ -1333,14 +1335,14 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   bool narrow = false;
   if (mode == 1) {
     // A node with a precomputed list, or with at most kPreMax edges, takes the
-    // one-CTA step (greedy steps without forced continuations): the list is
-    // read with the state, the next node's list is computed while the rows
-    // are in flight, and the first CTA alone works.
-    narrow = !kSmp && p.pre && !p.jump && s.pre_n > 0;
+    // one-CTA step (greedy steps): the list is read with the state, the next
+    // node's list is computed while the rows are in flight, and the first CTA
+    // alone works.
+    narrow = !kSmp && p.pre && s.pre_n > 0;
     const int nd = s.node;
     if (!narrow && nd >= 0 && nd < p.g.n_nodes) {
       const int fan = w.begin(nd + 1) - w.begin(nd);
-      narrow = !kSmp && p.pre && !p.jump && fan <= kPreMax;
+      narrow = !kSmp && p.pre && fan <= kPreMax;
       const int need = (fan + kWarps - 1) / kWarps;
       A = need < 1 ? 1 : (need < T ? need : T);
     }
