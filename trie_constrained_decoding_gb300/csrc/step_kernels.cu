@@ -1310,8 +1310,7 @@ template <bool kConst, int NCH, bool kSmp = false>
 __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // A narrow node's step uses the one-CTA step's shared state instead.
-  constexpr size_t kShBytes = kSmp || sizeof(Step1Shared) < sizeof(StepShared) ? sizeof(StepShared)
-                                                                                : sizeof(Step1Shared);
+  constexpr size_t kShBytes = sizeof(Step1Shared) < sizeof(StepShared) ? sizeof(StepShared) : sizeof(Step1Shared);
   __shared__ __align__(16) unsigned char sh_raw[kShBytes];
   StepShared& sh = *reinterpret_cast<StepShared*>(sh_raw);
   pdl_enter();
@@ -1321,7 +1320,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   const SeqState s = p.st[b];
   // (The first CTA's warps read their precomputed candidates with the state.)
   Cand pre0{make_int4(0, -1, 0, 0), make_int4(0, 0, -1, 0)};
-  if (!kSmp && t == 0 && p.pre) pre0 = p.pre[(size_t)b * kPreMax + warp];
+  if (t == 0 && p.pre) pre0 = p.pre[(size_t)b * kPreMax + warp];
   const int mode = seq_mode(p, s);
   const int nch = p.H >> 3;
   const int local_cap = sparse_local_cap(p.cand_cap, T);
@@ -1335,26 +1334,24 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   bool narrow = false;
   if (mode == 1) {
     // A node with a precomputed list, or with at most kPreMax edges, takes the
-    // one-CTA step (greedy steps): the list is read with the state, the next
-    // node's list is computed while the rows are in flight, and the first CTA
-    // alone works.
-    narrow = !kSmp && p.pre && s.pre_n > 0;
+    // one-CTA step: the list is read with the state, the next node's list is
+    // computed while the rows are in flight, and the first CTA alone works
+    // (drawing with the one-warp sampler when sampling).
+    narrow = p.pre && s.pre_n > 0;
     const int nd = s.node;
     if (!narrow && nd >= 0 && nd < p.g.n_nodes) {
       const int fan = w.begin(nd + 1) - w.begin(nd);
-      narrow = !kSmp && p.pre && fan <= kPreMax;
+      narrow = p.pre && fan <= kPreMax;
       const int need = (fan + kWarps - 1) / kWarps;
       A = need < 1 ? 1 : (need < T ? need : T);
     }
   }
-  if constexpr (!kSmp) {
-    if (narrow) {
-      Step1Shared& sh1 = *reinterpret_cast<Step1Shared*>(sh_raw);
-      if (p.stats && tid == 0 && t == 0 && b == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
-      if (t == 0) step1_body<kConst, NCH, false>(p, b, s, pre0, sh1, smem_raw);
-      loop_control(p, sh1.done_after);
-      return;
-    }
+  if (narrow) {
+    Step1Shared& sh1 = *reinterpret_cast<Step1Shared*>(sh_raw);
+    if (p.stats && tid == 0 && t == 0 && b == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
+    if (t == 0) step1_body<kConst, NCH, false>(p, b, s, pre0, sh1, smem_raw);
+    loop_control(p, sh1.done_after);
+    return;
   }
 
   float wl = -INFINITY;
