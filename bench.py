@@ -135,24 +135,28 @@ def sparse_kernel_name(max_fanout: int) -> str:
     return "sparse_step1_kernel" if max_fanout <= 32 else "sparse_step_kernel"
 
 
-def source_code_sha256(path: str) -> str:
-    """sha256 of a source file's code: `//` comments, surrounding blanks and
-    empty lines removed, so that comment edits keep a capture valid."""
+def source_code_sha256(*paths: str) -> str:
+    """sha256 of source files' code, in order: `//` comments, surrounding
+    blanks and empty lines removed, so that comment edits keep a capture valid."""
     import hashlib
     lines = []
-    for line in open(path, encoding="utf-8").read().splitlines():
-        code = line.split("//", 1)[0].strip()
-        if code:
-            lines.append(code)
+    for path in paths:
+        for line in open(path, encoding="utf-8").read().splitlines():
+            code = line.split("//", 1)[0].strip()
+            if code:
+                lines.append(code)
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
 def recorded_traffic(source: str, profile: str):
     """DRAM bytes per launch recorded by the last ncu capture of a kernel, or
-    None when the kernel's source code has changed since that capture."""
+    None when the kernel's source code has changed since that capture.
+    `source` names the kernel's files, `+`-separated (the kernel file and the
+    header of its shared types)."""
     try:
         text = open(os.path.join(ROOT, "profiles", profile)).read()
-        want = source_code_sha256(os.path.join(ROOT, "trie_constrained_decoding_gb300", "csrc", source))
+        want = source_code_sha256(*[os.path.join(ROOT, "trie_constrained_decoding_gb300", "csrc", f)
+                                    for f in source.split("+")])
     except OSError:
         return None
     sha = traffic = None
@@ -473,7 +477,7 @@ def run_ours(args):
             else "fallback 6.8 TB/s"
         if head == tcd.HEAD_SPARSE and args.workload == "large_head":
             prof = f"{sparse_kernel_name(tinfo['max_fanout'])}_large_head.md"
-            roof["traffic"] = recorded_traffic("step_kernels.cu", prof)
+            roof["traffic"] = recorded_traffic("step_kernels.cu+kernels.h", prof)
             roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, cold caches, "
                                       f"profiles/{prof}" if roof["traffic"] is not None
                                       else "kernel source changed since the last ncu capture")

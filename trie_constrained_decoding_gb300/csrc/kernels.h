@@ -29,7 +29,7 @@ constexpr int kBanMax = 8;
 constexpr int kBanMaxStrings = 65535;
 
 // Per-sequence decode state (device memory, one 48-byte record per sequence).
-struct SeqState {
+struct alignas(16) SeqState {
   int32_t node;     // current trie node
   int32_t emitted;  // pointers completed so far (j)
   int32_t len;      // tokens emitted so far
@@ -42,6 +42,8 @@ struct SeqState {
   // (scalar fields: an array member would keep the state out of registers).
   uint32_t ban0, ban1, ban2, ban3;
 };
+// 16-byte aligned: a step reads its state as three 16-byte loads.
+static_assert(sizeof(SeqState) == 48, "sequence state: three 16-byte loads");
 
 // A legal candidate as kept in candidate lists: {token, edge, child, live
 // pointers below} and the child's header {edge begin, edge end, pointer rank, 0}.
