@@ -6,25 +6,30 @@
 //
 //   D[b, n] = sum_h X[b, h] * E[rows[n], h]        b < B (sequences), n < n_cols
 //
-// Warp-specialised persistent kernel, 192 threads per CTA:
+// Warp-specialised persistent kernel, 320 threads per CTA:
 //  - warp 0 (producer) fills a ring of shared-memory stages with TMA: the
-//    activation tile (128 sequences x 64 K-elements per M tile) with a tiled
-//    2-D load, the embedding tile (128 columns x 64) either with one tiled load
-//    (dense head: contiguous rows) or with one four-row gather per lane (union
-//    head: listed rows), all 128-byte swizzled, completion counted on the
-//    stage's "full" mbarrier;
+//    activation tiles (128 sequences x 64 K-elements per M tile) with tiled
+//    2-D loads and, for the dense head, the embedding tile (128 contiguous
+//    rows x 64) with one more; all 128-byte swizzled, completion counted on
+//    the stage's "full" mbarrier;
 //  - warp 1, one thread, issues tcgen05.mma kind::f16 (bf16 in, fp32 in TMEM,
 //    M = 128 per tile, N = 128, K = 16 per instruction) and commits each stage
 //    back to its "empty" barrier and each finished task to an accumulator-full
 //    barrier; TMEM holds two accumulators so one task's epilogue overlaps the
 //    next task's MMAs;
-//  - warps 2-5 (epilogue) read the accumulator with tcgen05.ld: the thread on
-//    TMEM lane t of M tile m owns sequence 128 m + t and keeps, over the
-//    columns of its own legal candidates only, the largest logit (lowest
-//    column on ties; columns ascend with token ids), or, when K is split, its
-//    candidates' partial sums.
-// A task is one 128-column tile and one K split.  Every wait is bounded; on a
-// timeout the kernel records an error, stops issuing and frees its TMEM.
+//  - warps 2-9 (epilogue) first issue the union head's row gathers (one
+//    four-row gather per lane, four groups per warp per stage: one warp's
+//    lanes would issue all 32 one after another), then read the accumulator
+//    with tcgen05.ld: the thread on TMEM lane t of M tile m owns sequence
+//    128 m + t and keeps, over the columns of its own legal candidates only
+//    (a 32-byte record per sequence and tile), the largest logit (lowest column
+//    on ties; columns ascend with token ids), or, when K is split, writes its
+//    candidates' partial sums through a per-warp 32 x 32 transpose so that one
+//    store covers consecutive candidates of one sequence.
+// A task is one 128-column tile, one K split and, for the union head above
+// 128 sequences, one M tile (the dense head keeps both M tiles in one CTA so
+// every embedding tile is read once).  Every wait is bounded; on a timeout the
+// kernel records an error, stops issuing and frees its TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>

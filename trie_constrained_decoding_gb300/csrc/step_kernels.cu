@@ -12,8 +12,10 @@
 // candidates come from a list the previous step computed, each warp gathers a
 // candidate's embedding row and meanwhile computes that candidate's child
 // legal set, and the winner's set becomes the next step's list.  Otherwise
-// sparse_step_kernel gives each sequence up to `tiles` CTAs (one wave): every
-// CTA the node needs filters the node's edges itself (a few hundred bytes of
+// sparse_step_kernel gives each sequence up to `tiles` CTAs (one wave); a
+// sequence at a narrow node (a precomputed list, or at most 32 edges) is
+// served by its first CTA with the same one-CTA body, and at a wide node
+// every CTA the node needs filters the node's edges itself (a few hundred bytes of
 // cached reads), so no second launch publishes the candidate list; candidate
 // rank r belongs to CTA r % active; each CTA leaves its best (logit, token) in
 // a fixed slot and the last to arrive (atomic ticket after a fence, no
