@@ -5,7 +5,6 @@ over tokens": an edge range per node, a token and a child per edge, sentinel
 children for the separator and stop edges, each pointer's path of edges;
 section "Masked sampling inside the sampler": per-edge live-pointer counts;
 section "The sparse output layer": the fan-out cap."""
-from collections import deque
 
 import numpy as np
 import pytest
@@ -28,12 +27,13 @@ def _compare(tcd, cat, sep, stop, V, cap=256):
     assert info["total_tokens"] == sum(len(s) for s in cat)
     nb, tok, child, nptr, cnt = a["node_begin"], a["edge_tok"], a["edge_child"], a["node_ptr"], a["static_cnt"]
     assert nb[0] == 0 and nb[-1] == info["n_edges"] and np.all(np.diff(nb) >= 0)
-    # walk the CSR breadth-first; node ids must come out in BFS order, children by ascending token
+    # walk the CSR depth-first; node ids must come out in preorder, children by ascending token
     prefix_of = {0: ()}
-    order = [0]
-    q = deque([0])
+    order = []
+    q = [0]
     while q:
-        n = q.popleft()
+        n = q.pop()
+        order.append(n)
         u = prefix_of[n]
         es = range(nb[n], nb[n + 1])
         toks = [int(tok[e]) for e in es]
@@ -50,8 +50,7 @@ def _compare(tcd, cat, sep, stop, V, cap=256):
             assert c not in prefix_of
             prefix_of[c] = u + (t,)
             assert cnt[e] == len(ref.below[u + (t,)])
-            order.append(c)
-            q.append(c)
+        q.extend(c for _, c, _ in reversed(kids))
         for e in es:
             if child[e] < 0:
                 assert cnt[e] == 0

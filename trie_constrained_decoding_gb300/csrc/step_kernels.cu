@@ -487,6 +487,39 @@ __device__ __forceinline__ void forced_chain(const StepParams& p, const WalkRd<k
   list_pid = -2;
   unsigned long long forced = 0;
   while (!ns.done && ns.len < p.max_steps && ns.len < p.out_stride) {
+    if (!known && !p.forced_logits && hdr.y - hdr.x == 1) {
+      // A run of nodes with one edge each.  Nodes are numbered depth-first, so
+      // such a run's edge records are consecutive: lane j reads the record that
+      // is the run's j-th edge if the run gets that far, and the run is the
+      // leading lanes whose edge is a live token edge and whose predecessor's
+      // child has exactly that one edge.  One round trip for up to 32 tokens.
+      const int e = hdr.x + lane;
+      const int room = min(p.max_steps, p.out_stride) - ns.len;
+      const SeqLive L = seq_live(p, ns, b);
+      bool live = false, link = false;
+      int4 ed = make_int4(-1, -1, 0, 0), hd = make_int4(0, 0, -1, 0);
+      if (lane < room && e < p.g.n_edges) {
+        ed = w.edge(e);
+        hd = w.child_hdr(e);
+        const int32_t c = L.cnt ? L.cnt[e] : 0;
+        live = ed.x >= 0 && ed.x < p.V && ed.y >= 0 && ed.y < p.g.n_nodes && edge_live(L, e, ed, c) > 0;
+        link = hd.x == e + 1 && hd.y == e + 2;
+      }
+      const unsigned run = __ballot_sync(kFull, live) & ((__ballot_sync(kFull, link) << 1) | 1u);
+      const int m = run == kFull ? 32 : __ffs(~run) - 1;
+      if (m > 0) {
+        if (lane < m) {
+          p.tok_out[(size_t)b * p.out_stride + ns.len + lane] = ed.x;
+          p.logit_out[(size_t)b * p.out_stride + ns.len + lane] = __int_as_float(0x7fc00000);
+        }
+        ns.len += m;
+        forced += (unsigned long long)m;
+        ns.node = __shfl_sync(kFull, ed.y, m - 1);
+        hdr = make_int4(__shfl_sync(kFull, hd.x, m - 1), __shfl_sync(kFull, hd.y, m - 1),
+                        __shfl_sync(kFull, hd.z, m - 1), 0);
+        continue;
+      }
+    }
     int count;
     const int pid = hdr.z;
     Cand only{make_int4(0, -1, 0, 0), make_int4(0, 0, -1, 0)};

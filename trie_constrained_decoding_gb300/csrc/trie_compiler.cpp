@@ -9,7 +9,6 @@
 // layer" (the build refuses a node with more edges than the cap).
 #include <algorithm>
 #include <cstring>
-#include <deque>
 #include <unordered_map>
 
 #include "tcd_internal.h"
@@ -151,23 +150,22 @@ extern "C" tc_status tc_compile_trie(const int32_t* ids, const int64_t* offsets,
   }
   const int32_t N = (int32_t)term_ptr.size();
 
-  // 2. Breadth-first numbering, children visited in ascending token order.
+  // 2. Depth-first (preorder) numbering, children visited in ascending token
+  //    order: a node's first child directly follows it, so a chain of nodes
+  //    with one edge each gets consecutive ids and, in the CSR below,
+  //    consecutive edge records (a forced span can be read in one go).
   for (auto& k : kids)
     std::sort(k.begin(), k.end(), [&](int32_t a, int32_t b) { return node_tok[a] < node_tok[b]; });
-  std::vector<int32_t> bfs_order;
-  bfs_order.reserve(N);
+  std::vector<int32_t> order;
+  order.reserve(N);
   std::vector<int32_t> new_id(N, -1);
-  std::deque<int32_t> q{0};
-  new_id[0] = 0;
-  bfs_order.push_back(0);
-  while (!q.empty()) {
-    const int32_t n = q.front();
-    q.pop_front();
-    for (int32_t c : kids[n]) {
-      new_id[c] = (int32_t)bfs_order.size();
-      bfs_order.push_back(c);
-      q.push_back(c);
-    }
+  std::vector<int32_t> stack{0};
+  while (!stack.empty()) {
+    const int32_t n = stack.back();
+    stack.pop_back();
+    new_id[n] = (int32_t)order.size();
+    order.push_back(n);
+    for (auto it = kids[n].rbegin(); it != kids[n].rend(); ++it) stack.push_back(*it);
   }
 
   // 3. Emit the CSR: per node its child edges plus the two control edges of a
@@ -187,7 +185,7 @@ extern "C" tc_status tc_compile_trie(const int32_t* ids, const int64_t* offsets,
   edges.reserve((size_t)N + 2 * (size_t)n_strings);
   int32_t max_fan = 0;
   for (int32_t ni = 0; ni < N; ++ni) {
-    const int32_t old = bfs_order[ni];
+    const int32_t old = order[ni];
     t->node_begin[ni] = (int32_t)edges.size();
     std::vector<Edge> mine;
     mine.reserve(kids[old].size() + 2);
@@ -219,8 +217,8 @@ extern "C" tc_status tc_compile_trie(const int32_t* ids, const int64_t* offsets,
     t->edge_child[e] = edges[e].child;
   }
 
-  // 4. Live-pointer counts: children have larger BFS ids, so one reverse pass
-  //    accumulates subtree sizes.
+  // 4. Live-pointer counts: children have larger preorder ids, so one reverse
+  //    pass accumulates subtree sizes.
   for (int32_t ni = N - 1; ni >= 0; --ni) {
     int32_t s = t->node_ptr[ni] >= 0 ? 1 : 0;
     for (int32_t e = t->node_begin[ni]; e < t->node_begin[ni + 1]; ++e)
