@@ -184,3 +184,26 @@ def test_depth_first_ranks_give_each_subtree_one_range(tcd):
                 else:
                     assert lo == rk["ptr_rank"][ex["node_ptr"][n]]
         t.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "large_head", "batched", "unstructured"])
+def test_single_edge_chains_have_consecutive_records(tcd, name):
+    """Depth-first node numbers lay a chain of single-edge nodes out as
+    consecutive edge records, which lets a forced continuation read a whole
+    run at once: whenever a node's only edge leads to a child with a single
+    edge, that edge is the next record.  (The device walk checks every link
+    itself, so this pins the layout, not correctness.)"""
+    w = I.WORKLOADS[name]()
+    t = tcd.Trie.compile(w.catalog, w.sep_id, w.stop_id, w.vocab, w.max_fanout)
+    ex = t.export()
+    nb, child = ex["node_begin"], ex["edge_child"]
+    links = 0
+    for n in range(len(nb) - 1):
+        if nb[n + 1] - nb[n] != 1 or child[nb[n]] < 0:
+            continue
+        c = int(child[nb[n]])
+        if nb[c + 1] - nb[c] == 1:
+            assert nb[c] == nb[n] + 1
+            links += 1
+    t.close()
+    assert links > 0
