@@ -278,3 +278,38 @@ def test_wide_batch_equals_two_narrow_batches(tcd):
             assert np.array_equal(out[i], wide[i][h * (B // 2):(h + 1) * (B // 2)])
     ctx.close()
     assert np.all(wide[3] == 0)
+
+
+def test_host_steps_with_mixed_heads_equal_sparse_steps(tcd):
+    """tc_step with a different head on every other step: the other heads move
+    a sequence without refreshing the sparse step's precomputed candidate
+    list, which the next sparse step must not use.  On integer inputs every
+    head gives the same tokens and logits, so the mixed sequence of steps
+    equals the all-sparse one bit for bit."""
+    torch = torch_mod()
+    w = workload("tiny")
+    B = 16
+    hid_bits = w.hidden_states(0, B)  # [S, B, H]
+    S = hid_bits.shape[0]
+    hid = to_dev_bf16(hid_bits)
+    ctx, _ = make_ctx(tcd, "tiny", max_batch=B)
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    lg = torch.empty(B, dtype=torch.float32, device="cuda")
+    st = torch.empty(B, dtype=torch.int32, device="cuda")
+    others = [tcd.HEAD_DENSE, tcd.HEAD_UNION_GEMM, tcd.HEAD_DENSE_GEMM]
+
+    def run(mixed):
+        ctx.reset(B, w.k)
+        out = []
+        for t in range(S):
+            head = others[(t // 2) % 3] if (mixed and t % 2 == 1) else tcd.HEAD_SPARSE
+            ctx.step(hid[t], tok, lg, st, head=head)
+            torch.cuda.synchronize()
+            out.append((tok.cpu().numpy().copy(), lg.cpu().numpy().copy(), st.cpu().numpy().copy()))
+        return out
+
+    plain, mixed = run(False), run(True)
+    ctx.close()
+    for (a_t, a_l, a_s), (b_t, b_l, b_s) in zip(plain, mixed):
+        assert np.array_equal(a_t, b_t) and np.array_equal(a_l, b_l) and np.array_equal(a_s, b_s)
+    assert np.all(plain[-1][2] == 0)
