@@ -300,6 +300,11 @@ tc_status tc_reset(tc_ctx* ctx, int32_t batch, int32_t k, void* stream);
  *  logit_out   (device) float[batch]: its fp32 logit (0 for -1 tokens); may be NULL.
  *  status_out  (device) int32[batch]: TC_OK or the sequence's error; may be NULL.
  *
+ * The head may change from one call to the next: the first sparse step after
+ * a step with another head drops the candidate lists the sparse step keeps
+ * for the next node (a strided memset on `stream` before the step), since the
+ * other heads do not keep them.
+ *
  * Asynchronous on `stream`; a sequence that meets an error stops there.
  */
 tc_status tc_step(tc_ctx* ctx, const void* hidden_bf16, int32_t head, int32_t* tok_out,
