@@ -313,3 +313,57 @@ def test_host_steps_with_mixed_heads_equal_sparse_steps(tcd):
     for (a_t, a_l, a_s), (b_t, b_l, b_s) in zip(plain, mixed):
         assert np.array_equal(a_t, b_t) and np.array_equal(a_l, b_l) and np.array_equal(a_s, b_s)
     assert np.all(plain[-1][2] == 0)
+
+
+def test_tiny_dense_gemm_two_m_tiles_bitexact(tcd):
+    """The full-vocabulary tcgen05 GEMM above 128 sequences keeps both
+    128-sequence M tiles in one CTA (every embedding tile read once, a
+    three-stage ring, two 256-column TMEM accumulators).  On integer-valued
+    inputs every fp32 sum is exact, so at B=256 (two full tiles) and B=200 (a
+    ragged second tile of 72) tokens and logits equal the sparse head's bit for
+    bit, and the oracle's ("Understanding Inference for Systems Engineers",
+    section 7.5: every logit, then the mask, then the argmax)."""
+    w = workload("tiny")
+    for B in (256, 200):
+        (_, sp), = _run_head(tcd, "tiny", tcd.HEAD_SPARSE, batch=B)
+        (hid, dg), = _run_head(tcd, "tiny", tcd.HEAD_DENSE_GEMM, batch=B)
+        assert np.all(dg[3] == 0)
+        for x, y in zip(sp, dg):
+            assert np.array_equal(x, y), B
+        check_against_oracle("tiny", hid, dg, w.k, w.max_steps, exact=True)
+
+
+def test_tensor_batch_dense_gemm_b256(tcd):
+    """The dense comparator of the union head at its own shape: B=256, k=3,
+    hidden 4096, every vocabulary row by the two-M-tile tcgen05 GEMM, then each
+    sequence's mask and argmax; every sequence teacher-forced against the
+    oracle (Gaussian inputs: chosen logits within 1e-3 relative, a differing
+    token only below the oracle's 1e-5 top-2 margin)."""
+    w = workload("tensor_batch")
+    (hid, out), = _run_head(tcd, "tensor_batch", tcd.HEAD_DENSE_GEMM)
+    assert np.all(out[3] == 0)
+    reps = check_against_oracle("tensor_batch", hid, out, w.k, w.max_steps, exact=False)
+    assert sum(r.flips for r in reps) <= 5
+
+
+def test_dense_gemm_ragged_two_m_tiles_equal_narrow_batches(tcd):
+    """A sequence's dense-GEMM result does not depend on which M tile, or
+    which kernel configuration, computes it: B=200 in the two-M-tile kernel
+    equals the batches of its first 128 and last 72 sequences (one M tile
+    each) bit for bit, and stays within the oracle's tolerance."""
+    w = workload("batched")
+    B = 200
+    hid = w.hidden_states(0, B)
+    ctx, _ = make_ctx(tcd, "batched", max_batch=B)
+    buf = DecodeBuffers(w.max_steps, B, w.hidden, w.max_steps)
+    buf.load(hid)
+    wide = buf.run(ctx, w.k, head=tcd.HEAD_DENSE_GEMM)
+    assert np.all(wide[3] == 0)
+    for lo, hi in ((0, 128), (128, 200)):
+        part = DecodeBuffers(w.max_steps, hi - lo, w.hidden, w.max_steps)
+        part.load(hid[:, lo:hi])
+        out = part.run(ctx, w.k, head=tcd.HEAD_DENSE_GEMM)
+        for i in range(4):
+            assert np.array_equal(out[i], wide[i][lo:hi]), (lo, i)
+    ctx.close()
+    check_against_oracle("batched", hid, wide, w.k, w.max_steps, exact=False)
