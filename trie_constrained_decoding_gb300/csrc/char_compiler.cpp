@@ -12,7 +12,10 @@
 //
 // The result has the token compiler's layout: per node its outgoing token
 // edges sorted by token id, plus the separator and stop edges at a terminal;
-// nodes are numbered breadth-first over the character trie.  Live-pointer
+// nodes are numbered depth-first (preorder, children by ascending byte) over
+// the character trie, so a run of nodes with one character child each gets
+// consecutive ids and consecutive edge records, as in the token compiler
+// (a forced run of one-character tokens is read in one round trip).  Live-pointer
 // counts are subtree sizes in the character trie, and pointer ranks are
 // depth-first over it, so every edge's pointers are one rank range.
 #include <algorithm>
@@ -127,21 +130,18 @@ extern "C" tc_status tc_compile_char_trie(const uint8_t* chars, const int64_t* o
   }
   const int32_t N = (int32_t)term.size();
   for (auto& k : kids) std::sort(k.begin(), k.end());
-  // Breadth-first numbering, children by ascending byte.
-  std::vector<int32_t> bfs, new_id((size_t)N, -1);
-  bfs.reserve(N);
+  // Depth-first (preorder) numbering, children by ascending byte: order[i]
+  // is the trie node numbered i.
+  std::vector<int32_t> order, new_id((size_t)N, -1);
+  order.reserve(N);
   {
-    std::deque<int32_t> q{0};
-    new_id[0] = 0;
-    bfs.push_back(0);
-    while (!q.empty()) {
-      const int32_t n = q.front();
-      q.pop_front();
-      for (auto& ch : kids[n]) {
-        new_id[ch.second] = (int32_t)bfs.size();
-        bfs.push_back(ch.second);
-        q.push_back(ch.second);
-      }
+    std::vector<int32_t> stack{0};
+    while (!stack.empty()) {
+      const int32_t n = stack.back();
+      stack.pop_back();
+      new_id[(size_t)n] = (int32_t)order.size();
+      order.push_back(n);
+      for (auto it = kids[(size_t)n].rbegin(); it != kids[(size_t)n].rend(); ++it) stack.push_back(it->second);
     }
   }
 
@@ -215,7 +215,7 @@ extern "C" tc_status tc_compile_char_trie(const uint8_t* chars, const int64_t* o
     }
   }
 
-  // 4. CSR in breadth-first node order with control edges at terminals.
+  // 4. CSR in depth-first node order with control edges at terminals.
   auto* t = new tc_trie();
   t->vocab = vocab;
   t->sep = sep_id;
@@ -229,7 +229,7 @@ extern "C" tc_status tc_compile_char_trie(const uint8_t* chars, const int64_t* o
   int32_t max_fan = 0;
   std::vector<Edge> all;
   for (int32_t ni = 0; ni < N; ++ni) {
-    const int32_t old = bfs[(size_t)ni];
+    const int32_t old = order[(size_t)ni];
     t->node_begin[(size_t)ni] = (int32_t)all.size();
     std::vector<Edge> mine;
     for (const Edge& e : edges_of[(size_t)old]) mine.push_back({e.tok, new_id[(size_t)e.child]});
@@ -261,10 +261,10 @@ extern "C" tc_status tc_compile_char_trie(const uint8_t* chars, const int64_t* o
   }
 
   // 5. Subtree sizes and depth-first ranks over the character trie (its own
-  //    child links, not the token edges), in breadth-first node ids.
+  //    child links, not the token edges), in the new node ids.
   std::vector<std::vector<int32_t>> tree((size_t)N);
   for (int32_t ni = 0; ni < N; ++ni)
-    for (auto& ch : kids[(size_t)bfs[(size_t)ni]]) tree[(size_t)ni].push_back(new_id[(size_t)ch.second]);
+    for (auto& ch : kids[(size_t)order[(size_t)ni]]) tree[(size_t)ni].push_back(new_id[(size_t)ch.second]);
   std::vector<int32_t> lo((size_t)N, 0), cnt((size_t)N, 0);
   t->ptr_rank.assign((size_t)n_strings, -1);
   {
