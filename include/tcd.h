@@ -56,6 +56,9 @@ typedef enum tc_status {
   TC_ERR_NO_LIVE_EDGE = 17,      /* device: the chosen token sits on no live edge (defensive) */
   TC_ERR_MAX_STEPS = 18,         /* device: the step budget ran out before the stop token */
   TC_ERR_BOUNDS = 19,            /* device: an index of the grammar image or a logit is invalid */
+  TC_ERR_DEVICE_TIMEOUT = 20,    /* device: a bounded wait inside a kernel gave up (the kernel returned
+                                    without finishing its work; the step fails for every sequence it
+                                    served; cleared by tc_reset / the next decode's reset) */
   TC_ERR_CUDA = 32,              /* a CUDA runtime call failed (see tc_last_error_message) */
   TC_ERR_OOM = 33                /* device allocation failed */
 } tc_status;
@@ -127,7 +130,8 @@ typedef struct tc_ctx tc_ctx;     /* device context: model, bound grammar, per-s
 typedef struct tc_graph tc_graph; /* a captured device-resident decode loop */
 
 typedef struct tc_trie_info_t {
-  int32_t n_nodes;          /* N, root is node 0, nodes numbered in breadth-first order */
+  int32_t n_nodes;          /* N, root is node 0, nodes numbered depth-first (preorder, children in
+                               ascending token or byte order) */
   int32_t n_edges;          /* E, token edges plus two control edges per terminal node */
   int32_t n_strings;        /* K, catalog size (pointer ids 0..K-1 in input order) */
   int32_t max_fanout;       /* largest edge count of any node (control edges included) */
@@ -201,7 +205,7 @@ tc_status tc_trie_export(const tc_trie* trie, int32_t* node_begin, int32_t* edge
  *  max_fanout           cap on any node's edges (token edges + 2 control edges)
  *
  * The result is a tc_trie like tc_compile_trie's: nodes are character-trie
- * nodes numbered breadth-first, a node's edges are the tokens that walk from
+ * nodes numbered depth-first (preorder, children by ascending byte), a node's edges are the tokens that walk from
  * it (a token edge may skip several characters, and several edges may lead to
  * one node) plus the separator and stop edges at a terminal, sorted by token
  * id; static_cnt counts the strings below an edge's target.  It keeps no
@@ -300,10 +304,10 @@ tc_status tc_reset(tc_ctx* ctx, int32_t batch, int32_t k, void* stream);
  *  logit_out   (device) float[batch]: its fp32 logit (0 for -1 tokens); may be NULL.
  *  status_out  (device) int32[batch]: TC_OK or the sequence's error; may be NULL.
  *
- * The head may change from one call to the next: the first sparse step after
- * a step with another head drops the candidate lists the sparse step keeps
- * for the next node (a strided memset on `stream` before the step), since the
- * other heads do not keep them.
+ * The head may change from one call to the next, also inside a captured
+ * graph: the sparse step keeps each sequence's next candidate list in its
+ * device state, and every other head's step clears it there, so the next
+ * sparse step filters that node itself.
  *
  * Asynchronous on `stream`; a sequence that meets an error stops there.
  */
@@ -424,6 +428,29 @@ tc_status tc_read_seq_state(tc_ctx* ctx, void* stream, int32_t* node, int32_t* e
  */
 #define TC_STAT_SLOTS 5
 tc_status tc_read_stats(tc_ctx* ctx, void* stream, int64_t* out, int32_t reset);
+
+/*
+ * tc_gemm_wait_test - exercise the GEMM heads' error path without any fault
+ * ("Constraint made cheaper than no constraint", section "Masked sampling
+ * inside the sampler": a step that cannot finish fails loudly).  Every wait
+ * of the tcgen05 GEMM kernel on a shared-memory barrier is bounded by a poll
+ * count; when one runs out, the kernel stops issuing, waits (again bounded)
+ * for the copies and MMAs it started, frees its tensor memory, sets the
+ * context's timeout flag and returns; the step then fails every sequence it
+ * served with TC_ERR_DEVICE_TIMEOUT, and the next tc_reset (or decode) clears
+ * the flag.
+ *
+ *  withhold    nonzero: in later GEMM-head steps, the kernel's first CTA
+ *              issues no copy for its first pipeline stage, so the waits on
+ *              that stage run out.  0: normal operation.
+ *  wait_polls  polls of one wait before it gives up; 0 restores the default
+ *              (2^22).  A small count (e.g. 2000) makes the timeout quick.
+ *
+ * Test use only; it allocates the GEMM heads' scratch if needed, synchronises
+ * the device and drops the context's cached decode graphs (they hold the old
+ * settings).  Errors: TC_ERR_INVALID_ARG, TC_ERR_OOM, TC_ERR_CUDA.
+ */
+tc_status tc_gemm_wait_test(tc_ctx* ctx, int32_t withhold, int64_t wait_polls);
 
 /*
  * tc_dense_argmax_noalloc - the dense head's masked argmax without any device

@@ -33,6 +33,7 @@ FLAG_JUMP_FORWARD = 0x100      # or-ed into `head` of decode / decode_graph: for
 FLAG_FORCED_LOGITS = 0x200     # with FLAG_JUMP_FORWARD: forced tokens still get their logits
 STAT_SLOTS = 5
 TC_ERR_EMPTY_MASK, TC_ERR_NO_LIVE_EDGE, TC_ERR_MAX_STEPS, TC_ERR_BOUNDS = 16, 17, 18, 19
+TC_ERR_DEVICE_TIMEOUT = 20
 CONST_CAPACITY_BYTES = 63 * 1024
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -93,6 +94,7 @@ _step_sample = _decl("tc_step_sample", ctypes.c_int, [_vp, _vp, ctypes.c_int32, 
                                                       _vp, _vp, _vp])
 _loop_floor = _decl("tc_loop_floor", ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
                                                     ctypes.POINTER(ctypes.c_float), _i64p])
+_gemm_wait_test = _decl("tc_gemm_wait_test", ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int64])
 _status_str = _decl("tc_status_str", ctypes.c_char_p, [ctypes.c_int])
 _last_msg = _decl("tc_last_error_message", ctypes.c_char_p, [])
 
@@ -303,6 +305,11 @@ class Context:
         _check(_read_stats(self._h, _stream_ptr(stream), out.ctypes.data_as(_i64p), int(reset)), "tc_read_stats")
         return {"step_launches": int(out[0]), "seq_steps": int(out[1]), "cand_rows": int(out[2]),
                 "reset_launches": int(out[3]), "forced": int(out[4])}
+
+    def gemm_wait_test(self, withhold: bool, wait_polls: int = 0):
+        """tc_gemm_wait_test: make the GEMM heads' first pipeline stage never
+        arrive (withhold) with waits of `wait_polls` polls; (False, 0) restores."""
+        _check(_gemm_wait_test(self._h, int(bool(withhold)), int(wait_polls)), "tc_gemm_wait_test")
 
     def close(self):
         for g in self._graphs:

@@ -46,7 +46,7 @@ constexpr int kTileK = 64;  // bf16 elements = one 128-byte swizzle row
 constexpr uint32_t kRowBytes = 128;
 constexpr uint32_t kATileBytes = 128 * kRowBytes;     // 16 KiB per 128-row M tile
 constexpr uint32_t kBTileBytes = kTileN * kRowBytes;  // 16 KiB
-constexpr long long kWaitLimit = 1ll << 22;           // try_wait polls before giving up
+constexpr long long kWaitLimit = 1ll << 22;           // default try_wait polls of one wait before giving up
 
 constexpr int kTbStride = 33;  // floats per row of an epilogue warp's 32 x 32 transpose buffer
 // Per epilogue warp: the transpose buffer, then each lane's (candidate bits, first index) pair.
@@ -72,6 +72,7 @@ struct GemmHdr {
   uint64_t empty[6];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t drain;  // after an abort: completion of every MMA the issuer started
   uint32_t tmem_base;
   int32_t abort;
   int32_t row0;
@@ -91,8 +92,8 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kWaitLimit; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
+  for (long long i = 0; i < limit; ++i) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       mbar_init(smem_u32(&hdr->tfull[a]), 1);
       mbar_init(smem_u32(&hdr->tempty[a]), 32 * C::kEpiWarps);
     }
+    mbar_init(smem_u32(&hdr->drain), 1);
     hdr->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -234,6 +236,11 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   // from here on.  The next kernel may start launching now.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const long long wl = p.wait_limit;  // polls of one wait before it gives up
+  // Test switch: CTA 0 issues nothing for its first stage (issue 0), so every
+  // wait on that stage runs out and the error path below is taken.
+  const bool held = p.withhold != 0 && blockIdx.x == 0;
+  long long prod_it = 0;             // stages the producer armed (read at exit after an abort)
   const int KS = p.ksplit;           // K splits per column tile (divides H / 64)
   const int KT = p.H / kTileK / KS;  // k-steps per task
   // Tasks: (column tile, K split, M tile); the M tiles of one (tile, split)
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const int stage = (int)(it % S);
         const uint32_t ph = (uint32_t)((it / S) & 1);
-        if (!mbar_wait(smem_u32(&hdr->empty[stage]), ph ^ 1u)) {
+        if (!mbar_wait(smem_u32(&hdr->empty[stage]), ph ^ 1u, wl)) {
           hdr->abort = 1;
           stop = true;
           break;
@@ -288,7 +295,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         const uint32_t b_base = a_base + MT * kATileBytes;
         const uint32_t fb = smem_u32(&hdr->full[stage]);
         const int k0 = (split * KT + kt) * kTileK;
-        if (lane == 0) {
+        if (lane == 0 && !(held && it == 0)) {
           // The stage's bytes: the activation tiles issued here, and the
           // embedding tile (tiled here, or gathered by the epilogue warps).
           mbar_expect_tx(fb, C::kStageBytes);
@@ -299,6 +306,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       }
       if (stop || hdr->abort) break;
     }
+    prod_it = it;
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -307,7 +315,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       int tl = 0;
       for (int task = blockIdx.x; task < n_tasks; task += gridDim.x, ++tl) {
         const int acc = tl & 1;
-        if (!mbar_wait(smem_u32(&hdr->tempty[acc]), (uint32_t)(((tl >> 1) & 1) ^ 1))) {
+        if (!mbar_wait(smem_u32(&hdr->tempty[acc]), (uint32_t)(((tl >> 1) & 1) ^ 1), wl)) {
           hdr->abort = 1;
           break;
         }
@@ -316,7 +324,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         bool stop = false;
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int stage = (int)(it % S);
-          if (!mbar_wait(smem_u32(&hdr->full[stage]), (uint32_t)((it / S) & 1))) {
+          if (!mbar_wait(smem_u32(&hdr->full[stage]), (uint32_t)((it / S) & 1), wl)) {
             hdr->abort = 1;
             stop = true;
             break;
@@ -376,13 +384,19 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         bool stop = false;
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int stage = (int)(it % S);
-          if (!mbar_wait(smem_u32(&hdr->empty[stage]), (uint32_t)((it / S) & 1) ^ 1u)) {
+          if (!mbar_wait(smem_u32(&hdr->empty[stage]), (uint32_t)((it / S) & 1) ^ 1u, wl)) {
             hdr->abort = 1;
             stop = true;
             break;
           }
+          // (After an abort nothing more is issued: the exit path waits only
+          // for the stages the producer armed.)
+          if (*reinterpret_cast<volatile int32_t*>(&hdr->abort)) {
+            stop = true;
+            break;
+          }
           const uint32_t b_base = tiles_s + stage * C::kStageBytes + MT * kATileBytes;
-          if (lane < kGroups)
+          if (lane < kGroups && !(held && it == 0))
             tma_gather4(b_base + g * 4 * kRowBytes, &tmG, (split * KT + kt) * kTileK, rr0, rr1, rr2, rr3,
                         smem_u32(&hdr->full[stage]));
         }
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           cb[3] |= (c >> 5) == 3 ? bit : 0u;
         }
       }
-      if (!mbar_wait(smem_u32(&hdr->tfull[acc]), (uint32_t)((tl >> 1) & 1))) {
+      if (!mbar_wait(smem_u32(&hdr->tfull[acc]), (uint32_t)((tl >> 1) & 1), wl)) {
         hdr->abort = 1;
         break;
       }
@@ -501,6 +515,23 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (hdr->abort) {
+    // A wait ran out.  Before the CTA leaves, everything it started must be
+    // finished (each wait again bounded): the MMA issuer's MMAs (one commit
+    // tracks all of them), and the loads of every stage the producer armed and
+    // no MMA consumed (its last S issues; the epilogue's gathers of those
+    // stages land on the same barriers).
+    if (warp == 1 && lane == 0) {
+      mma_commit(smem_u32(&hdr->drain));
+      mbar_wait(smem_u32(&hdr->drain), 0u, wl);
+    }
+    if (warp == 0 && lane == 0) {
+      for (long long j = prod_it > S ? prod_it - S : 0; j < prod_it; ++j)
+        if (!(held && j == 0)) mbar_wait(smem_u32(&hdr->full[j % S]), (uint32_t)((j / S) & 1), wl);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
@@ -570,6 +601,7 @@ cudaError_t launch_union_gemm(const GemmParams& p, const void* hidden, int64_t r
   // (more, shorter tasks for its few column tiles); the full-vocabulary GEMM
   // keeps both M tiles in one CTA so that every embedding tile is read once.
   GemmParams q = p;
+  if (q.wait_limit <= 0) q.wait_limit = kWaitLimit;
   const bool two_m = p.B > 128 && p.row_list == nullptr;
   q.msplit = p.B > 128 && !two_m ? 2 : 1;
   cfg.gridDim = dim3(num_ctas);

@@ -39,6 +39,9 @@ struct GemmParams {
   int32_t msplit;            // set by the launcher: 128-sequence M tiles taken by separate tasks
   float* split_part;         // [ksplit, B, C] candidate partial sums (ksplit > 1)
   int32_t* err;              // set to 1 when a wait timed out
+  long long wait_limit;      // try_wait polls of one wait before it gives up (the launcher fills 0 in)
+  int32_t withhold;          // test switch: CTA 0 issues nothing for its first stage, so the waits on
+                             // that stage run out (the error path without any fault)
 };
 
 // Tensor maps of the embedding: 64 x 128 boxes (contiguous rows) and 64 x 1

@@ -57,7 +57,7 @@ struct Partial {
   float logit;
   int32_t tok;
   int32_t edge;
-  int32_t pad;
+  int32_t err;  // the CTA's error flag (nonzero: its filter or a bounded wait failed)
 };
 
 // Device control block of the device-resident loop.
@@ -101,7 +101,9 @@ struct HeadScratch {
   int32_t ksplit;           // K splits of the union GEMM (fixed by the hidden size)
   float* split_part;        // [ksplit, B, C] per-split candidate sums of the union GEMM
   int32_t union_mode;       // 1: columns are the union; 0: every vocabulary row
-  int32_t* gemm_err;        // [1] GEMM wait timeout
+  int32_t* gemm_err;        // [1] GEMM wait timeout (cleared by every reset)
+  long long wait_limit;     // polls of one GEMM wait before it gives up (0: the default)
+  int32_t withhold;         // test switch of the GEMM (see GemmParams::withhold)
   int32_t* row0;            // [1] first activation row of the current step
   const EmbMaps* emb_maps;  // host: tensor maps of the embedding
 };
@@ -171,6 +173,7 @@ struct ResetParams {
   int32_t iv;               // 1: read-only no-repeat state (no count arrays to fill)
   uint32_t* seq_ticket;
   Ctrl* ctrl;
+  int32_t* gemm_err;        // the GEMM heads' timeout flag, cleared here (null before their first use)
   int32_t* toks;            // optional [B, max_steps] prefill with -1
   float* logits;            // optional [B, max_steps] prefill with 0
   int32_t* lens_out;        // optional

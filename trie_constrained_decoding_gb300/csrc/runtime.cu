@@ -91,9 +91,6 @@ struct DevGrammar {
   bool force_counts = false;  // TC_BIND_LIVE_COUNTS: per-sequence count arrays for every k
   bool no_counts = false;     // character-level grammar: no pointer paths, read-only state only
   int32_t iv = 0;             // state mode of the last reset (1: read-only no-repeat state)
-  // A tc_step with another head ran since the last reset: the sparse step's
-  // precomputed candidate lists may describe a node the sequences have left.
-  bool pre_stale = false;
   size_t cnt_batch = 0;       // sequences the count arrays (allocated on first use) hold
 
   GrammarView view() const {
@@ -348,6 +345,7 @@ ResetParams reset_params(const tc_ctx* c, const DevGrammar* g, int B, int k, int
   r.seq_ticket = c->d_seq_ticket;
   r.ctrl = c->d_ctrl;
   r.stats = c->d_stats;
+  r.gemm_err = c->hs_ready ? c->hs.gemm_err : nullptr;
   return r;
 }
 
@@ -756,7 +754,6 @@ extern "C" tc_status tc_reset(tc_ctx* c, int32_t batch, int32_t k, void* stream)
   g->batch = batch;
   g->k = k;
   g->iv = r.iv;
-  g->pre_stale = false;
   return TC_OK;
 }
 
@@ -793,15 +790,7 @@ tc_status step_impl(tc_ctx* c, const void* hidden, int32_t head, const tc_sampli
     p.smp_tok = c->d_smp_tok;
     p.smp_edge = c->d_smp_edge;
   }
-  if (head == TC_HEAD_SPARSE && g->pre_stale) {
-    // The other heads move a sequence without refreshing its precomputed list:
-    // drop every list (pre_n = 0) so that this step filters its node.
-    TC_CUDA(cudaMemset2DAsync(reinterpret_cast<char*>(g->d_st) + offsetof(SeqState, pre_n), sizeof(SeqState), 0,
-                              sizeof(int32_t), (size_t)g->batch, s));
-    g->pre_stale = false;
-  }
   TC_CUDA(launch_any_step(c, g, p, head, s, false));
-  if (head != TC_HEAD_SPARSE) g->pre_stale = true;
   return TC_OK;
 }
 
@@ -994,6 +983,20 @@ extern "C" tc_status tc_first_error(tc_ctx* c, void* stream, int32_t* seq, int32
       break;
     }
   }
+  return TC_OK;
+}
+
+extern "C" tc_status tc_gemm_wait_test(tc_ctx* c, int32_t withhold, int64_t wait_polls) {
+  if (!c || wait_polls < 0) return TC_ERR_INVALID_ARG;
+  DeviceGuard dg(c->device);
+  tc_status rc = ensure_gemm_scratch(c);
+  if (rc != TC_OK) return rc;
+  // Captured graphs hold the kernels' parameters as they were: drop them.
+  TC_CUDA(cudaDeviceSynchronize());
+  for (tc_graph* g : c->cache) destroy_graph(g);
+  c->cache.clear();
+  c->hs.withhold = withhold ? 1 : 0;
+  c->hs.wait_limit = wait_polls;
   return TC_OK;
 }
 

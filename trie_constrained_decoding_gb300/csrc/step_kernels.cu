@@ -586,7 +586,8 @@ __device__ __forceinline__ int finish_sequence(const StepParams& p, const WalkRd
   bool stop = false;
   int4 chain_hdr = make_int4(0, 0, -1, 0);  // header of the node after the transition (jump only)
   if (err) {
-    status = TC_ERR_BOUNDS;
+    // (a wait that gave up reports its own code; any other error flag is an index out of range)
+    status = err == TC_ERR_DEVICE_TIMEOUT ? TC_ERR_DEVICE_TIMEOUT : TC_ERR_BOUNDS;
   } else if (ncand == 0) {
     status = TC_ERR_EMPTY_MASK;
   } else if (best_t == INT_MAX || best_e < 0 || best_e >= p.g.n_edges || !(best_l == best_l)) {
@@ -621,6 +622,10 @@ __device__ __forceinline__ int finish_sequence(const StepParams& p, const WalkRd
   if (tid < 32) {
     const int lane = tid;
     SeqState ns = s;
+    // This path keeps no candidate list for the next node: a sparse step
+    // after it filters that node itself (whatever head or kernel runs next).
+    ns.pre_n = 0;
+    ns.pre_pid = -2;
     if (status != TC_OK) {
       ns.status = status;
       ns.done = 1;
@@ -740,8 +745,10 @@ __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kCon
         if (better(sh.wl[i], sh.wt[i], bl, bt)) { bl = sh.wl[i]; bt = sh.wt[i]; be = sh.we[i]; }
       int last = 1;
       if (tiles > 1) {
+        // Each CTA's best and its error flag (a CTA whose bounded wait ran out
+        // fails the sequence's step, whichever CTA arrives last).
         Partial* slot = p.part + (size_t)b * gridDim.x;
-        slot[t] = Partial{bl, bt, be, 0};
+        slot[t] = Partial{bl, bt, be, sh.err};
         __threadfence();
         const uint32_t ticket = atomicAdd(&p.seq_ticket[b], 1u);
         last = (ticket == (uint32_t)tiles - 1);
@@ -754,6 +761,7 @@ __device__ __forceinline__ void step_tail(const StepParams& p, const WalkRd<kCon
             const float l = __ldcg(&slot[i].logit);
             const int32_t tk = __ldcg(&slot[i].tok);
             const int32_t ee = __ldcg(&slot[i].edge);
+            if (__ldcg(&slot[i].err) == TC_ERR_DEVICE_TIMEOUT) sh.err = TC_ERR_DEVICE_TIMEOUT;
             if (better(l, tk, bl, bt)) { bl = l; bt = tk; be = ee; }
           }
           p.seq_ticket[b] = 0;
@@ -1562,7 +1570,7 @@ __global__ void __launch_bounds__(kThreads) dense_step_kernel(const StepParams p
         // A copy never completed: wait (bounded) for the ones still in flight, then report.
         if (tid == 0) {
           for (int c = 0; c < n_chunks; ++c) stage_wait(smem_addr(&full[c % S]), (uint32_t)((c / S) & 1));
-          sh.err = 1;
+          sh.err = TC_ERR_DEVICE_TIMEOUT;
         }
         __syncthreads();
       }
@@ -1598,6 +1606,7 @@ __global__ void __launch_bounds__(kThreads) reset_kernel(const ResetParams r) {
     }
     if (b == 0 && tid == 0) {
       if (r.stats) atomicAdd(&r.stats[kStatResetLaunches], 1ull);
+      if (r.gemm_err) *r.gemm_err = 0;  // a timed-out GEMM wait fails the steps up to the next reset only
       r.ctrl->live = r.B;
       r.ctrl->ticket = 0u;
       if (r.cond) cudaGraphSetConditional((cudaGraphConditionalHandle)r.cond, r.B > 0 ? 1u : 0u);
@@ -1771,7 +1780,8 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
   // The step's scalars are read together with the state (one round trip).
   const SeqState s = p.st[b];
   const int n = hs.ncand[b];
-  const int err = hs.errf[b] | *hs.gemm_err;  // a GEMM wait that timed out fails the step
+  // A GEMM wait that timed out fails the step of every sequence.
+  const int err = *hs.gemm_err ? TC_ERR_DEVICE_TIMEOUT : hs.errf[b];
   const int n_cols = hs.union_mode ? *hs.n_union : p.V;
   const int mode = seq_mode(p, s);
   float wl = -INFINITY;
@@ -2040,6 +2050,8 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
   gp.ksplit = q.hs.union_mode ? q.hs.ksplit : 1;
   gp.split_part = q.hs.split_part;
   gp.err = q.hs.gemm_err;
+  gp.wait_limit = q.hs.wait_limit;
+  gp.withhold = q.hs.withhold;
   if ((e = launch_union_gemm(gp, p.hidden, p.hidden_rows, *q.hs.emb_maps, gemm_ctas, s)) != cudaSuccess) return e;
   return const_resident ? launch_pdl(gemm_finish_kernel<true>, dim3(1, p.B), dim3(kThreads), 0, s, q)
                         : launch_pdl(gemm_finish_kernel<false>, dim3(1, p.B), dim3(kThreads), 0, s, q);

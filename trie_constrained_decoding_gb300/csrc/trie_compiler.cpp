@@ -356,6 +356,7 @@ extern "C" const char* tc_status_str(tc_status s) {
     case TC_ERR_NO_LIVE_EDGE: return "TC_ERR_NO_LIVE_EDGE";
     case TC_ERR_MAX_STEPS: return "TC_ERR_MAX_STEPS";
     case TC_ERR_BOUNDS: return "TC_ERR_BOUNDS";
+    case TC_ERR_DEVICE_TIMEOUT: return "TC_ERR_DEVICE_TIMEOUT";
     case TC_ERR_CUDA: return "TC_ERR_CUDA";
     case TC_ERR_OOM: return "TC_ERR_OOM";
   }
