@@ -422,11 +422,13 @@ tc_status tc_read_seq_state(tc_ctx* ctx, void* stream, int32_t* node, int32_t* e
  * kernel counters into out (host) int64[TC_STAT_SLOTS]: step-kernel launches
  * (idle launches at the end of a graph loop included), head decisions (one
  * per live sequence per step), legal candidates evaluated (rows gathered by
- * the sparse head), reset-kernel launches, and tokens emitted as forced
- * continuations (TC_FLAG_JUMP_FORWARD).  reset != 0 zeroes them afterwards.
+ * the sparse head), reset-kernel launches, tokens emitted as forced
+ * continuations (TC_FLAG_JUMP_FORWARD), and the union head's rows (the size
+ * of the union of legal rows, summed over its steps).  reset != 0 zeroes them
+ * afterwards.
  * Used to count launches and algorithmic bytes.
  */
-#define TC_STAT_SLOTS 5
+#define TC_STAT_SLOTS 6
 tc_status tc_read_stats(tc_ctx* ctx, void* stream, int64_t* out, int32_t reset);
 
 /*

@@ -31,7 +31,7 @@ BIND_LIVE_COUNTS = 0x10        # or-ed into bind's residency: per-sequence live-
 HEAD_SPARSE, HEAD_DENSE, HEAD_UNION_GEMM, HEAD_DENSE_GEMM = 0, 1, 2, 3
 FLAG_JUMP_FORWARD = 0x100      # or-ed into `head` of decode / decode_graph: forced tokens skip the head
 FLAG_FORCED_LOGITS = 0x200     # with FLAG_JUMP_FORWARD: forced tokens still get their logits
-STAT_SLOTS = 5
+STAT_SLOTS = 6
 TC_ERR_EMPTY_MASK, TC_ERR_NO_LIVE_EDGE, TC_ERR_MAX_STEPS, TC_ERR_BOUNDS = 16, 17, 18, 19
 TC_ERR_DEVICE_TIMEOUT = 20
 CONST_CAPACITY_BYTES = 63 * 1024
@@ -304,7 +304,7 @@ class Context:
         out = np.zeros(STAT_SLOTS, dtype=np.int64)
         _check(_read_stats(self._h, _stream_ptr(stream), out.ctypes.data_as(_i64p), int(reset)), "tc_read_stats")
         return {"step_launches": int(out[0]), "seq_steps": int(out[1]), "cand_rows": int(out[2]),
-                "reset_launches": int(out[3]), "forced": int(out[4])}
+                "reset_launches": int(out[3]), "forced": int(out[4]), "union_rows": int(out[5])}
 
     def gemm_wait_test(self, withhold: bool, wait_polls: int = 0):
         """tc_gemm_wait_test: make the GEMM heads' first pipeline stage never

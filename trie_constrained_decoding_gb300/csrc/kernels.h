@@ -160,7 +160,8 @@ enum StatSlot {
   kStatCandRows = 2,       // legal candidates the head evaluated
   kStatResetLaunches = 3,
   kStatForced = 4,         // tokens emitted as forced continuations (no head read)
-  kStatSlots = 5
+  kStatUnionRows = 5,      // union head: rows of the union, summed over its steps
+  kStatSlots = 6
 };
 
 struct ResetParams {

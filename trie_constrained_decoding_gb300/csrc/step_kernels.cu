@@ -1724,7 +1724,10 @@ __global__ void __launch_bounds__(kCompactThreads) union_compact_kernel(const St
       ++idx;
     }
   }
-  if (tid == 0) *hs.n_union = s_warp[kCompactThreads / 32 - 1];
+  if (tid == 0) {
+    *hs.n_union = s_warp[kCompactThreads / 32 - 1];
+    if (p.stats) atomicAdd(&p.stats[kStatUnionRows], (unsigned long long)s_warp[kCompactThreads / 32 - 1]);
+  }
 }
 
 // Grid (1, B): the GEMM column of each of sequence b's candidates, and for
@@ -2028,7 +2031,9 @@ cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head,
                       : launch_pdl(cand_filter_kernel<false>, dim3(1, p.B), dim3(kThreads), fsmem, s, no_ctrl);
   if (e != cudaSuccess) return e;
   if (q.hs.union_mode) {
-    if ((e = launch_pdl(union_compact_kernel, dim3(1), dim3(kCompactThreads), 0, s, no_ctrl)) != cudaSuccess) return e;
+    StepParams counted = no_ctrl;
+    counted.stats = p.stats;  // (the compaction counts the union's rows)
+    if ((e = launch_pdl(union_compact_kernel, dim3(1), dim3(kCompactThreads), 0, s, counted)) != cudaSuccess) return e;
     if ((e = launch_pdl(cand_column_kernel, dim3(1, p.B), dim3(kThreads), (size_t)p.cand_cap * sizeof(int32_t), s,
                         no_ctrl)) != cudaSuccess)
       return e;
