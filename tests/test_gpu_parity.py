@@ -367,3 +367,26 @@ def test_dense_gemm_ragged_two_m_tiles_equal_narrow_batches(tcd):
             assert np.array_equal(out[i], wide[i][lo:hi]), (lo, i)
     ctx.close()
     check_against_oracle("batched", hid, wide, w.k, w.max_steps, exact=False)
+
+
+def test_multi_cta_step_x_in_shared_memory_equals_register_variant(tcd):
+    """The multi-CTA sparse step stages the hidden state in shared memory (two
+    CTAs per SM) when one wave of its register variant cannot give every
+    sequence the CTAs its widest node needs: the hex catalog (root fan-out
+    267) at B=16 takes it, at B=4 it does not.  Both use the same lane map and
+    reduction tree, so the 16 queries decoded as one batch equal the same
+    queries in four batches of 4, bit for bit."""
+    w = workload("unstructured")
+    hid = w.hidden_states(0, 16)
+    ctx, _ = make_ctx(tcd, "unstructured", max_batch=16)
+    wide = DecodeBuffers(w.max_steps, 16, w.hidden, w.max_steps)
+    wide.load(hid)
+    a = wide.run(ctx, w.k)
+    assert np.all(a[3] == 0)
+    narrow = DecodeBuffers(w.max_steps, 4, w.hidden, w.max_steps)
+    for q in range(0, 16, 4):
+        narrow.load(hid[:, q:q + 4])
+        b = narrow.run(ctx, w.k)
+        for i in range(4):
+            assert np.array_equal(b[i], a[i][q:q + 4]), (q, i)
+    ctx.close()

@@ -151,6 +151,7 @@ struct StepParams {
   int32_t* smp_tok;
   int32_t* smp_edge;
   int32_t wide;             // batch above the SM count: the one-CTA step stages x in shared memory
+  int32_t multi_xs;         // multi-CTA sparse step: x staged in shared memory (two CTAs per SM)
 };
 
 // Cumulative counters kept by the kernels (one atomic per launch / per sequence step).
@@ -188,7 +189,8 @@ enum Head { kHeadSparse = 0, kHeadDense = 1, kHeadUnionGemm = 2, kHeadDenseGemm 
 // Number of CTAs per sequence the multi-CTA sparse step uses for a grammar of
 // the given largest fan-out at batch B (at most one wave of resident CTAs),
 // and the dense step's CTAs per sequence.
-int sparse_tiles(int max_fanout, int B, int num_sms, int H, int cand_cap, bool const_resident);
+// *xs_out: 1 when the step stages x in shared memory for two CTAs per SM.
+int sparse_tiles(int max_fanout, int B, int num_sms, int H, int cand_cap, bool const_resident, int* xs_out);
 int dense_tiles(int B, int num_sms);
 
 // Opt the step kernels in to kMaxDynamicSmem bytes of dynamic shared memory

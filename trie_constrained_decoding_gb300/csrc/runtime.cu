@@ -184,10 +184,11 @@ namespace {
 // which also precomputes the next step's candidates.
 bool one_cta_sparse(const DevGrammar* g) { return g->max_fanout <= 32; }
 
-int tiles_for(const tc_ctx* c, const DevGrammar* g, int head, int B) {
+int tiles_for(const tc_ctx* c, const DevGrammar* g, int head, int B, int* xs = nullptr) {
+  if (xs) *xs = 0;
   if (head == TC_HEAD_SPARSE && one_cta_sparse(g)) return 1;
   return head == TC_HEAD_SPARSE ? sparse_tiles(g->max_fanout, B, c->num_sms, c->H, c->cand_cap,
-                                              g->residency == TC_RES_CONST)
+                                              g->residency == TC_RES_CONST, xs)
                                  : dense_tiles(B, c->num_sms);
 }
 
@@ -275,7 +276,9 @@ cudaError_t launch_any_step(tc_ctx* c, DevGrammar* g, const StepParams& p, int h
     q.hs = c->hs;
     return launch_gemm_step(q, cst, head, gemm_ctas(c, head), s);
   }
-  return launch_step(p, cst, head, tiles_for(c, g, head, p.B), s, pdl);
+  StepParams q = p;
+  const int tiles = tiles_for(c, g, head, p.B, &q.multi_xs);
+  return launch_step(q, cst, head, tiles, s, pdl);
 }
 
 StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {

@@ -161,6 +161,20 @@ __device__ __forceinline__ float row_dot(const uint16_t* row, const XFrag<NCH>& 
   return warp_sum(acc);
 }
 
+// row_dot with x staged in shared memory but the row's NCH chunks all in
+// flight at once (the same lane map and order: bit-identical to row_dot).
+template <int NCH>
+__device__ __forceinline__ float row_dot_xs(const uint16_t* row, const uint4* xs, int lane) {
+  const uint4* r4 = reinterpret_cast<const uint4*>(row);
+  uint4 e[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) e[i] = ld_row(r4 + i * 32 + lane);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xs[i * 32 + lane], acc);
+  return warp_sum(acc);
+}
+
 // Two rows at once (more loads in flight); each result is bit-identical to row_dot.
 template <int NCH>
 __device__ __forceinline__ void row_dot2(const uint16_t* ra, const uint16_t* rb, const XFrag<NCH>& xf,
@@ -1349,8 +1363,11 @@ __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(con
 
 // ---------------------------------------------------------------- multi-CTA sparse step
 
-template <bool kConst, int NCH, bool kSmp = false>
-__global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams p) {
+// kXs: the hidden state staged in shared memory instead of registers (greedy
+// steps at hidden sizes of 2048 and up), so two CTAs share an SM: for batches
+// whose nodes' fan-out needs more CTAs than one wave of the register variant holds.
+template <bool kConst, int NCH, bool kSmp = false, bool kXs = false>
+__global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // A narrow node's step uses the one-CTA step's shared state instead.
   constexpr size_t kShBytes = sizeof(Step1Shared) < sizeof(StepShared) ? sizeof(StepShared) : sizeof(Step1Shared);
@@ -1368,7 +1385,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   const int nch = p.H >> 3;
   const int local_cap = sparse_local_cap(p.cand_cap, T);
   uint4* xs = reinterpret_cast<uint4*>(smem_raw);
-  int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 ? (size_t)nch * 16 : 0));
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem_raw + (NCH == 0 || kXs ? (size_t)nch * 16 : 0));
   int32_t* s_edge = s_tok + local_cap;
   float* s_lg = reinterpret_cast<float*>(s_edge + local_cap);  // sampling only
   // A node needs one CTA per kWarps of its edges: the others leave at once
@@ -1392,7 +1409,7 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   if (narrow) {
     Step1Shared& sh1 = *reinterpret_cast<Step1Shared*>(sh_raw);
     if (p.stats && tid == 0 && t == 0 && b == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
-    if (t == 0) step1_body<kConst, NCH, false>(p, b, s, pre0, sh1, smem_raw);
+    if (t == 0) step1_body<kConst, NCH, kXs>(p, b, s, pre0, sh1, smem_raw);
     loop_control(p, sh1.done_after);
     return;
   }
@@ -1401,10 +1418,11 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
   int32_t wt = INT_MAX, we = -1;
   if (mode == 1 && t < A) {
     const uint16_t* x = hidden_row(p, s, b);
-    XFrag<NCH> xf;
-    if constexpr (NCH > 0) {
+    XFrag<kXs ? 0 : NCH> xf;
+    if constexpr (NCH > 0 && !kXs) {
       xf.load(x, lane);
     } else {
+      // (visible to every warp after the filter's closing barrier)
       for (int c = tid; c < nch; c += kThreads) xs[c] = __ldg(reinterpret_cast<const uint4*>(x) + c);
     }
     filter_node<kConst>(p, w, s, b, A, t, s_tok, s_edge, sh);
@@ -1413,7 +1431,9 @@ __global__ void __launch_bounds__(kThreads) sparse_step_kernel(const StepParams 
       const int nlocal = nc > t ? (nc - t + A - 1) / A : 0;
       for (int l = warp; l < nlocal; l += kWarps) {
         const int32_t tok = s_tok[l];
-        const float v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
+        float v;
+        if constexpr (kXs) v = row_dot_xs<NCH>(p.emb + (size_t)tok * p.H, xs, lane);
+        else v = row_dot<NCH>(p.emb + (size_t)tok * p.H, xf, xs, nch, lane);
         if (better(v, tok, wl, wt)) { wl = v; wt = tok; we = s_edge[l]; }
         if (kSmp && lane == 0) s_lg[l] = v;
       }
@@ -1873,13 +1893,21 @@ namespace {
 // Resident CTAs per SM of the multi-CTA sparse step for this hidden size and
 // dynamic shared memory (registers usually allow one).
 template <bool kConst>
-int sparse_occupancy(int H, size_t smem) {
+int sparse_occupancy(int H, size_t smem, bool xs) {
   int occ = 0;
   cudaError_t e;
   switch (H) {
     case 256: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 1>, kThreads, smem); break;
-    case 2048: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 8>, kThreads, smem); break;
-    case 4096: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 16>, kThreads, smem); break;
+    case 2048:
+      e = xs ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 8, false, true>,
+                                                             kThreads, smem)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 8>, kThreads, smem);
+      break;
+    case 4096:
+      e = xs ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 16, false, true>,
+                                                             kThreads, smem)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 16>, kThreads, smem);
+      break;
     default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_step_kernel<kConst, 0>, kThreads, smem); break;
   }
   if (e != cudaSuccess) {
@@ -1891,14 +1919,29 @@ int sparse_occupancy(int H, size_t smem) {
 
 }  // namespace
 
-int sparse_tiles(int max_fanout, int B, int num_sms, int H, int cand_cap, bool const_resident) {
+int sparse_tiles(int max_fanout, int B, int num_sms, int H, int cand_cap, bool const_resident, int* xs_out) {
   // One warp per candidate, but no more CTAs than the GPU holds at once: a
   // second wave would add a whole kernel's latency to every step.
   int by_fan = (max_fanout + kWarps - 1) / kWarps;
   const int b = B > 0 ? B : 1;
   const size_t xbytes = (H == 256 || H == 2048 || H == 4096) ? 0 : (size_t)H * 2;  // x staged for other sizes
-  const size_t smem = xbytes + 2 * (size_t)sparse_local_cap(cand_cap, by_fan > 0 ? by_fan : 1) * sizeof(int32_t);
-  const int occ = const_resident ? sparse_occupancy<true>(H, smem) : sparse_occupancy<false>(H, smem);
+  const size_t lists = 2 * (size_t)sparse_local_cap(cand_cap, by_fan > 0 ? by_fan : 1) * sizeof(int32_t);
+  const size_t smem = xbytes + lists;
+  int occ = const_resident ? sparse_occupancy<true>(H, smem, false) : sparse_occupancy<false>(H, smem, false);
+  // When one wave of the register variant cannot give every sequence the
+  // CTAs its widest node needs, stage x in shared memory if that fits more
+  // CTAs per SM.
+  int xs = 0;
+  if ((H == 2048 || H == 4096) && (long long)b * by_fan > (long long)num_sms * occ) {
+    const size_t smem_xs = (size_t)H * 2 + lists;
+    const int occ_xs = const_resident ? sparse_occupancy<true>(H, smem_xs, true)
+                                      : sparse_occupancy<false>(H, smem_xs, true);
+    if (occ_xs > occ) {
+      occ = occ_xs;
+      xs = 1;
+    }
+  }
+  if (xs_out) *xs_out = xs;
   int by_grid = (num_sms * occ) / b;
   if (by_grid < 1) by_grid = 1;
   int t = by_fan < by_grid ? by_fan : by_grid;
@@ -1952,6 +1995,12 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
     cfg.dynamicSmemBytes = sample_smem_offset(p, tiles) + kSampleSmem;
     return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH, true>, p);
   }
+  if constexpr (NCH >= 8) {
+    if (head == kHeadSparse && p.multi_xs) {
+      cfg.dynamicSmemBytes = (size_t)nch * 16 + 2 * (size_t)cap * sizeof(int32_t);
+      return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH, false, true>, p);
+    }
+  }
   if (head == kHeadSparse) return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH>, p);
   return cudaLaunchKernelEx(&cfg, dense_step_kernel<kConst, NCH>, p);
 }
@@ -1963,6 +2012,11 @@ cudaError_t prepare_one() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
+  if constexpr (NCH >= 8) {
+    e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+  }
   return cudaFuncSetAttribute(dense_step_kernel<kConst, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
 }
 
