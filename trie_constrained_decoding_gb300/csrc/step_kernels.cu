@@ -1168,8 +1168,6 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
           const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
           if (lane == 0) sh.spec_n[l] = sn;
           __syncwarp();
-          // If this candidate wins, its child's rows are the next step's reads: start them towards L2 now.
-          if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].a.x * p.H, (uint32_t)p.H * 2u);
           if constexpr (kXs) {
 #pragma unroll
             for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xs[i * 32 + lane], acc);
@@ -1181,8 +1179,6 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
           const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
           if (lane == 0) sh.spec_n[l] = sn;
           __syncwarp();
-          // If this candidate wins, its child's rows are the next step's reads: start them towards L2 now.
-          if (lane < sn) prefetch_l2(p.emb + (size_t)sh.spec[l][lane].a.x * p.H, (uint32_t)p.H * 2u);
           for (int c = lane; c < nch; c += 32) acc = dot8(ld_row(r4 + c), xs[c], acc);
         }
         const float v = warp_sum(acc);
@@ -1276,7 +1272,13 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
     // separator (the root's set is not precomputed), or when no set was kept
     // (a child wider than a list, counted by the chain itself).
     const bool chain = p.jump && status == TC_OK && !stop && (next_n == 1 || next_n < 0 || ptr_done >= 0);
-    if (!chain && lane < next_n) p.pre[(size_t)b * kPreMax + lane] = sh.spec[bs][lane];
+    if (!chain && lane < next_n) {
+      // The next step's candidates: their list, and their rows started towards
+      // L2 (only these rows: prefetching every candidate's child rows while
+      // the rows were in flight cost time at every batch size).
+      p.pre[(size_t)b * kPreMax + lane] = sh.spec[bs][lane];
+      prefetch_l2(p.emb + (size_t)sh.spec[bs][lane].a.x * p.H, (uint32_t)p.H * 2u);
+    }
     if (ptr_done >= 0 && !p.iv) decrement_path(p, b, ptr_done, lane, 32);
     SeqState ns = s;
     int pre_n = next_n, pre_pid = next_n >= 0 ? win.h.z : -2;  // the child's pointer rank
