@@ -55,16 +55,19 @@ constexpr uint32_t kTbWarpBytes = 32 * kTbStride * 4 + 32 * 8;
 // MT: 128-row M tiles (sequences) per CTA.  Warps: TMA producer, MMA issuer,
 // then 8 epilogue warps: with two M tiles each takes one lane quarter of one
 // tile, with one M tile each takes one lane quarter and half of the columns.
+// The two-M-tile configuration serves the full-vocabulary GEMM only, whose K
+// is never split: it has no transpose buffers, and their shared memory holds
+// a fourth stage (more bytes in flight per SM).
 template <int MT>
 struct Cfg {
-  static constexpr int kStages = MT == 2 ? 3 : 5;
+  static constexpr int kStages = MT == 2 ? 4 : 5;
   static constexpr uint32_t kStageBytes = MT * kATileBytes + kBTileBytes;
   static constexpr int kAccCols = MT * kTileN;  // TMEM columns of one accumulator
   static constexpr int kTmemCols = 2 * kAccCols;
   static constexpr int kEpiWarps = 8;
   static constexpr int kChunks = 2 * MT;  // 32-column chunks of a tile per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr size_t kTbBytes = (size_t)kEpiWarps * kTbWarpBytes;
+  static constexpr size_t kTbBytes = MT == 2 ? 0 : (size_t)kEpiWarps * kTbWarpBytes;
 };
 
 struct GemmHdr {
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols + m * kTileN);
-      if (KS > 1) {
+      if (MT == 1 && KS > 1) {
         // This split's partial sum of every candidate, at the candidate's
         // index.  Through a 32 x 32 transpose in shared memory, one store
         // instruction writes consecutive candidates of one sequence.
@@ -603,6 +606,7 @@ cudaError_t launch_union_gemm(const GemmParams& p, const void* hidden, int64_t r
   GemmParams q = p;
   if (q.wait_limit <= 0) q.wait_limit = kWaitLimit;
   const bool two_m = p.B > 128 && p.row_list == nullptr;
+  if (two_m && p.ksplit != 1) return cudaErrorInvalidValue;  // (no transpose buffers for split sums)
   q.msplit = p.B > 128 && !two_m ? 2 : 1;
   cfg.gridDim = dim3(num_ctas);
   cfg.blockDim = dim3(two_m ? Cfg<2>::kThreads : Cfg<1>::kThreads);
