@@ -56,14 +56,18 @@ constexpr uint32_t kTbWarpBytes = 32 * kTbStride * 4 + 32 * 8;
 // then 8 epilogue warps: with two M tiles each takes one lane quarter of one
 // tile, with one M tile each takes one lane quarter and half of the columns.
 // The two-M-tile configuration serves the full-vocabulary GEMM only, whose K
-// is never split: it has no transpose buffers, and their shared memory holds
-// a fourth stage (more bytes in flight per SM).
+// is never split (no transpose buffers).  Its tasks are 256 columns wide, so
+// each activation tile loaded serves twice as many columns (the activations
+// are re-read once per task); the accumulator (two M tiles x 256 columns)
+// then fills the 512 TMEM columns, so there is one, not two.
 template <int MT>
 struct Cfg {
-  static constexpr int kStages = MT == 2 ? 4 : 5;
-  static constexpr uint32_t kStageBytes = MT * kATileBytes + kBTileBytes;
-  static constexpr int kAccCols = MT * kTileN;  // TMEM columns of one accumulator
-  static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr int kTaskN = MT == 2 ? 256 : kTileN;  // columns per task (one MMA's N)
+  static constexpr int kStages = MT == 2 ? 3 : 5;
+  static constexpr uint32_t kStageBytes = MT * kATileBytes + (uint32_t)kTaskN * kRowBytes;
+  static constexpr int kAccCols = MT * kTaskN;  // TMEM columns of one accumulator
+  static constexpr int kAccs = MT == 2 ? 1 : 2;  // accumulators in TMEM (512 columns)
+  static constexpr int kTmemCols = kAccs * kAccCols;
   static constexpr int kEpiWarps = 8;
   static constexpr int kChunks = 2 * MT;  // 32-column chunks of a tile per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   const uint32_t tmem = hdr->tmem_base;
   const int row0 = hdr->row0;
   const int n_cols = hdr->n_cols;
-  const int n_tiles = (n_cols + kTileN - 1) / kTileN;
+  const int n_tiles = (n_cols + C::kTaskN - 1) / C::kTaskN;
   const int n_tasks = n_tiles * KS * MS;
 
   if (warp == 0) {
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     long long it = 0;
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
       const int mt = task % MS, tile = task / MS / KS, split = task / MS % KS;
-      const int n0 = tile * kTileN;
+      const int n0 = tile * C::kTaskN;
       bool stop = false;
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const int stage = (int)(it % S);
@@ -303,7 +307,10 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           // embedding tile (tiled here, or gathered by the epilogue warps).
           mbar_expect_tx(fb, C::kStageBytes);
           for (int m = 0; m < MT; ++m) tma_tile_2d(a_base + m * kATileBytes, &tmA, k0, row0 + (mt + m) * 128, fb);
-          if (!gather) tma_tile_2d(b_base, &tmB, k0, n0, fb);
+          // (rows past the vocabulary are filled with zeros and count in full)
+          if (!gather)
+            for (int h = 0; h < C::kTaskN / kTileN; ++h)
+              tma_tile_2d(b_base + h * kBTileBytes, &tmB, k0, n0 + h * kTileN, fb);
         }
         __syncwarp();
       }
@@ -313,12 +320,12 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, kTileN);
+      constexpr uint32_t idesc = idesc_bf16(128, C::kTaskN);
       long long it = 0;
       int tl = 0;
       for (int task = blockIdx.x; task < n_tasks; task += gridDim.x, ++tl) {
-        const int acc = tl & 1;
-        if (!mbar_wait(smem_u32(&hdr->tempty[acc]), (uint32_t)(((tl >> 1) & 1) ^ 1), wl)) {
+        const int acc = tl % C::kAccs;
+        if (!mbar_wait(smem_u32(&hdr->tempty[acc]), (uint32_t)(((tl / C::kAccs) & 1) ^ 1), wl)) {
           hdr->abort = 1;
           break;
         }
@@ -339,8 +346,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           for (int m = 0; m < MT; ++m) {
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk) {
-              mma_bf16(d + m * kTileN, sw128_desc(a_base + m * kATileBytes + kk * 32), sw128_desc(b_base + kk * 32),
-                       idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+              mma_bf16(d + m * C::kTaskN, sw128_desc(a_base + m * kATileBytes + kk * 32),
+                       sw128_desc(b_base + kk * 32), idesc, (kt > 0 || kk > 0) ? 1u : 0u);
             }
           }
           mma_commit(smem_u32(&hdr->empty[stage]));
@@ -363,8 +370,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     int tl = 0;
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x, ++tl) {
       const int mt = task % MS, tile = task / MS / KS, split = task / MS % KS;
-      const int n0 = tile * kTileN;
-      const int acc = tl & 1;
+      const int n0 = tile * C::kTaskN;
+      const int acc = tl % C::kAccs;
       const int s0 = (mt + m) * 128 + q * 32;  // this warp's first sequence
       const int b = s0 + lane;
       const bool has = hdr->active[b] != 0;
@@ -405,9 +412,12 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         }
         if (stop) break;
       }
-      // Which columns of this tile are this sequence's candidates, and the
+      // Which columns of this task are this sequence's candidates, and the
       // index of the first one (found while the MMAs of this task run).
-      uint32_t cb[kTileN / 32] = {0u, 0u, 0u, 0u};
+      constexpr int NH = C::kTaskN / kTileN;  // 128-column halves of a task
+      uint32_t cb[4 * NH];
+#pragma unroll
+      for (int i = 0; i < 4 * NH; ++i) cb[i] = 0u;
       int cpos = 0;
       if (p.tile_cands) {
         if (has) {
@@ -430,20 +440,18 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         cpos = lo;
         for (int i = lo; i < nc; ++i) {
           const int c = cand[i] - n0;
-          if (c >= kTileN) break;
+          if (c >= C::kTaskN) break;
           const uint32_t bit = 1u << (c & 31);  // cb kept in registers: no dynamic index
-          cb[0] |= (c >> 5) == 0 ? bit : 0u;
-          cb[1] |= (c >> 5) == 1 ? bit : 0u;
-          cb[2] |= (c >> 5) == 2 ? bit : 0u;
-          cb[3] |= (c >> 5) == 3 ? bit : 0u;
+#pragma unroll
+          for (int w = 0; w < 4 * NH; ++w) cb[w] |= (c >> 5) == w ? bit : 0u;
         }
       }
-      if (!mbar_wait(smem_u32(&hdr->tfull[acc]), (uint32_t)((tl >> 1) & 1), wl)) {
+      if (!mbar_wait(smem_u32(&hdr->tfull[acc]), (uint32_t)((tl / C::kAccs) & 1), wl)) {
         hdr->abort = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols + m * kTileN);
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols + m * C::kTaskN);
       if (MT == 1 && KS > 1) {
         // This split's partial sum of every candidate, at the candidate's
         // index.  Through a 32 x 32 transpose in shared memory, one store
@@ -491,27 +499,40 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           pos += __popc(bits);
         }
       } else {
-        // Masked argmax of the tile: the warps with the first chunk take all
-        // of the tile's columns, the others only hand the accumulator back.
-        float bl = -INFINITY;
-        int32_t bc = INT32_MAX;
-#pragma unroll 1
-        for (int ch = 0; ch < (ch_lo == 0 ? kTileN / 32 : 0); ++ch) {
-          uint32_t v[32];
-          tmem_ld32(tacc + ch * 32, v);
-          const uint32_t bits = (ch == 0) ? cb[0] : (ch == 1) ? cb[1] : (ch == 2) ? cb[2] : cb[3];
+        // Masked argmax of each 128-column tile of the task: the warps with
+        // the first chunk take all of its columns, the others only hand the
+        // accumulator back.  One partial per 128-column tile.
+        float bl[NH];
+        int32_t bcol[NH];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = __uint_as_float(v[j]);
-            if (((bits >> j) & 1u) && gbetter(x, n0 + ch * 32 + j, bl, bc)) {
-              bl = x;
-              bc = n0 + ch * 32 + j;
+        for (int h = 0; h < NH; ++h) {
+          bl[h] = -INFINITY;
+          bcol[h] = INT32_MAX;
+          const int nh0 = n0 + h * kTileN;
+#pragma unroll 1
+          for (int ch = 0; ch < (ch_lo == 0 ? kTileN / 32 : 0); ++ch) {
+            uint32_t v[32];
+            tmem_ld32(tacc + h * kTileN + ch * 32, v);
+            const uint32_t bits = (ch == 0) ? cb[4 * h] : (ch == 1) ? cb[4 * h + 1] : (ch == 2) ? cb[4 * h + 2]
+                                                                                             : cb[4 * h + 3];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float x = __uint_as_float(v[j]);
+              if (((bits >> j) & 1u) && gbetter(x, nh0 + ch * 32 + j, bl[h], bcol[h])) {
+                bl[h] = x;
+                bcol[h] = nh0 + ch * 32 + j;
+              }
             }
           }
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&hdr->tempty[acc]));
-        if (has && ch_lo == 0) p.part[(size_t)b * p.max_tiles + tile] = GemmPartial{bl, bc};
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const int nh0 = n0 + h * kTileN;
+          if (has && ch_lo == 0 && nh0 < n_cols)
+            p.part[(size_t)b * p.max_tiles + nh0 / kTileN] = GemmPartial{bl[h], bcol[h]};
+        }
       }
     }
   }
