@@ -14,8 +14,9 @@ constexpr int kMaxCandCap = 4096;
 // Decode steps per iteration of the graph's WHILE body.  Each iteration of a
 // conditional node costs a few microseconds of its own; running several step
 // kernels per iteration amortises it, at the price of up to kLoopUnroll - 1
-// idle step launches after the last sequence stops.
-constexpr int kLoopUnroll = 8;
+// idle step launches after the last sequence stops (an idle launch that sees
+// the batch already finished only waits, counts itself and steers the loop).
+constexpr int kLoopUnroll = 16;
 // Dynamic shared memory a step kernel may request: x staged for the generic
 // hidden size, two int32 candidate lists of up to kMaxCandCap entries, and
 // (dense head) 128 KiB of row stages or (multi-CTA sampling) 64 KiB of sort

@@ -854,6 +854,21 @@ __device__ __forceinline__ void pdl_enter() {
   pdl_trigger();
 }
 
+// Device form: the live count left by the launch before the previous one is
+// final when this launch starts (the previous launch let this one start only
+// after its own dependency wait returned), so it may be read before this
+// launch's wait.  Zero means every sequence has stopped: the launch then does
+// nothing but count itself and steer the loop, without reading any state
+// (a stale non-zero value takes the normal path, which finds the same).
+__device__ __forceinline__ bool idle_launch(const StepParams& p) {
+  if (!p.device_form || __ldcg(&p.ctrl->live) != 0) return false;
+  pdl_enter();
+  if (p.stats && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
+  const int done_after = 1;
+  loop_control(p, done_after);
+  return true;
+}
+
 // kSmp: sampling instead of the argmax (a separate instantiation, so the greedy
 // kernel carries none of it).
 // ---------------------------------------------------------------- one-CTA sparse step
@@ -1353,6 +1368,7 @@ template <bool kConst, int NCH, bool kXs = false>
 __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ Step1Shared sh;
+  if (idle_launch(p)) return;
   pdl_enter();
   const int b = blockIdx.y;
   // The state and this warp's first precomputed candidate are read together.
@@ -1375,6 +1391,7 @@ __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step_kernel(cons
   constexpr size_t kShBytes = sizeof(Step1Shared) < sizeof(StepShared) ? sizeof(StepShared) : sizeof(Step1Shared);
   __shared__ __align__(16) unsigned char sh_raw[kShBytes];
   StepShared& sh = *reinterpret_cast<StepShared*>(sh_raw);
+  if (idle_launch(p)) return;
   pdl_enter();
   const int b = blockIdx.y, t = blockIdx.x, T = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
