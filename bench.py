@@ -70,6 +70,8 @@ def parse_args():
                     help="per-sequence live-count arrays instead of the read-only no-repeat state")
     ap.add_argument("--jump", action="store_true",
                     help="forced continuations: emit grammar-forced tokens without the head (sparse/dense heads)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences per query batch (default: the workload's)")
     return ap.parse_args()
 
 
@@ -363,6 +365,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = I.WORKLOADS[args.workload]()
+    if args.batch:
+        w.batch = args.batch
     # Each bench step decodes one query batch with the oracle; bounded so that
     # warm-up + steps finish within a few minutes.
     budget = min(120.0, max(5.0, 0.05 * (args.steps + args.warmup)))
@@ -397,6 +401,8 @@ def run_ours(args):
     dev = torch.cuda.current_device()
     stream = torch.cuda.current_stream()
     w = I.WORKLOADS[args.workload]()
+    if args.batch:
+        w.batch = args.batch
     head = {"sparse": tcd.HEAD_SPARSE, "dense": tcd.HEAD_DENSE, "union": tcd.HEAD_UNION_GEMM,
             "dense_gemm": tcd.HEAD_DENSE_GEMM}[args.head]
     if args.jump:
