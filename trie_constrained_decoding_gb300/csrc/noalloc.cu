@@ -46,18 +46,22 @@ std::mutex g_na_mu;
 void* g_na_ptr[kNaMaxDevices];  // device address of g_noalloc_scratch, per device
 int g_na_sms[kNaMaxDevices];
 
-__device__ __forceinline__ float na_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float na_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// Two bf16 products of a packed word pair (low halves first), each rounded
+// once in fp32 (mixed-precision FMA: the same value as an fp32 FMA of the
+// widened operands).
+__device__ __forceinline__ float na_fma2(uint32_t e, uint32_t x, float acc) {
+  asm("{\n .reg .b16 el, eh, xl, xh;\n mov.b32 {el, eh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+      " fma.rn.f32.bf16 %0, el, xl, %0;\n fma.rn.f32.bf16 %0, eh, xh, %0;\n}"
+      : "+f"(acc)
+      : "r"(e), "r"(x));
+  return acc;
+}
 
 __device__ __forceinline__ float na_dot8(const uint4 e, const uint4 x, float acc) {
-  acc = fmaf(na_lo(e.x), na_lo(x.x), acc);
-  acc = fmaf(na_hi(e.x), na_hi(x.x), acc);
-  acc = fmaf(na_lo(e.y), na_lo(x.y), acc);
-  acc = fmaf(na_hi(e.y), na_hi(x.y), acc);
-  acc = fmaf(na_lo(e.z), na_lo(x.z), acc);
-  acc = fmaf(na_hi(e.z), na_hi(x.z), acc);
-  acc = fmaf(na_lo(e.w), na_lo(x.w), acc);
-  acc = fmaf(na_hi(e.w), na_hi(x.w), acc);
+  acc = na_fma2(e.x, x.x, acc);
+  acc = na_fma2(e.y, x.y, acc);
+  acc = na_fma2(e.z, x.z, acc);
+  acc = na_fma2(e.w, x.w, acc);
   return acc;
 }
 

@@ -92,19 +92,26 @@ struct WalkRd {
   }
 };
 
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// acc += e0*x0 + e1*x1 for the two bf16 values packed in each word (low half
+// first), one FMA at a time: the mixed-precision FMA takes the bf16 operands
+// as they are (their fp32 values are exact) and rounds once in fp32, the same
+// result as an fp32 FMA of the widened values, without the widening
+// instructions.
+__device__ __forceinline__ float fma_bf2(uint32_t e, uint32_t x, float acc) {
+  asm("{\n .reg .b16 el, eh, xl, xh;\n mov.b32 {el, eh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+      " fma.rn.f32.bf16 %0, el, xl, %0;\n fma.rn.f32.bf16 %0, eh, xh, %0;\n}"
+      : "+f"(acc)
+      : "r"(e), "r"(x));
+  return acc;
+}
 
 // acc += e[0]*x[0] + ... + e[7]*x[7], one FMA at a time in element order.
 __device__ __forceinline__ float dot8(const uint4 e, const uint4 x, float acc) {
-  acc = fmaf(bf_lo(e.x), bf_lo(x.x), acc);
-  acc = fmaf(bf_hi(e.x), bf_hi(x.x), acc);
-  acc = fmaf(bf_lo(e.y), bf_lo(x.y), acc);
-  acc = fmaf(bf_hi(e.y), bf_hi(x.y), acc);
-  acc = fmaf(bf_lo(e.z), bf_lo(x.z), acc);
-  acc = fmaf(bf_hi(e.z), bf_hi(x.z), acc);
-  acc = fmaf(bf_lo(e.w), bf_lo(x.w), acc);
-  acc = fmaf(bf_hi(e.w), bf_hi(x.w), acc);
+  acc = fma_bf2(e.x, x.x, acc);
+  acc = fma_bf2(e.y, x.y, acc);
+  acc = fma_bf2(e.z, x.z, acc);
+  acc = fma_bf2(e.w, x.w, acc);
   return acc;
 }
 
