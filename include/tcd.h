@@ -169,7 +169,12 @@ tc_status tc_compile_trie(const int32_t* ids, const int64_t* offsets, int32_t n_
                           int32_t sep_id, int32_t stop_id, int32_t vocab, int32_t max_fanout,
                           tc_trie** out);
 
-/* tc_trie_info - sizes of a compiled trie into *out (host). */
+/*
+ * tc_trie_info - sizes of a compiled trie into *out (host): node and edge
+ * counts, fan-outs, depth and the bytes of its walk image ("The grammar as a
+ * trie over tokens": the size of the compiled trie decides whether it fits
+ * the constant-memory budget).  Errors: TC_ERR_INVALID_ARG on a NULL argument.
+ */
 tc_status tc_trie_info(const tc_trie* trie, tc_trie_info_t* out);
 
 /*
@@ -240,7 +245,10 @@ void tc_trie_free(tc_trie* trie);
 /* --------------------------------------------------------------- context */
 
 /*
- * tc_ctx_create - a decoding context on `device` over a tied embedding.
+ * tc_ctx_create - a decoding context on `device` over a tied embedding
+ * ("The sparse output layer": the output head is the tied embedding, one row
+ * per token; "The batched engine": each sequence of a batch keeps its own
+ * small state next to the shared, read-only grammar).
  *
  *  emb_bf16   (device) bf16[vocab, hidden], row-major, 16-byte aligned; the
  *             caller keeps it alive and unchanged while the context is used.
@@ -279,13 +287,16 @@ void tc_ctx_destroy(tc_ctx* ctx);
  */
 tc_status tc_bind_grammar(tc_ctx* ctx, const tc_trie* trie, int32_t residency, void* stream);
 
-/* tc_bound_residency - the residency the bound grammar resolved to (TC_RES_CONST / TC_RES_GLOBAL). */
+/* tc_bound_residency - the residency the bound grammar resolved to (TC_RES_CONST / TC_RES_GLOBAL;
+ * "The grammar as a trie over tokens": constant memory for a small catalog, global memory otherwise). */
 tc_status tc_bound_residency(const tc_ctx* ctx, int32_t* residency);
 
 /*
  * tc_reset - start `batch` sequences, each owing exactly k pointers, at the
- * root of the bound grammar (live counts copied from the static counts,
- * spent flags cleared).  1 <= batch <= max_batch; 1 <= k <= K (a larger k
+ * root of the bound grammar ("Masked sampling inside the sampler": a query
+ * owes exactly k distinct pointers; every pointer starts live, so the live
+ * counts start as the static counts and no spent flag is set).  Also clears
+ * the GEMM heads' timeout flag (TC_ERR_DEVICE_TIMEOUT).  1 <= batch <= max_batch; 1 <= k <= K (a larger k
  * would make the language empty; TC_ERR_K_RANGE).  Asynchronous on `stream`.
  */
 tc_status tc_reset(tc_ctx* ctx, int32_t batch, int32_t k, void* stream);
@@ -405,14 +416,19 @@ void tc_graph_destroy(tc_graph* graph);
 
 /*
  * tc_first_error - synchronise `stream`, then report the lowest sequence
- * index whose status is not TC_OK (*seq = -1, *code = TC_OK if none).
+ * index whose status is not TC_OK (*seq = -1, *code = TC_OK if none)
+ * ("Masked sampling inside the sampler": a step with no legal token stops
+ * the sequence with an error instead of emitting one; this surfaces it).
+ * Errors: TC_ERR_INVALID_ARG, TC_ERR_NOT_BOUND (no reset since binding),
+ * TC_ERR_CUDA.
  */
 tc_status tc_first_error(tc_ctx* ctx, void* stream, int32_t* seq, int32_t* code);
 
 /*
  * tc_read_seq_state - synchronise `stream` and copy per-sequence state of the
  * last reset's batch into host arrays int32[batch] (any may be NULL): current
- * node, pointers completed, tokens emitted, status, done flag.
+ * node, pointers completed, tokens emitted, status, done flag (the walk state
+ * of "Masked sampling inside the sampler").
  */
 tc_status tc_read_seq_state(tc_ctx* ctx, void* stream, int32_t* node, int32_t* emitted,
                             int32_t* len, int32_t* status, int32_t* done);
