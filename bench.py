@@ -671,13 +671,15 @@ def head_rates(tcd, torch, dev, stream, flush, embs, name, heads, n_q, batch=Non
 
 
 def heads_by_batch(tcd, torch, dev, stream, flush):
-    """The constrained decode step at B=64 and B=256 with the sparse head, the
-    union-of-legal-rows tcgen05 GEMM and the full-vocabulary tcgen05 GEMM +
-    mask (the 1000-tool catalog, hidden 4096), and the hex catalog (root
+    """The constrained decode step at B=1 (large_head: sparse and union heads;
+    the dense GEMV is the line's dense_head), at B=64 and B=256 with the sparse
+    head, the union-of-legal-rows tcgen05 GEMM and the full-vocabulary tcgen05
+    GEMM + mask (the 1000-tool catalog, hidden 4096), and the hex catalog (root
     fan-out 267) at B=16, 64 and 256 with the sparse and union heads: where the
     union of legal rows is large and shared, the GEMM reads each row once."""
     embs = {}
     out = {
+        "1": head_rates(tcd, torch, dev, stream, flush, embs, "large_head", ("sparse", "union"), 40),
         "64": head_rates(tcd, torch, dev, stream, flush, embs, "batched", ("sparse", "union", "dense_gemm"), 12),
         "256": head_rates(tcd, torch, dev, stream, flush, embs, "tensor_batch", ("sparse", "union", "dense_gemm"),
                           4),

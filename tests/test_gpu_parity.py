@@ -390,3 +390,22 @@ def test_multi_cta_step_x_in_shared_memory_equals_register_variant(tcd):
         for i in range(4):
             assert np.array_equal(b[i], a[i][q:q + 4]), (q, i)
     ctx.close()
+
+
+def test_hex_catalog_b256_sparse_and_union(tcd):
+    """The hex catalog (root fan-out 267) at B=256, the launch shape the bench
+    reports beside the workload's own B=16: the multi-CTA step with the hidden
+    state in shared memory and one CTA per sequence, and the union GEMM with
+    two 128-sequence M tiles and wide union tiles; every 8th sequence
+    teacher-forced against the oracle, all sequences finished."""
+    w = workload("unstructured")
+    B = 256
+    hid = w.hidden_states(0, B)
+    ctx, _ = make_ctx(tcd, "unstructured", max_batch=B)
+    buf = DecodeBuffers(w.max_steps, B, w.hidden, w.max_steps)
+    buf.load(hid)
+    for head in (tcd.HEAD_SPARSE, tcd.HEAD_UNION_GEMM):
+        out = buf.run(ctx, w.k, head=head)
+        assert np.all(out[3] == 0), head
+        check_against_oracle("unstructured", hid, out, w.k, w.max_steps, exact=False, seqs=range(0, B, 8))
+    ctx.close()

@@ -1113,10 +1113,14 @@ __device__ __noinline__ int block_sample(const StepParams& p, const float* lg, c
 // read by the caller right after the programmatic-dependency wait; the caller
 // does the launch count and the loop control.  Leaves sh.done_after for
 // thread 0.
-template <bool kConst, int NCH, bool kXs>
+// kLean: greedy steps without forced continuations, the common case, in an
+// instantiation that carries neither the sampler nor the forced-span walk
+// (a smaller kernel: the step is bound by latency, instruction fetch included).
+template <bool kConst, int NCH, bool kXs, bool kLean = false>
 __device__ __forceinline__ void step1_body(const StepParams& p, int b, const SeqState& s, const Cand& pre0,
                                            Step1Shared& sh, unsigned char* smem_raw) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool smp = !kLean && p.smp, jump = !kLean && p.jump;
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
   const int mode = seq_mode(p, s);
   const int nch = p.H >> 3;
@@ -1206,7 +1210,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
         const float v = warp_sum(acc);
         if (lane == 0) {
           if (pre) sh.cand[l] = cd;  // the winner's edge data is read from here below
-          if (p.smp) sh.lg[l] = v;
+          if (smp) sh.lg[l] = v;
         }
         if (better(v, cd.a.x, wl, wt)) {
           wl = v;
@@ -1227,7 +1231,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
   if (mode == 1 && warp == 0) {
     float bl = -INFINITY;
     int32_t bt = INT_MAX, bs = -1;
-    if (p.smp) {
+    if (smp) {
       int nan = 0, slot = -1;
       if (!err && n > 0) {
         const float u = p.device_form ? p.u[(size_t)b * p.out_stride + s.len] : p.u[b];
@@ -1293,7 +1297,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
     // Forced continuations follow when that set is a single token, after a
     // separator (the root's set is not precomputed), or when no set was kept
     // (a child wider than a list, counted by the chain itself).
-    const bool chain = p.jump && status == TC_OK && !stop && (next_n == 1 || next_n < 0 || ptr_done >= 0);
+    const bool chain = jump && status == TC_OK && !stop && (next_n == 1 || next_n < 0 || ptr_done >= 0);
     if (!chain && lane < next_n) {
       // The next step's candidates: their list, and their rows started towards
       // L2 (only these rows: prefetching every candidate's child rows while
@@ -1371,7 +1375,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
   }
 }
 
-template <bool kConst, int NCH, bool kXs = false>
+template <bool kConst, int NCH, bool kXs = false, bool kLean = false>
 __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ Step1Shared sh;
@@ -1382,7 +1386,7 @@ __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(con
   const SeqState s = p.st[b];
   const Cand pre0 = p.pre[(size_t)b * kPreMax + (threadIdx.x >> 5)];
   if (p.stats && threadIdx.x == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
-  step1_body<kConst, NCH, kXs>(p, b, s, pre0, sh, smem_raw);
+  step1_body<kConst, NCH, kXs, kLean>(p, b, s, pre0, sh, smem_raw);
   loop_control(p, sh.done_after);
 }
 
@@ -2008,14 +2012,17 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
   cfg.numAttrs = pdl ? 1 : 0;
   if (head == kHeadSparse && p.one_cta) {
     cfg.gridDim = dim3(1, p.B);
+    const bool lean = !p.smp && !p.jump;  // greedy without forced continuations
     if constexpr (NCH >= 8) {
       if (p.wide) {
         cfg.dynamicSmemBytes = (size_t)nch * 16;
-        return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, true>, p);
+        return lean ? cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, true, true>, p)
+                    : cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, true>, p);
       }
     }
     cfg.dynamicSmemBytes = xbytes;
-    return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH>, p);
+    return lean ? cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, false, true>, p)
+                : cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH>, p);
   }
   if (head == kHeadSparse && p.smp) {
     cfg.dynamicSmemBytes = sample_smem_offset(p, tiles) + kSampleSmem;
