@@ -1395,7 +1395,9 @@ __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(con
 // kXs: the hidden state staged in shared memory instead of registers (greedy
 // steps at hidden sizes of 2048 and up), so two CTAs share an SM: for batches
 // whose nodes' fan-out needs more CTAs than one wave of the register variant holds.
-template <bool kConst, int NCH, bool kSmp = false, bool kXs = false>
+// kLean (greedy steps without forced continuations): the narrow nodes' one-CTA
+// body without the sampler or the forced-span walk.
+template <bool kConst, int NCH, bool kSmp = false, bool kXs = false, bool kLean = false>
 __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // A narrow node's step uses the one-CTA step's shared state instead.
@@ -1439,7 +1441,7 @@ __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step_kernel(cons
   if (narrow) {
     Step1Shared& sh1 = *reinterpret_cast<Step1Shared*>(sh_raw);
     if (p.stats && tid == 0 && t == 0 && b == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
-    if (t == 0) step1_body<kConst, NCH, kXs>(p, b, s, pre0, sh1, smem_raw);
+    if (t == 0) step1_body<kConst, NCH, kXs, kLean>(p, b, s, pre0, sh1, smem_raw);
     loop_control(p, sh1.done_after);
     return;
   }
@@ -2028,13 +2030,17 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
     cfg.dynamicSmemBytes = sample_smem_offset(p, tiles) + kSampleSmem;
     return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH, true>, p);
   }
+  const bool lean = !p.jump;  // (sampling took its own kernel above)
   if constexpr (NCH >= 8) {
     if (head == kHeadSparse && p.multi_xs) {
       cfg.dynamicSmemBytes = (size_t)nch * 16 + 2 * (size_t)cap * sizeof(int32_t);
-      return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH, false, true>, p);
+      return lean ? cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH, false, true, true>, p)
+                  : cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH, false, true>, p);
     }
   }
-  if (head == kHeadSparse) return cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH>, p);
+  if (head == kHeadSparse)
+    return lean ? cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH, false, false, true>, p)
+                : cudaLaunchKernelEx(&cfg, sparse_step_kernel<kConst, NCH>, p);
   return cudaLaunchKernelEx(&cfg, dense_step_kernel<kConst, NCH>, p);
 }
 
@@ -2045,8 +2051,14 @@ cudaError_t prepare_one() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH, false, false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
   if constexpr (NCH >= 8) {
     e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(sparse_step_kernel<kConst, NCH, false, true, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
   }
