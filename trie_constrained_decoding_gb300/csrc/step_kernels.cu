@@ -246,9 +246,11 @@ struct SeqLive {
   int32_t nban;
 };
 
+// kRO: the read-only mode is known at compile time (no count arrays to read).
+template <bool kRO = false>
 __device__ __forceinline__ SeqLive seq_live(const StepParams& p, const SeqState& s, int b) {
   SeqLive L;
-  L.cnt = p.iv ? nullptr : p.cnt + (size_t)b * p.g.n_edges;
+  L.cnt = (kRO || p.iv) ? nullptr : p.cnt + (size_t)b * p.g.n_edges;
   L.spent = p.spent + (size_t)b * p.kw;
   L.ban[0] = s.ban0;
   L.ban[1] = s.ban1;
@@ -434,12 +436,12 @@ constexpr int kPreMax = 32;  // largest legal set kept as a precomputed candidat
 
 // Legal candidates of node `node` into out[] (one warp, node fan-out <= 32).
 // Returns the count, or -1 when an index is out of range or the fan-out is larger.
-template <bool kConst>
+template <bool kConst, bool kRO = false>
 __device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<kConst>& w, const SeqState& s,
                                               int b, int beg, int end, int pid, int lane, Cand* out) {
   if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > kPreMax) return -1;
   int bad = pid >= p.g.n_strings;
-  const SeqLive L = seq_live(p, s, b);
+  const SeqLive L = seq_live<kRO>(p, s, b);
   const bool ctl_ok = pid >= 0 && !bad && ptr_free(p, L, pid);
   const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
   const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
@@ -1116,11 +1118,12 @@ __device__ __noinline__ int block_sample(const StepParams& p, const float* lg, c
 // kLean: greedy steps without forced continuations, the common case, in an
 // instantiation that carries neither the sampler nor the forced-span walk
 // (a smaller kernel: the step is bound by latency, instruction fetch included).
-template <bool kConst, int NCH, bool kXs, bool kLean = false>
+// kRO (with kLean): the read-only no-repeat state, known at compile time.
+template <bool kConst, int NCH, bool kXs, bool kLean = false, bool kRO = false>
 __device__ __forceinline__ void step1_body(const StepParams& p, int b, const SeqState& s, const Cand& pre0,
                                            Step1Shared& sh, unsigned char* smem_raw) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool smp = !kLean && p.smp, jump = !kLean && p.jump;
+  const bool smp = !kLean && p.smp, jump = !kLean && p.jump, iv = kRO || p.iv;
   const WalkRd<kConst> w{p.g.img, p.g.off_edges, p.g.off_ptr};
   const int mode = seq_mode(p, s);
   const int nch = p.H >> 3;
@@ -1158,7 +1161,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
         const bool n_ok = nd >= 0 && nd < p.g.n_nodes;
         const int nn = n_ok ? nd : 0;
         const int beg = w.begin(nn), end = w.begin(nn + 1), pid = w.ptr(nn);
-        const int cnt = n_ok ? warp_legal_set<kConst>(p, w, s, b, beg, end, pid, lane, sh.cand) : -1;
+        const int cnt = n_ok ? warp_legal_set<kConst, kRO>(p, w, s, b, beg, end, pid, lane, sh.cand) : -1;
         if (lane == 0) {
           sh.ncand = cnt < 0 ? 0 : cnt;
           sh.err = cnt < 0;
@@ -1191,7 +1194,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
 #pragma unroll
             for (int i = 0; i < NCH; ++i) e[i] = ld_row(r4 + i * 32 + lane);
           }
-          const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
+          const int sn = spec ? warp_legal_set<kConst, kRO>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
           if (lane == 0) sh.spec_n[l] = sn;
           __syncwarp();
           if constexpr (kXs) {
@@ -1202,7 +1205,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
             for (int i = 0; i < NCH; ++i) acc = dot8(e[i], xf.v[i], acc);
           }
         } else {
-          const int sn = spec ? warp_legal_set<kConst>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
+          const int sn = spec ? warp_legal_set<kConst, kRO>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
           if (lane == 0) sh.spec_n[l] = sn;
           __syncwarp();
           for (int c = lane; c < nch; c += 32) acc = dot8(ld_row(r4 + c), xs[c], acc);
@@ -1283,7 +1286,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
         else new_node = win.a.z;
       } else {
         const int32_t pid = pre ? s.pre_pid : sh.pid;
-        if (!ptr_free(p, seq_live(p, s, b), pid)) {
+        if (!ptr_free(p, seq_live<kRO>(p, s, b), pid)) {
           status = TC_ERR_NO_LIVE_EDGE;
         } else {
           ptr_done = pid;
@@ -1305,7 +1308,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
       p.pre[(size_t)b * kPreMax + lane] = sh.spec[bs][lane];
       prefetch_l2(p.emb + (size_t)sh.spec[bs][lane].a.x * p.H, (uint32_t)p.H * 2u);
     }
-    if (ptr_done >= 0 && !p.iv) decrement_path(p, b, ptr_done, lane, 32);
+    if (ptr_done >= 0 && !iv) decrement_path(p, b, ptr_done, lane, 32);
     SeqState ns = s;
     int pre_n = next_n, pre_pid = next_n >= 0 ? win.h.z : -2;  // the child's pointer rank
     if (status != TC_OK) {
@@ -1315,7 +1318,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
       ns.node = new_node;
       ns.len = s.len + 1;
       if (ptr_done >= 0) {
-        if (p.iv) ban_add(ns, ptr_done);
+        if (iv) ban_add(ns, ptr_done);
         else if (lane == 0) p.spent[(size_t)b * p.kw + (ptr_done >> 5)] |= 1u << (ptr_done & 31);
         ns.emitted = s.emitted + 1;
       }
@@ -1375,7 +1378,7 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
   }
 }
 
-template <bool kConst, int NCH, bool kXs = false, bool kLean = false>
+template <bool kConst, int NCH, bool kXs = false, bool kLean = false, bool kRO = false>
 __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ Step1Shared sh;
@@ -1386,7 +1389,7 @@ __global__ void __launch_bounds__(kThreads, kXs ? 2 : 1) sparse_step1_kernel(con
   const SeqState s = p.st[b];
   const Cand pre0 = p.pre[(size_t)b * kPreMax + (threadIdx.x >> 5)];
   if (p.stats && threadIdx.x == 0 && blockIdx.y == 0) atomicAdd(&p.stats[kStatStepLaunches], 1ull);
-  step1_body<kConst, NCH, kXs, kLean>(p, b, s, pre0, sh, smem_raw);
+  step1_body<kConst, NCH, kXs, kLean, kRO>(p, b, s, pre0, sh, smem_raw);
   loop_control(p, sh.done_after);
 }
 
@@ -2018,11 +2021,13 @@ cudaError_t launch_one(const StepParams& p, int head, int tiles, bool pdl, cudaS
     if constexpr (NCH >= 8) {
       if (p.wide) {
         cfg.dynamicSmemBytes = (size_t)nch * 16;
+        if (lean && p.iv) return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, true, true, true>, p);
         return lean ? cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, true, true>, p)
                     : cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, true>, p);
       }
     }
     cfg.dynamicSmemBytes = xbytes;
+    if (lean && p.iv) return cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, false, true, true>, p);
     return lean ? cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH, false, true>, p)
                 : cudaLaunchKernelEx(&cfg, sparse_step1_kernel<kConst, NCH>, p);
   }
