@@ -70,6 +70,8 @@ def parse_args():
                     help="per-sequence live-count arrays instead of the read-only no-repeat state")
     ap.add_argument("--jump", action="store_true",
                     help="forced continuations: emit grammar-forced tokens without the head (sparse/dense heads)")
+    ap.add_argument("--root-gemm", action="store_true",
+                    help="sparse head with the first (root) step on the tcgen05 GEMM (TC_FLAG_ROOT_GEMM)")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per query batch (default: the workload's)")
     return ap.parse_args()
@@ -407,6 +409,8 @@ def run_ours(args):
             "dense_gemm": tcd.HEAD_DENSE_GEMM}[args.head]
     if args.jump:
         head |= tcd.FLAG_JUMP_FORWARD
+    if args.root_gemm:
+        head |= tcd.FLAG_ROOT_GEMM
     B, S, H = w.batch, w.max_steps, w.hidden
 
     emb_bits = w.embedding()
@@ -501,7 +505,7 @@ def run_ours(args):
     # algorithmic bytes of those steps (candidate rows + hidden states; the
     # union head: union rows + hidden states; dense heads: every row).
     hb = 2.0 * H
-    base_head = head & ~(tcd.FLAG_JUMP_FORWARD | tcd.FLAG_FORCED_LOGITS)
+    base_head = head & ~(tcd.FLAG_JUMP_FORWARD | tcd.FLAG_FORCED_LOGITS | tcd.FLAG_ROOT_GEMM)
     if base_head == tcd.HEAD_SPARSE:
         algo = (st["cand_rows"] + st["seq_steps"]) * hb
     elif base_head == tcd.HEAD_UNION_GEMM:
@@ -562,7 +566,8 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": B, "k": w.k, "vocab": w.vocab, "hidden": H,
                    "catalog_strings": len(w.catalog), "trie_nodes": tinfo["n_nodes"], "trie_edges": tinfo["n_edges"],
                    "max_fanout": tinfo["max_fanout"], "residency": ["auto", "const", "global"][ctx.residency()],
-                   "head": args.head, "jump_forward": bool(args.jump), "no_repeat_state": state_mode,
+                   "head": args.head + (" (root step on the tcgen05 GEMM)" if args.root_gemm else ""),
+                   "jump_forward": bool(args.jump), "no_repeat_state": state_mode,
                    "bench_step": "one tc_decode graph launch decoding one query batch to the end",
                    "decode_steps_per_bench_step": all_steps / (K * world),
                    "step_launches_per_bench_step": st["step_launches"] / K,
@@ -621,7 +626,8 @@ def head_rates(tcd, torch, dev, stream, flush, embs, name, heads, n_q, batch=Non
     status = torch.empty(B, dtype=torch.int32, device=f"cuda:{dev}")
     out = {"workload": name, "batch": B, "k": w.k, "query_batches": n_q}
     for hname in heads:
-        head = {"sparse": tcd.HEAD_SPARSE, "union": tcd.HEAD_UNION_GEMM, "dense_gemm": tcd.HEAD_DENSE_GEMM}[hname]
+        head = {"sparse": tcd.HEAD_SPARSE, "union": tcd.HEAD_UNION_GEMM, "dense_gemm": tcd.HEAD_DENSE_GEMM,
+                "sparse_root_gemm": tcd.HEAD_SPARSE | tcd.FLAG_ROOT_GEMM}[hname]
         steps = {}
         for q in qids:        # untimed: the decode steps of each query batch under this head
             buf.copy_(hid[q])
@@ -650,7 +656,9 @@ def head_rates(tcd, torch, dev, stream, flush, embs, name, heads, n_q, batch=Non
         n_steps = sum(steps[q][0] for q in qids)
         n_tok = sum(steps[q][1] for q in qids)
         hid_bytes = st["seq_steps"] * 2.0 * H
-        if hname == "sparse":
+        if hname in ("sparse", "sparse_root_gemm"):
+            # (with the root step on the GEMM each root row is read once per step, not
+            # once per sequence: these bytes count it per sequence, as the sparse head reads it)
             algo = st["cand_rows"] * 2.0 * H + hid_bytes
         elif hname == "union":
             algo = st["union_rows"] * 2.0 * H + hid_bytes
@@ -676,18 +684,20 @@ def heads_by_batch(tcd, torch, dev, stream, flush):
     head, the union-of-legal-rows tcgen05 GEMM and the full-vocabulary tcgen05
     GEMM + mask (the 1000-tool catalog, hidden 4096), and the hex catalog (root
     fan-out 267) at B=16, 64 and 256 with the sparse and union heads: where the
-    union of legal rows is large and shared, the GEMM reads each row once."""
+    union of legal rows is large and shared, the GEMM reads each row once.
+    `sparse_root_gemm`: the sparse head with the first (root) step on the
+    tcgen05 GEMM (TC_FLAG_ROOT_GEMM), on the hex catalog and at B=256."""
     embs = {}
     out = {
         "1": head_rates(tcd, torch, dev, stream, flush, embs, "large_head", ("sparse", "union"), 40),
         "64": head_rates(tcd, torch, dev, stream, flush, embs, "batched", ("sparse", "union", "dense_gemm"), 12),
-        "256": head_rates(tcd, torch, dev, stream, flush, embs, "tensor_batch", ("sparse", "union", "dense_gemm"),
-                          4),
+        "256": head_rates(tcd, torch, dev, stream, flush, embs, "tensor_batch",
+                          ("sparse", "union", "dense_gemm", "sparse_root_gemm"), 4),
     }
     hexes = {}
     for B, n_q in ((16, 8), (64, 4), (256, 2)):
-        hexes[str(B)] = head_rates(tcd, torch, dev, stream, flush, embs, "unstructured", ("sparse", "union"), n_q,
-                                   batch=B)
+        hexes[str(B)] = head_rates(tcd, torch, dev, stream, flush, embs, "unstructured",
+                                   ("sparse", "union", "sparse_root_gemm"), n_q, batch=B)
     out["hex_catalog"] = hexes
     del embs
     return out
@@ -701,7 +711,7 @@ def extra_passes(args, w, ctx, tcd, torch, stream, dev, dev_hidden, hh, qids, he
     out = {}
     n_roof = min(len(qids), 200 if B == 1 else 8)
     flags = head & tcd.FLAG_JUMP_FORWARD
-    head = head & ~tcd.FLAG_JUMP_FORWARD        # the per-launch and host-loop passes run plain steps
+    head = head & ~(tcd.FLAG_JUMP_FORWARD | tcd.FLAG_ROOT_GEMM)  # the per-launch and host-loop passes run plain steps
 
     # --- step kernel alone: tc_step (same kernel body, host-argument form), one
     # event pair per launch; L2 flushed before every launch (cold) or not (warm).

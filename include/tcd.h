@@ -122,6 +122,28 @@ enum {
  */
 #define TC_FLAG_FORCED_LOGITS 0x200
 
+/*
+ * Flag or-ed into the `head` argument of tc_decode, tc_decode_graph_create
+ * and tc_decode_host together with TC_HEAD_SPARSE: the first step runs on the
+ * tcgen05 GEMM ("Constraint made cheaper than no constraint", section "The
+ * sparse output layer": in batched form the rows of the legal set are one
+ * GEMM).  At that step every sequence is at the root with nothing emitted, so
+ * its legal set is the root's token edges, the same for all sequences: one
+ * [batch x hidden] x [hidden x root edges] product with each sequence's argmax
+ * over all columns (ties to the lower token id), then the transition; later
+ * steps use the sparse head.  The first step's logits are fp32 sums of the
+ * same bf16 products in the tensor cores' order and K split, so they equal the
+ * sparse head's on integer-valued inputs and differ by rounding otherwise (a
+ * token may then differ only where two logits are within rounding).  It pays
+ * off where the root is wide and the batch large (e.g. a catalog of
+ * unstructured strings at 256 sequences) and costs time at small batches.
+ * Needs batch <= 256, hidden % 64 == 0 and a root whose edges all lead to
+ * pointers (no empty catalog string); TC_ERR_UNSUPPORTED with
+ * TC_FLAG_JUMP_FORWARD, sampling or another head.  The device checks that each
+ * sequence is at the root with nothing emitted (TC_ERR_BOUNDS otherwise).
+ */
+#define TC_FLAG_ROOT_GEMM 0x400
+
 /* Bytes of __constant__ memory reserved for the header part of one walk image. */
 #define TC_CONST_CAPACITY_BYTES (63 * 1024)
 

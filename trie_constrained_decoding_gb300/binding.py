@@ -31,6 +31,7 @@ BIND_LIVE_COUNTS = 0x10        # or-ed into bind's residency: per-sequence live-
 HEAD_SPARSE, HEAD_DENSE, HEAD_UNION_GEMM, HEAD_DENSE_GEMM = 0, 1, 2, 3
 FLAG_JUMP_FORWARD = 0x100      # or-ed into `head` of decode / decode_graph: forced tokens skip the head
 FLAG_FORCED_LOGITS = 0x200     # with FLAG_JUMP_FORWARD: forced tokens still get their logits
+FLAG_ROOT_GEMM = 0x400         # with HEAD_SPARSE in decodes: the first (root) step on the tcgen05 GEMM
 STAT_SLOTS = 6
 TC_ERR_EMPTY_MASK, TC_ERR_NO_LIVE_EDGE, TC_ERR_MAX_STEPS, TC_ERR_BOUNDS = 16, 17, 18, 19
 TC_ERR_DEVICE_TIMEOUT = 20

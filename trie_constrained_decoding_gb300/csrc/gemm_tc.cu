@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     hdr->row0 = p.row0_ptr ? *p.row0_ptr : 0;
     hdr->n_cols = p.n_cols_ptr ? *p.n_cols_ptr : p.n_cols_fixed;
   }
-  for (int r = tid; r < 256; r += C::kThreads) hdr->active[r] = (r < p.B && p.xrow[r] >= 0) ? 1 : 0;
+  for (int r = tid; r < 256; r += C::kThreads) hdr->active[r] = (r < p.B && (!p.xrow || p.xrow[r] >= 0)) ? 1 : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -421,7 +421,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       int cpos = 0;
       if (p.tile_cands) {
         if (has) {
-          const int4* r = reinterpret_cast<const int4*>(p.tile_cands + (size_t)b * p.max_tiles + tile);
+          const int4* r =
+              reinterpret_cast<const int4*>(p.tile_cands + (p.uniform ? 0 : (size_t)b * p.max_tiles) + tile);
           const int4 bits = __ldg(r);
           cpos = __ldg(reinterpret_cast<const int*>(r + 1));
           cb[0] = (uint32_t)bits.x;

@@ -22,7 +22,7 @@ struct alignas(16) TileCands {
 };
 
 struct GemmParams {
-  const int64_t* xrow;       // [B] >= 0 for sequences that take this step, -1 otherwise
+  const int64_t* xrow;       // [B] >= 0 for sequences that take this step, -1 otherwise; null: all B take it
   const int32_t* row0_ptr;   // device: first activation row of the step in the activation map (null: 0)
   int32_t B;                 // sequences, <= 256
   int32_t H;                 // multiple of 64
@@ -32,6 +32,7 @@ struct GemmParams {
   const int32_t* cand_col;   // [B, C] ascending columns of each sequence's legal candidates
   const int32_t* ncand;      // [B]
   const TileCands* tile_cands;  // [B, max_tiles] per-tile candidate records, or null (search cand_col)
+  int32_t uniform;           // 1: every sequence has the same candidates: tile_cands holds one record per tile
   int32_t C;
   GemmPartial* part;         // [B, max_tiles] (ksplit == 1)
   int32_t max_tiles;

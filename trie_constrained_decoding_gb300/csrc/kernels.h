@@ -106,6 +106,13 @@ struct HeadScratch {
   long long wait_limit;     // polls of one GEMM wait before it gives up (0: the default)
   int32_t withhold;         // test switch of the GEMM (see GemmParams::withhold)
   int32_t* row0;            // [1] first activation row of the current step
+  // Root step (the first step of a decode, every sequence at the root with
+  // nothing completed): its candidates are the root's token edges, the same
+  // for every sequence, so no filter or union compaction runs.
+  int32_t root_mode;        // 1: this GEMM step is the root step
+  int32_t n_root;           // the root's token edges
+  const int32_t* root_tok;  // [n_root] their tokens, ascending (the GEMM's columns)
+  const int32_t* root_edge; // [n_root] their edge indices
   const EmbMaps* emb_maps;  // host: tensor maps of the embedding
 };
 
@@ -205,6 +212,8 @@ cudaError_t launch_finalize(const StepParams& p, cudaStream_t s);
 // One step of a GEMM head: candidate filter, [union compaction], tcgen05 GEMM
 // with masked-argmax epilogue, per-sequence fold and transition.
 cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head, int gemm_ctas, cudaStream_t s);
+cudaError_t launch_root_step(const StepParams& p, bool const_resident, const TileCands* root_tiles, int gemm_ctas,
+                             cudaStream_t s);
 // Copy a walk image (device memory) into the constant bank, stream-ordered.
 cudaError_t const_upload(const void* d_src, size_t bytes, cudaStream_t s);
 

@@ -85,6 +85,12 @@ struct DevGrammar {
   int32_t* d_cnt = nullptr;
   uint32_t* d_spent = nullptr;
   Cand* d_pre = nullptr;  // [max_batch, 32] next-step candidate lists
+  // Root step (TC_FLAG_ROOT_GEMM): the root's token edges as GEMM columns:
+  // tokens [n_root], edge indices [n_root], then one TileCands record per 128
+  // columns at word root_tiles_off (16-byte aligned).
+  int32_t* d_root = nullptr;
+  int32_t n_root = 0;  // 0: the root step does not apply (the root has a control edge or an edge without pointers)
+  int32_t root_tiles_off = 0;
   int32_t root_beg = 0, root_end = 0, root_pid = -1;
   int32_t kw = 1;
   int32_t batch = 0, k = 0;  // of the last reset (0: none)
@@ -118,6 +124,7 @@ struct DevGrammar {
     cudaFree(d_cnt);
     cudaFree(d_spent);
     cudaFree(d_pre);
+    cudaFree(d_root);
   }
 };
 
@@ -281,6 +288,20 @@ cudaError_t launch_any_step(tc_ctx* c, DevGrammar* g, const StepParams& p, int h
   return launch_step(q, cst, head, tiles, s, pdl);
 }
 
+// The root step of TC_FLAG_ROOT_GEMM: every sequence at the root (the first
+// step after a reset), its candidates the root's token edges, on the tcgen05
+// GEMM.  p is the step's parameters as for the sparse head.
+cudaError_t launch_root(tc_ctx* c, DevGrammar* g, const StepParams& p, cudaStream_t s) {
+  StepParams q = p;
+  q.hs = c->hs;
+  q.hs.n_root = g->n_root;
+  q.hs.root_tok = g->d_root;
+  q.hs.root_edge = g->d_root + g->n_root;
+  const TileCands* tiles = reinterpret_cast<const TileCands*>(g->d_root + g->root_tiles_off);
+  const int tasks = (g->n_root + gemm_tile_cols() - 1) / gemm_tile_cols() * c->hs.ksplit * (p.B > 128 ? 2 : 1);
+  return launch_root_step(q, g->residency == TC_RES_CONST, tiles, std::min(c->num_sms, tasks), s);
+}
+
 StepParams step_params(const tc_ctx* c, const DevGrammar* g, int B) {
   StepParams p{};
   p.g = g->view();
@@ -375,6 +396,18 @@ tc_status check_decode_args(tc_ctx* c, const void* hidden, int32_t n_steps, int3
   if (batch < 1 || batch > c->max_batch) return TC_ERR_CAPACITY;
   if (k < 1 || k > c->bound->n_strings) return TC_ERR_K_RANGE;
   if (max_steps < 1 || max_steps > n_steps) return TC_ERR_INVALID_ARG;
+  if (head & TC_FLAG_ROOT_GEMM) {
+    head &= ~TC_FLAG_ROOT_GEMM;
+    if (head != TC_HEAD_SPARSE) {
+      set_error_message("TC_FLAG_ROOT_GEMM: the sparse head without forced continuations only");
+      return TC_ERR_UNSUPPORTED;
+    }
+    if (c->bound->n_root == 0) {
+      set_error_message("TC_FLAG_ROOT_GEMM: the grammar's root has a control edge or an edge without pointers");
+      return TC_ERR_UNSUPPORTED;
+    }
+    return check_head(c, TC_HEAD_UNION_GEMM, batch);  // the GEMM's limits and scratch
+  }
   if ((head & TC_FLAG_FORCED_LOGITS) && !(head & TC_FLAG_JUMP_FORWARD)) {
     set_error_message("TC_FLAG_FORCED_LOGITS needs TC_FLAG_JUMP_FORWARD");
     return TC_ERR_INVALID_ARG;
@@ -412,7 +445,7 @@ tc_status check_sampling(tc_ctx* c, const DevGrammar* g, int head, const tc_samp
     return TC_ERR_INVALID_ARG;
   }
   if ((head & ~(TC_FLAG_JUMP_FORWARD | TC_FLAG_FORCED_LOGITS)) != TC_HEAD_SPARSE || !g) {
-    set_error_message("sampling: sparse head only");
+    set_error_message("sampling: sparse head only (without TC_FLAG_ROOT_GEMM)");
     return TC_ERR_UNSUPPORTED;
   }
   if (!one_cta_sparse(g) && !c->d_smp_lg) {
@@ -489,6 +522,27 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
   r.status_out = static_cast<int32_t*>(key.status);
   r.cond = (unsigned long long)cond;
   if ((e = launch_reset(r, cs)) != cudaSuccess) return fail(e, "reset kernel capture");
+  StepParams p = step_params(c, g, key.batch);
+  p.hidden = static_cast<const uint16_t*>(key.hidden);
+  p.hidden_rows = (int64_t)key.n_steps * key.batch;
+  p.tok_out = static_cast<int32_t*>(key.toks);
+  p.logit_out = static_cast<float*>(key.logits);
+  p.status_out = static_cast<int32_t*>(key.status);
+  p.lens_out = static_cast<int32_t*>(key.lens);
+  p.out_stride = key.max_steps;
+  p.max_steps = key.max_steps;
+  p.cond = (unsigned long long)cond;
+  p.device_form = 1;
+  p.jump = (key.head & TC_FLAG_JUMP_FORWARD) ? 1 : 0;
+  p.forced_logits = (key.head & TC_FLAG_FORCED_LOGITS) ? 1 : 0;
+  p.iv = r.iv;
+  apply_sampling(p, key.smp);
+  if (key.head & TC_FLAG_ROOT_GEMM) {
+    // The first step, every sequence at the root, on the tensor cores; the
+    // loop then continues with the sparse head.
+    p.loop_ctrl = 0;
+    if ((e = launch_root(c, g, p, cs)) != cudaSuccess) return fail(e, "root step capture");
+  }
   cudaStreamCaptureStatus cst;
   cudaGraph_t cap_graph = nullptr;
   const cudaGraphNode_t* deps = nullptr;
@@ -514,22 +568,7 @@ tc_status build_graph(tc_ctx* c, DevGrammar* g, const GraphKey& key, tc_graph** 
   if ((e = cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal)) !=
       cudaSuccess)
     return fail(e, "cudaStreamBeginCaptureToGraph(body)");
-  StepParams p = step_params(c, g, key.batch);
-  p.hidden = static_cast<const uint16_t*>(key.hidden);
-  p.hidden_rows = (int64_t)key.n_steps * key.batch;
-  p.tok_out = static_cast<int32_t*>(key.toks);
-  p.logit_out = static_cast<float*>(key.logits);
-  p.status_out = static_cast<int32_t*>(key.status);
-  p.lens_out = static_cast<int32_t*>(key.lens);
-  p.out_stride = key.max_steps;
-  p.max_steps = key.max_steps;
-  p.cond = (unsigned long long)cond;
-  p.device_form = 1;
-  p.jump = (key.head & TC_FLAG_JUMP_FORWARD) ? 1 : 0;
-  p.forced_logits = (key.head & TC_FLAG_FORCED_LOGITS) ? 1 : 0;
-  p.iv = r.iv;
-  apply_sampling(p, key.smp);
-  const int head = key.head & ~(TC_FLAG_JUMP_FORWARD | TC_FLAG_FORCED_LOGITS);
+  const int head = key.head & ~(TC_FLAG_JUMP_FORWARD | TC_FLAG_FORCED_LOGITS | TC_FLAG_ROOT_GEMM);
   // The body runs kLoopUnroll steps; only the last sets the loop condition.
   // A sequence that has stopped makes the remaining steps of the body no-ops.
   for (int u = 0; u < kLoopUnroll; ++u) {
@@ -698,6 +737,32 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
       }
       path_off[(size_t)t->n_strings] = (int32_t)path.size();
     }
+    // The root step's columns: the root's token edges in CSR order (ascending
+    // tokens).  At the first step of a decode each is legal for every
+    // sequence: the root is not a terminal (empty strings are refused) and a
+    // token edge has a pointer below it.
+    std::vector<int32_t> root_img;
+    {
+      const int32_t rb = t->node_begin[0], re = t->node_begin[1];
+      bool ok = re > rb;
+      for (int32_t e = rb; ok && e < re; ++e) ok = t->edge_child[e] >= 0 && t->static_cnt[e] > 0;
+      if (ok) {
+        const int32_t R = re - rb, cols = gemm_tile_cols(), tiles = (R + cols - 1) / cols;
+        const int32_t toff = (2 * R + 3) / 4 * 4;
+        root_img.assign((size_t)toff + 8 * (size_t)tiles, 0);
+        for (int32_t i = 0; i < R; ++i) {
+          root_img[(size_t)i] = t->edge_tok[rb + i];
+          root_img[(size_t)R + i] = rb + i;
+        }
+        for (int32_t col = 0; col < R; ++col) {
+          const int32_t j = col % cols;
+          root_img[(size_t)toff + 8 * (col / cols) + (j >> 5)] |= (int32_t)(1u << (j & 31));
+        }
+        for (int32_t tl = 0; tl < tiles; ++tl) root_img[(size_t)toff + 8 * tl + 4] = cols * tl;  // first index
+        g->n_root = R;
+        g->root_tiles_off = toff;
+      }
+    }
     const size_t B = (size_t)c->max_batch;
     cudaError_t e = cudaMalloc(&g->d_img, img_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&g->d_static_cnt, sizeof(int32_t) * std::max<size_t>(1, t->static_cnt.size()));
@@ -715,6 +780,9 @@ extern "C" tc_status tc_bind_grammar(tc_ctx* c, const tc_trie* t, int32_t reside
     if (e == cudaSuccess)
       e = cudaMemcpy(g->d_path, path.data(), sizeof(int32_t) * path.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(g->d_st, 0, sizeof(SeqState) * B);
+    if (e == cudaSuccess && !root_img.empty()) e = cudaMalloc(&g->d_root, root_img.size() * sizeof(int32_t));
+    if (e == cudaSuccess && !root_img.empty())
+      e = cudaMemcpy(g->d_root, root_img.data(), root_img.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
       g->release();
       delete g;
@@ -928,6 +996,8 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
   g->k = k;
   g->iv = r.iv;
   const size_t row = (size_t)batch * (size_t)c->H;
+  const bool root_gemm = (head & TC_FLAG_ROOT_GEMM) != 0;
+  head &= ~TC_FLAG_ROOT_GEMM;
   for (int32_t t = 0; t < max_steps; ++t) {
     StepParams p = step_params(c, g, batch);
     p.hidden = static_cast<const uint16_t*>(hidden) + (size_t)t * row;
@@ -938,7 +1008,8 @@ extern "C" tc_status tc_decode_host(tc_ctx* c, const void* hidden, int32_t n_ste
     p.lens_out = lens;
     p.out_stride = max_steps;
     p.max_steps = max_steps;
-    TC_CUDA(launch_any_step(c, g, p, head, s, false));
+    if (root_gemm && t == 0) TC_CUDA(launch_root(c, g, p, s));
+    else TC_CUDA(launch_any_step(c, g, p, head, s, false));
     TC_CUDA(cudaMemcpyAsync(c->h_live, &c->d_ctrl->live, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
     TC_CUDA(cudaStreamSynchronize(s));
     if (*c->h_live <= 0) break;

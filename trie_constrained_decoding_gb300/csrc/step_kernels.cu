@@ -1837,10 +1837,17 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
   const HeadScratch& hs = p.hs;
   // The step's scalars are read together with the state (one round trip).
   const SeqState s = p.st[b];
-  const int n = hs.ncand[b];
-  // A GEMM wait that timed out fails the step of every sequence.
-  const int err = *hs.gemm_err ? TC_ERR_DEVICE_TIMEOUT : hs.errf[b];
-  const int n_cols = hs.union_mode ? *hs.n_union : p.V;
+  const bool root = hs.root_mode != 0;
+  const int n = root ? hs.n_root : hs.ncand[b];
+  // A GEMM wait that timed out fails the step of every sequence.  The root
+  // step's candidates hold only for a sequence that is at the root with
+  // nothing emitted (the first step after a reset).
+  const int err = *hs.gemm_err ? TC_ERR_DEVICE_TIMEOUT
+                  : root        ? ((s.node != 0 || s.len != 0 || s.emitted != 0) ? 1 : 0)
+                                : hs.errf[b];
+  const int n_cols = root ? n : hs.union_mode ? *hs.n_union : p.V;
+  const int32_t* c_tok = root ? hs.root_tok : hs.cand_tok + (size_t)b * p.cand_cap;
+  const int32_t* c_edge = root ? hs.root_edge : hs.cand_edge + (size_t)b * p.cand_cap;
   const int mode = seq_mode(p, s);
   float wl = -INFINITY;
   int32_t wt = INT_MAX, we = -1;
@@ -1848,7 +1855,7 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
     const int n_tiles = (n_cols + gemm_tile_cols_dev - 1) / gemm_tile_cols_dev;
     int32_t bc = INT_MAX;  // winning column (tile partials)
     int32_t bi = INT_MAX;  // winning candidate index (split sums)
-    const bool split = hs.union_mode && hs.ksplit > 1;
+    const bool split = (hs.union_mode || root) && hs.ksplit > 1;
     if (!err && n > 0 && split) {
       // Split-K: each candidate's logit is the sum of its per-split partial
       // sums, added in split order (a fixed order, independent of the batch).
@@ -1894,20 +1901,25 @@ __global__ void __launch_bounds__(kThreads) gemm_finish_kernel(const StepParams 
     }
     if (split) {
       if (key != INT_MAX) {
-        wt = hs.cand_tok[(size_t)b * p.cand_cap + key];
-        we = hs.cand_edge[(size_t)b * p.cand_cap + key];
+        wt = c_tok[key];
+        we = c_edge[key];
       }
     } else if ((bc = key) != INT_MAX) {
       // columns ascend with tokens, so the column order breaks ties like the token order
-      const int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
-      int lo = 0, hi = n;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (cc[mid] < bc) lo = mid + 1; else hi = mid;
+      int lo = bc;  // (root step: the column is the candidate's index)
+      if (!root) {
+        const int32_t* cc = hs.cand_col + (size_t)b * p.cand_cap;
+        int hi = n;
+        lo = 0;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (cc[mid] < bc) lo = mid + 1; else hi = mid;
+        }
+        if (!(lo < n && cc[lo] == bc)) lo = -1;
       }
-      if (lo < n && cc[lo] == bc) {
-        wt = hs.cand_tok[(size_t)b * p.cand_cap + lo];
-        we = hs.cand_edge[(size_t)b * p.cand_cap + lo];
+      if (lo >= 0 && lo < n) {
+        wt = c_tok[lo];
+        we = c_edge[lo];
       } else {
         wl = -INFINITY;  // cannot happen: the column came from this sequence's list
       }
@@ -2121,9 +2133,44 @@ cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t sm
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The root step: the GEMM over the root's token rows (the same candidates for
+// every sequence: one uniform record per column tile), then the fold and
+// transition.  p.hs carries the root arrays; `root_tiles` holds the records.
+cudaError_t launch_root_step(const StepParams& p, bool const_resident, const TileCands* root_tiles, int gemm_ctas,
+                             cudaStream_t s) {
+  StepParams q = p;
+  q.hs.root_mode = 1;
+  q.hs.union_mode = 0;
+  GemmParams gp{};
+  gp.xrow = nullptr;     // every sequence takes the root step
+  gp.row0_ptr = nullptr; // the step's hidden states are the activation map's first rows
+  gp.B = p.B;
+  gp.H = p.H;
+  gp.row_list = p.hs.root_tok;
+  gp.n_cols_ptr = nullptr;
+  gp.n_cols_fixed = p.hs.n_root;
+  gp.cand_col = nullptr;
+  gp.ncand = nullptr;
+  gp.tile_cands = root_tiles;
+  gp.uniform = 1;
+  gp.C = p.cand_cap;
+  gp.part = p.hs.part;
+  gp.max_tiles = p.hs.max_tiles;
+  gp.ksplit = p.hs.ksplit;
+  gp.split_part = p.hs.split_part;
+  gp.err = p.hs.gemm_err;
+  gp.wait_limit = p.hs.wait_limit;
+  gp.withhold = p.hs.withhold;
+  cudaError_t e = launch_union_gemm(gp, p.hidden, p.hidden_rows, *p.hs.emb_maps, gemm_ctas, s);
+  if (e != cudaSuccess) return e;
+  return const_resident ? launch_pdl(gemm_finish_kernel<true>, dim3(1, p.B), dim3(kThreads), 0, s, q)
+                        : launch_pdl(gemm_finish_kernel<false>, dim3(1, p.B), dim3(kThreads), 0, s, q);
+}
+
 cudaError_t launch_gemm_step(const StepParams& p, bool const_resident, int head, int gemm_ctas, cudaStream_t s) {
   StepParams q = p;
   q.hs.union_mode = head == kHeadUnionGemm;
+  q.hs.root_mode = 0;
   const size_t fsmem = 2 * (size_t)p.cand_cap * sizeof(int32_t);
   StepParams no_ctrl = q;
   no_ctrl.loop_ctrl = 0;
