@@ -686,18 +686,20 @@ def heads_by_batch(tcd, torch, dev, stream, flush):
     fan-out 267) at B=16, 64 and 256 with the sparse and union heads: where the
     union of legal rows is large and shared, the GEMM reads each row once.
     `sparse_root_gemm`: the sparse head with the first (root) step on the
-    tcgen05 GEMM (TC_FLAG_ROOT_GEMM), on the hex catalog and at B=256."""
+    tcgen05 GEMM (TC_FLAG_ROOT_GEMM), on the hex catalog and at B=256, timed
+    right after the sparse head (the power-capped dense GEMM slows what
+    follows it)."""
     embs = {}
     out = {
         "1": head_rates(tcd, torch, dev, stream, flush, embs, "large_head", ("sparse", "union"), 40),
         "64": head_rates(tcd, torch, dev, stream, flush, embs, "batched", ("sparse", "union", "dense_gemm"), 12),
         "256": head_rates(tcd, torch, dev, stream, flush, embs, "tensor_batch",
-                          ("sparse", "union", "dense_gemm", "sparse_root_gemm"), 4),
+                          ("sparse", "sparse_root_gemm", "union", "dense_gemm"), 4),
     }
     hexes = {}
     for B, n_q in ((16, 8), (64, 4), (256, 2)):
         hexes[str(B)] = head_rates(tcd, torch, dev, stream, flush, embs, "unstructured",
-                                   ("sparse", "union", "sparse_root_gemm"), n_q, batch=B)
+                                   ("sparse", "sparse_root_gemm", "union"), n_q, batch=B)
     out["hex_catalog"] = hexes
     del embs
     return out
