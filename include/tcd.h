@@ -124,7 +124,8 @@ enum {
 
 /*
  * Flag or-ed into the `head` argument of tc_decode, tc_decode_graph_create
- * and tc_decode_host together with TC_HEAD_SPARSE: the first step runs on the
+ * and tc_decode_host together with TC_HEAD_SPARSE (and of tc_step, for the
+ * first step after tc_reset): the first step runs on the
  * tcgen05 GEMM ("Constraint made cheaper than no constraint", section "The
  * sparse output layer": in batched form the rows of the legal set are one
  * GEMM).  At that step every sequence is at the root with nothing emitted, so
@@ -340,7 +341,10 @@ tc_status tc_reset(tc_ctx* ctx, int32_t batch, int32_t k, void* stream);
  * The head may change from one call to the next, also inside a captured
  * graph: the sparse step keeps each sequence's next candidate list in its
  * device state, and every other head's step clears it there, so the next
- * sparse step filters that node itself.
+ * sparse step filters that node itself.  TC_HEAD_SPARSE | TC_FLAG_ROOT_GEMM
+ * runs the first step after tc_reset as the tensor-core root step (see the
+ * flag); a sequence that is not at the root with nothing emitted fails that
+ * step with TC_ERR_BOUNDS.
  *
  * Asynchronous on `stream`; a sequence that meets an error stops there.
  */

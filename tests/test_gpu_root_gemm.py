@@ -9,7 +9,7 @@ those values are exact) and within the oracle's tolerance on Gaussian ones."""
 import numpy as np
 import pytest
 
-from gpu_common import DecodeBuffers, check_against_oracle, make_ctx, torch_mod, workload
+from gpu_common import DecodeBuffers, check_against_oracle, make_ctx, to_dev_bf16, torch_mod, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -123,4 +123,59 @@ def test_root_gemm_rejections(tcd):
     # the context still decodes
     out = buf.run(ctx, w.k, head=tcd.HEAD_SPARSE | tcd.FLAG_ROOT_GEMM)
     assert np.all(out[3] == 0)
+    ctx.close()
+
+
+def test_tensor_batch_root_gemm_b256(tcd):
+    """The 1000-tool catalog at B=256 (the bench's tensor_batch launch shape):
+    every 8th sequence teacher-forced against the oracle, all finished."""
+    w = workload("tensor_batch")
+    hid, out = _run(tcd, "tensor_batch", tcd.HEAD_SPARSE | tcd.FLAG_ROOT_GEMM)
+    assert np.all(out[3] == 0)
+    check_against_oracle("tensor_batch", hid, out, w.k, w.max_steps, exact=False, seqs=range(0, w.batch, 8))
+
+
+def test_host_steps_with_root_gemm_equal_decode(tcd):
+    """tc_step with the flag on the first step after a reset, then sparse
+    steps, gives the decode with the flag (integer inputs: and the all-sparse
+    steps), bit for bit; the flag on a later step fails every live sequence
+    with TC_ERR_BOUNDS (the device finds them away from a fresh root)."""
+    torch = torch_mod()
+    w = workload("tiny")
+    B = 16
+    hid_bits = w.hidden_states(0, B)
+    S = hid_bits.shape[0]
+    hid = to_dev_bf16(hid_bits)
+    ctx, _ = make_ctx(tcd, "tiny", max_batch=B)
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    lg = torch.empty(B, dtype=torch.float32, device="cuda")
+    st = torch.empty(B, dtype=torch.int32, device="cuda")
+
+    def run(first_head):
+        ctx.reset(B, w.k)
+        toks, lgs = np.full((B, S), -1, np.int32), np.zeros((B, S), np.float32)
+        for t in range(S):
+            ctx.step(hid[t], tok, lg, st, head=first_head if t == 0 else tcd.HEAD_SPARSE)
+            torch.cuda.synchronize()
+            toks[:, t], lgs[:, t] = tok.cpu().numpy(), lg.cpu().numpy()
+        return toks, lgs, st.cpu().numpy().copy()
+
+    rt, rl, rs = run(tcd.HEAD_SPARSE | tcd.FLAG_ROOT_GEMM)
+    pt, pl, ps = run(tcd.HEAD_SPARSE)
+    assert np.array_equal(rt, pt) and np.array_equal(rl, pl) and np.array_equal(rs, ps)
+    assert np.all(rs == 0)
+    # the decode with the flag: the same tokens and logits
+    buf = DecodeBuffers(w.max_steps, B, w.hidden, w.max_steps)
+    buf.load(hid_bits)
+    dt, dl, dn, ds = buf.run(ctx, w.k, head=tcd.HEAD_SPARSE | tcd.FLAG_ROOT_GEMM)
+    for b in range(B):
+        n = int(dn[b])
+        assert np.array_equal(dt[b, :n], rt[b, :n]) and np.array_equal(dl[b, :n], rl[b, :n])
+    # the flag on the second step: every sequence is away from a fresh root
+    ctx.reset(B, w.k)
+    ctx.step(hid[0], tok, lg, st, head=tcd.HEAD_SPARSE)
+    ctx.step(hid[1], tok, lg, st, head=tcd.HEAD_SPARSE | tcd.FLAG_ROOT_GEMM)
+    torch.cuda.synchronize()
+    assert np.all(st.cpu().numpy() == tcd.TC_ERR_BOUNDS)
+    assert np.all(tok.cpu().numpy() == -1)
     ctx.close()

@@ -840,7 +840,19 @@ tc_status step_impl(tc_ctx* c, const void* hidden, int32_t head, const tc_sampli
   DevGrammar* g = c->bound;
   if (!g || g->batch < 1) return TC_ERR_NOT_BOUND;
   DeviceGuard dg(c->device);
-  tc_status rc = check_head(c, head, g->batch);
+  const bool root_gemm = (head & TC_FLAG_ROOT_GEMM) != 0;
+  if (root_gemm) {
+    head &= ~TC_FLAG_ROOT_GEMM;
+    if (head != TC_HEAD_SPARSE || sp || u) {
+      set_error_message("tc_step: TC_FLAG_ROOT_GEMM with the greedy sparse head only");
+      return TC_ERR_UNSUPPORTED;
+    }
+    if (g->n_root == 0) {
+      set_error_message("TC_FLAG_ROOT_GEMM: the grammar's root has a control edge or an edge without pointers");
+      return TC_ERR_UNSUPPORTED;
+    }
+  }
+  tc_status rc = check_head(c, root_gemm ? TC_HEAD_UNION_GEMM : head, g->batch);
   if (rc != TC_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rc = ensure_const(c, g, s);
@@ -861,7 +873,8 @@ tc_status step_impl(tc_ctx* c, const void* hidden, int32_t head, const tc_sampli
     p.smp_tok = c->d_smp_tok;
     p.smp_edge = c->d_smp_edge;
   }
-  TC_CUDA(launch_any_step(c, g, p, head, s, false));
+  if (root_gemm) TC_CUDA(launch_root(c, g, p, s));
+  else TC_CUDA(launch_any_step(c, g, p, head, s, false));
   return TC_OK;
 }
 
