@@ -285,11 +285,9 @@ __device__ __forceinline__ int32_t edge_live(const SeqLive& L, int e, const int4
 
 // Legality of one edge of the current node (see the filter below); `live`
 // receives the live count of a token edge.
-template <bool kConst>
-__device__ __forceinline__ bool edge_legal(const StepParams& p, const WalkRd<kConst>& w, const SeqLive& L,
-                                           int e, bool sep_ok, bool stop_ok, int4& ed, int32_t& live, int& bad) {
-  ed = w.edge(e);
-  const int32_t c = L.cnt ? L.cnt[e] : 0;  // count mode: issued together with the edge record
+// edge_rec_legal takes the edge's record (first half) already read.
+__device__ __forceinline__ bool edge_rec_legal(const StepParams& p, const SeqLive& L, int e, bool sep_ok,
+                                               bool stop_ok, const int4& ed, int32_t c, int32_t& live, int& bad) {
   live = 0;
   if (ed.x < 0 || ed.x >= p.V) {
     bad = 1;
@@ -307,6 +305,14 @@ __device__ __forceinline__ bool edge_legal(const StepParams& p, const WalkRd<kCo
   if (ed.y == -2) return stop_ok;
   bad = 1;
   return false;
+}
+
+template <bool kConst>
+__device__ __forceinline__ bool edge_legal(const StepParams& p, const WalkRd<kConst>& w, const SeqLive& L,
+                                           int e, bool sep_ok, bool stop_ok, int4& ed, int32_t& live, int& bad) {
+  ed = w.edge(e);
+  const int32_t c = L.cnt ? L.cnt[e] : 0;  // count mode: issued together with the edge record
+  return edge_rec_legal(p, L, e, sep_ok, stop_ok, ed, c, live, bad);
 }
 
 // A completed pointer leaves the live sets: count mode decrements the counts
@@ -450,6 +456,26 @@ __device__ __forceinline__ int warp_legal_set(const StepParams& p, const WalkRd<
   const int4 hd = e < end ? w.child_hdr(e) : make_int4(0, 0, -1, 0);  // issued with the first half
   int32_t c = 0;
   const bool legal = e < end && edge_legal<kConst>(p, w, L, e, sep_ok, stop_ok, ed, c, bad);
+  const unsigned bal = __ballot_sync(kFull, legal);
+  if (legal) out[__popc(bal & ((1u << lane) - 1u))] = Cand{make_int4(ed.x, e, ed.y, c), hd};
+  if (__ballot_sync(kFull, bad)) return -1;
+  return __popc(bal);
+}
+
+// warp_legal_set with this lane's edge record and child header (edge beg +
+// lane, when below end) already read; the read-only no-repeat state only (no
+// count array to read).
+__device__ __forceinline__ int warp_legal_set_rec(const StepParams& p, const SeqState& s, int b, int beg, int end,
+                                                  int pid, int lane, const int4& ed, const int4& hd, Cand* out) {
+  if (beg < 0 || end < beg || end > p.g.n_edges || end - beg > kPreMax) return -1;
+  int bad = pid >= p.g.n_strings;
+  const SeqLive L = seq_live<true>(p, s, b);
+  const bool ctl_ok = pid >= 0 && !bad && ptr_free(p, L, pid);
+  const bool sep_ok = ctl_ok && (s.emitted + 1 < s.k);
+  const bool stop_ok = ctl_ok && (s.emitted + 1 == s.k);
+  const int e = beg + lane;
+  int32_t c = 0;
+  const bool legal = e < end && edge_rec_legal(p, L, e, sep_ok, stop_ok, ed, 0, c, bad);
   const unsigned bal = __ballot_sync(kFull, legal);
   if (legal) out[__popc(bal & ((1u << lane) - 1u))] = Cand{make_int4(ed.x, e, ed.y, c), hd};
   if (__ballot_sync(kFull, bad)) return -1;
@@ -1136,8 +1162,21 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
   // alone: the first one's row loads start at once, before the hidden state is
   // read, and no barrier precedes the candidate loop.
   uint4 e[NCH > 0 ? NCH : 1];  // the row of the candidate in flight
+  // Lean steps with the read-only state: the first candidate's child edge
+  // records (lane i: edge i) are requested before its row, since the child
+  // legal set waits on them longer than the dot product waits on the row
+  // (A/B: B=1 +2 %, B=64 +4 %, B=256 +1.6 %; in the steps with forced
+  // continuations it cost 3.5 %, so only this instantiation does it).
+  int4 ped = make_int4(0, 0, 0, 0), phd = make_int4(0, 0, -1, 0);
   if constexpr (NCH > 0) {
     if (mode == 1 && pre && warp < s.pre_n - 1) {
+      if constexpr (kRO) {
+        const int e0 = pre0.h.x + lane;
+        if (pre0.a.z >= 0 && pre0.h.x >= 0 && e0 < pre0.h.y && pre0.h.y <= p.g.n_edges) {
+          phd = w.child_hdr(e0);
+          ped = w.edge(e0);
+        }
+      }
       const uint4* r0 = reinterpret_cast<const uint4*>(p.emb + (size_t)pre0.a.x * p.H);
 #pragma unroll
       for (int i = 0; i < NCH; ++i) e[i] = ld_row(r0 + i * 32 + lane);
@@ -1194,7 +1233,15 @@ __device__ __forceinline__ void step1_body(const StepParams& p, int b, const Seq
 #pragma unroll
             for (int i = 0; i < NCH; ++i) e[i] = ld_row(r4 + i * 32 + lane);
           }
-          const int sn = spec ? warp_legal_set<kConst, kRO>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]) : -1;
+          int sn = -1;
+          if (spec) {
+            if constexpr (kRO) {
+              sn = (pre && l == warp) ? warp_legal_set_rec(p, s, b, cb, ce, cpid, lane, ped, phd, sh.spec[l])
+                                      : warp_legal_set<kConst, kRO>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]);
+            } else {
+              sn = warp_legal_set<kConst, kRO>(p, w, s, b, cb, ce, cpid, lane, sh.spec[l]);
+            }
+          }
           if (lane == 0) sh.spec_n[l] = sn;
           __syncwarp();
           if constexpr (kXs) {
